@@ -1,0 +1,377 @@
+"""Pins for the fp64 oracle: checks against things other than the oracle itself.
+
+* brute force: contiguous (unpaged) attention with Python loops, math.exp and
+  no max-subtraction, and torch's fp64 scaled_dot_product_attention;
+* invariants: block-placement permutation, softmax weights sum to 1, shared
+  prefix blocks == private copies, split + log-sum-exp merge == unsplit;
+* special cases: one-token context returns V exactly, equal keys give mean(V),
+  GQA equals MHA with each KV head repeated g times;
+* number formats: every fp16 / bf16 bit pattern against torch's conversion;
+* page worked examples (tests/golden/*.json, each with its source);
+* planted mistakes: each mutation of the oracle below is caught by a pin.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def make_contiguous_case(seed, B=3, Hq=8, Hkv=2, D=16, lens=(1, 5, 23), dtype="fp16"):
+    """Contiguous per-sequence K/V [B][Hkv][Lmax][D] (bits) + q, as a model would
+    hold them before paging."""
+    g = torch.Generator().manual_seed(seed)
+    tdt = torch.float16 if dtype == "fp16" else torch.bfloat16
+    Lmax = max(lens)
+    K = torch.randn(B, Hkv, Lmax, D, generator=g).to(tdt)
+    V = torch.randn(B, Hkv, Lmax, D, generator=g).to(tdt)
+    q = torch.randn(B, Hq, D, generator=g).to(tdt)
+    return bits_of(q), bits_of(K), bits_of(V)
+
+
+def page_it(K_bits, V_bits, lens, block_size, num_blocks, rng):
+    """Scatter contiguous K/V into a paged pool with a random block placement;
+    unused slots hold NaN so any stray read shows."""
+    B, Hkv, _, D = K_bits.shape
+    nan_bits = np.uint16(0x7E00)
+    kc = np.full((num_blocks, Hkv, block_size, D), nan_bits, np.uint16)
+    vc = np.full_like(kc, nan_bits)
+    nblk = [-(-L // block_size) for L in lens]
+    perm = rng.permutation(num_blocks)
+    mb = max(max(nblk), 1)
+    tables = np.full((B, mb), -1, np.int32)
+    c = 0
+    for b, L in enumerate(lens):
+        for j in range(nblk[b]):
+            tables[b, j] = perm[c]
+            c += 1
+        for t in range(L):
+            blk, off = tables[b, t // block_size], t % block_size
+            kc[blk, :, off, :] = K_bits[b, :, t, :]
+            vc[blk, :, off, :] = V_bits[b, :, t, :]
+    return kc, vc, tables
+
+
+def brute_force(q_bits, K_bits, V_bits, lens, scale, dtype):
+    """Contiguous attention with plain Python loops: exp(s_t) / sum_u exp(s_u)."""
+    B, Hq, D = q_bits.shape
+    Hkv = K_bits.shape[1]
+    g = Hq // Hkv
+    q, K, V = (oracle.widen(x, dtype) for x in (q_bits, K_bits, V_bits))
+    out = np.zeros((B, Hq, D))
+    for b in range(B):
+        for h in range(Hq):
+            kv = h // g
+            L = lens[b]
+            if L == 0:
+                continue
+            s = [scale * math.fsum(q[b, h, d] * K[b, kv, t, d] for d in range(D)) for t in range(L)]
+            e = [math.exp(x) for x in s]
+            z = math.fsum(e)
+            for d in range(D):
+                out[b, h, d] = math.fsum(e[t] * V[b, kv, t, d] for t in range(L)) / z
+    return out
+
+
+def sdpa_reference(q_bits, K_bits, V_bits, lens, scale, dtype):
+    """torch fp64 scaled_dot_product_attention on each sequence's contiguous K/V."""
+    B, Hq, D = q_bits.shape
+    Hkv = K_bits.shape[1]
+    g = Hq // Hkv
+    q, K, V = (torch.from_numpy(oracle.widen(x, dtype)) for x in (q_bits, K_bits, V_bits))
+    out = torch.zeros(B, Hq, D, dtype=torch.float64)
+    for b in range(B):
+        L = lens[b]
+        if L == 0:
+            continue
+        Kb = K[b, :, :L].repeat_interleave(g, dim=0)   # [Hq][L][D]
+        Vb = V[b, :, :L].repeat_interleave(g, dim=0)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            q[b][:, None, :], Kb, Vb, scale=scale)
+        out[b] = o[:, 0, :]
+    return out.numpy()
+
+
+def paged_case(seed, lens=(1, 5, 23), dtype="fp16", Hq=8, Hkv=2, D=16, bs=4, spare=3):
+    q, K, V = make_contiguous_case(seed, B=len(lens), Hq=Hq, Hkv=Hkv, D=D, lens=lens, dtype=dtype)
+    nb = sum(-(-L // bs) for L in lens) + spare
+    kc, vc, tables = page_it(K, V, lens, bs, nb, np.random.default_rng(seed))
+    return q, K, V, kc, vc, tables
+
+
+# ------------------------------------------------------------------ number formats
+
+def test_widen_fp16_all_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.widen(bits, "fp16")
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.float16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    # closed forms from the binary16 definition
+    assert oracle.widen(np.array([0x3C00]), "fp16")[0] == 1.0
+    assert oracle.widen(np.array([0xC000]), "fp16")[0] == -2.0
+    assert oracle.widen(np.array([0x0001]), "fp16")[0] == 2.0 ** -24
+    assert oracle.widen(np.array([0x7BFF]), "fp16")[0] == 65504.0
+    assert oracle.widen(np.array([0x7C00]), "fp16")[0] == math.inf
+
+
+def test_widen_bf16_all_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.widen(bits, "bf16")
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert oracle.widen(np.array([0x3F80]), "bf16")[0] == 1.0
+    assert oracle.widen(np.array([0xC000]), "bf16")[0] == -2.0
+    assert oracle.widen(np.array([0x0001]), "bf16")[0] == 2.0 ** -133
+    assert oracle.widen(np.array([0x4049]), "bf16")[0] == 3.140625
+    assert oracle.widen(np.array([0xFF80]), "bf16")[0] == -math.inf
+
+
+# ------------------------------------------------------------------ attention vs brute force
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_paged_equals_bruteforce_contiguous(seed, dtype):
+    lens = (1, 5, 23)
+    q, K, V, kc, vc, tables = paged_case(seed, lens=lens, dtype=dtype)
+    scale = 1 / math.sqrt(16)
+    ours = oracle.decode_attention(q, kc, vc, tables, np.array(lens), scale, dtype, 4)
+    bf = brute_force(q, K, V, lens, scale, dtype)
+    assert np.abs(ours - bf).max() < 1e-13
+    ref = sdpa_reference(q, K, V, lens, scale, dtype)
+    assert np.abs(ours - ref).max() < 1e-12
+
+
+def test_gqa_groups_mha_and_mqa_bruteforce():
+    for Hq, Hkv in [(4, 4), (8, 1), (6, 3)]:
+        lens = (7, 2)
+        q, K, V, kc, vc, tables = paged_case(5, lens=lens, Hq=Hq, Hkv=Hkv, D=8, bs=2)
+        ours = oracle.decode_attention(q, kc, vc, tables, np.array(lens), 0.3, "fp16", 2)
+        assert np.abs(ours - brute_force(q, K, V, lens, 0.3, "fp16")).max() < 1e-13
+
+
+def test_scale_is_a_multiplier():
+    """scale = 1/sqrt(d) reproduces the listing's scores / sqrt(d_k)."""
+    lens = (9,)
+    q, K, V, kc, vc, tables = paged_case(3, lens=lens, Hq=2, Hkv=1, D=16)
+    ours = oracle.decode_attention(q, kc, vc, tables, np.array(lens), 0.25, "fp16", 4)
+    qd, Kd, Vd = (torch.from_numpy(oracle.widen(x, "fp16")) for x in (q, K, V))
+    scores = (qd[0] @ Kd[0, 0, :9].T) / math.sqrt(16)
+    ref = torch.softmax(scores, dim=-1) @ Vd[0, 0, :9]
+    assert np.abs(ours[0] - ref.numpy()).max() < 1e-13
+
+
+# ------------------------------------------------------------------ invariants
+
+def test_block_placement_permutation_is_invisible():
+    lens = (3, 16, 17, 33)
+    q, K, V, kc, vc, tables = paged_case(7, lens=lens, spare=6)
+    base = oracle.decode_attention(q, kc, vc, tables, np.array(lens), 0.2, "fp16", 4)
+    rng = np.random.default_rng(11)
+    for _ in range(3):
+        perm = rng.permutation(kc.shape[0])           # new home of each block
+        kc2 = np.empty_like(kc); vc2 = np.empty_like(vc)
+        kc2[perm] = kc; vc2[perm] = vc
+        t2 = np.where(tables >= 0, perm[np.maximum(tables, 0)], -1).astype(np.int32)
+        other = oracle.decode_attention(q, kc2, vc2, t2, np.array(lens), 0.2, "fp16", 4)
+        assert np.array_equal(base, other)
+
+
+def test_softmax_weights_sum_to_one():
+    rng = np.random.default_rng(0)
+    for L in (1, 2, 17, 1000):
+        K = rng.standard_normal((L, 32)); V = rng.standard_normal((L, 32)); q = rng.standard_normal(32)
+        _, p, lse = oracle.attend_one(q, K, V, 3.0)
+        assert abs(p.sum() - 1.0) < 1e-12
+        assert np.all(p >= 0)
+        s = 3.0 * K @ q
+        assert abs(lse - (s.max() + math.log(np.exp(s - s.max()).sum()))) < 1e-9
+
+
+def test_one_token_context_returns_v_exactly():
+    lens = (1, 1)
+    q, K, V, kc, vc, tables = paged_case(2, lens=lens)
+    out = oracle.decode_attention(q, kc, vc, tables, np.array(lens), 0.7, "fp16", 4)
+    Vd = oracle.widen(V, "fp16")
+    for b in range(2):
+        for h in range(8):
+            assert np.array_equal(out[b, h], Vd[b, h // 4, 0])
+
+
+def test_equal_keys_give_mean_of_v():
+    q, K, V, kc, vc, tables = paged_case(4, lens=(37,))
+    kc[:] = kc[tables[0, 0], :, 0:1, :]  # every slot gets the same key
+    out = oracle.decode_attention(q, kc, vc, tables, np.array([37]), 0.5, "fp16", 4)
+    Vd = oracle.widen(V, "fp16")
+    for h in range(8):
+        assert np.abs(out[0, h] - Vd[0, h // 4, :37].mean(axis=0)).max() < 1e-12
+
+
+def test_gqa_equals_mha_with_repeated_kv_heads():
+    lens = (6, 19)
+    q, K, V, kc, vc, tables = paged_case(8, lens=lens, Hq=8, Hkv=2)
+    gqa = oracle.decode_attention(q, kc, vc, tables, np.array(lens), 0.3, "fp16", 4)
+    mha = oracle.decode_attention(q, np.repeat(kc, 4, axis=1), np.repeat(vc, 4, axis=1),
+                                  tables, np.array(lens), 0.3, "fp16", 4)
+    assert np.array_equal(gqa, mha)
+
+
+def test_split_merge_identity():
+    rng = np.random.default_rng(1)
+    for L, split in [(1, 4), (33, 8), (100, 7), (512, 512), (513, 512)]:
+        K = rng.standard_normal((L, 16)); V = rng.standard_normal((L, 16)); q = rng.standard_normal(16)
+        whole = oracle.attend_one(q, K, V, 0.9)[0]
+        merged = oracle.lse_merge(oracle.split_partials(q, K, V, 0.9, split))
+        assert np.abs(whole - merged).max() < 1e-12
+    # an empty split carries zero weight
+    parts = [(np.ones(4), 0.5), (np.zeros(4), -math.inf)]
+    assert np.array_equal(oracle.lse_merge(parts), np.ones(4))
+
+
+def test_shared_prefix_equals_private_copies():
+    bs = 4
+    q, K, V = make_contiguous_case(9, B=3, lens=(13, 13, 13))
+    K[1, :, :8] = K[0, :, :8]; V[1, :, :8] = V[0, :, :8]   # 8-token shared prefix
+    K[2, :, :8] = K[0, :, :8]; V[2, :, :8] = V[0, :, :8]
+    kc, vc, private = page_it(K, V, (13, 13, 13), bs, 16, np.random.default_rng(0))
+    shared = private.copy()
+    shared[1, :2] = private[0, :2]
+    shared[2, :2] = private[0, :2]
+    a = oracle.decode_attention(q, kc, vc, private, np.array([13] * 3), 0.25, "fp16", bs)
+    b = oracle.decode_attention(q, kc, vc, shared, np.array([13] * 3), 0.25, "fp16", bs)
+    assert np.array_equal(a, b)
+
+
+def test_empty_context_gives_zeros():
+    q, K, V, kc, vc, tables = paged_case(1, lens=(0, 3))
+    out = oracle.decode_attention(q, kc, vc, tables, np.array([0, 3]), 0.25, "fp16", 4)
+    assert np.array_equal(out[0], np.zeros_like(out[0]))
+    assert np.all(np.isfinite(out))
+
+
+# ------------------------------------------------------------------ append
+
+def test_append_is_a_byte_permutation_and_matches_torch_cat():
+    """Appending token L-1 through the slot mapping, then attending, equals
+    torch.cat of the new K/V onto contiguous K/V (the pre-paging cache)."""
+    lens_before = (0, 4, 15, 16)
+    bs, Hq, Hkv, D = 4, 4, 2, 8
+    lens = tuple(L + 1 for L in lens_before)
+    q, K, V = make_contiguous_case(12, B=4, Hq=Hq, Hkv=Hkv, D=D, lens=lens)
+    nan = np.uint16(0x7E00)
+    Kold = K.copy(); Vold = V.copy()
+    for b, L in enumerate(lens_before):
+        Kold[b, :, L:] = nan; Vold[b, :, L:] = nan
+    kc, vc, tables = page_it(Kold, Vold, lens, bs, 12, np.random.default_rng(3))
+    slots = oracle.slot_mapping(tables, np.array(lens), bs)
+    k_new = np.stack([K[b, :, L] for b, L in enumerate(lens_before)])
+    v_new = np.stack([V[b, :, L] for b, L in enumerate(lens_before)])
+    kc2, vc2 = oracle.kv_append(kc, vc, k_new, v_new, slots, bs)
+    changed = np.argwhere(np.any(kc2 != kc, axis=(1, 3)))
+    assert sorted(map(tuple, changed)) == sorted((int(s) // bs, int(s) % bs) for s in slots)
+    out = oracle.decode_attention(q, kc2, vc2, tables, np.array(lens), 0.3, "fp16", bs)
+    assert np.abs(out - brute_force(q, K, V, lens, 0.3, "fp16")).max() < 1e-13
+    # negative slot -> nothing stored
+    kc3, _ = oracle.kv_append(kc, vc, k_new, v_new, np.full(4, -1, np.int32), bs)
+    assert np.array_equal(kc3, kc)
+
+
+def test_slot_mapping_on_page_block_tables(golden_dir):
+    gold = json.load(open(os.path.join(golden_dir, "block_tables.json")))
+    bs = gold["block_size"]
+    for page in ("kasblo", "youngju"):
+        for req, table in gold[page]["tables"].items():
+            row = np.array(table, np.int32)
+            for pos, slot in zip(gold[page]["positions"][req], gold[page]["slots"][req]):
+                assert oracle.slot_of_position(row, pos, bs) == slot
+    tables = np.array([[7, 1, 9], [3, 8, -1]], np.int32)
+    assert list(oracle.slot_mapping(tables, np.array([48, 20]), bs)) == [159, 131]
+    assert list(oracle.slot_mapping(tables, np.array([0, 1]), bs)) == [-1, 48]
+
+
+# ------------------------------------------------------------------ accounting vs the pages
+
+def test_kv_accounting_worked_examples(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "kv_accounting.json")))
+    w = g["kasblo_worked_example"]
+    m = oracle.kv_bytes_per_token(w["layers"], w["kv_heads"], w["head_dim"], w["elem_bytes"])
+    assert m == w["m_token_bytes"]
+    assert w["block_size"] * m == w["block_bytes"]
+    assert oracle.blocks_needed(w["tokens"], w["block_size"]) == w["n_blocks"]
+    assert w["tokens"] * m == w["token_bytes_formula"]
+    assert oracle.allocated_bytes(w["tokens"], w["block_size"], m) == w["alloc_bytes_formula"]
+    assert oracle.wasted_bytes(w["tokens"], w["block_size"], m) == w["waste_bytes_formula"]
+    # the page's table used the block size where the token size belongs (x16)
+    printed = w["printed_table_mib"]
+    mib = 2 ** 20
+    assert printed["tokens"] * mib == w["block_size"] * w["token_bytes_formula"]
+    assert printed["allocated"] * mib == w["block_size"] * w["alloc_bytes_formula"]
+    assert printed["unused_tail"] * mib == w["block_size"] * w["waste_bytes_formula"]
+    b = g["babushkai_llama3_70b"]
+    m70 = oracle.kv_bytes_per_token(b["layers"], b["kv_heads"], b["head_dim"], b["elem_bytes"])
+    assert m70 == b["m_token_kib"] * 1024
+    assert m70 * b["context_tokens"] == b["total_gib"] * 2 ** 30
+    s = g["scalingbook_llama2_13b"]
+    tot = oracle.kv_cache_bytes(s["tokens"], s["layers"], s["kv_heads"], s["head_dim"], 1, s["elem_bytes"])
+    assert round(tot / 1e9, 1) == s["approx_gb"]
+    # waste stays below one block for every length
+    for n in range(1, 200):
+        assert 0 <= oracle.wasted_bytes(n, 16, 1) < 16
+
+
+def test_roofline_step_time_printed_values(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "step_time.json")))
+    for batch, (total, per_stream) in g["printed"].items():
+        tps = oracle.decode_step_tokens_per_s(int(batch), g["ctx"], g["bandwidth"], g["compute"],
+                                              g["weight_bytes"], g["kv_bytes_per_token"], g["params"])
+        assert round(tps) == total
+        assert round(tps / int(batch), 1) == per_stream
+    ceiling = oracle.decode_step_tokens_per_s(1, 0, g["bandwidth"], g["compute"], g["weight_bytes"], 0, g["params"])
+    assert round(ceiling) == g["single_stream_ceiling_tok_s"]
+
+
+def test_attention_bytes_formula():
+    # 2 sequences of 10 and 6 tokens, Hkv=2, D=4, 2-byte values, Hq=4, 3 table entries read
+    n = oracle.attention_call_bytes([10, 6], 2, 4, 2, 4, 2, 3)
+    assert n == 16 * 2 * 4 * 2 * 2 + 2 * 2 * 4 * 4 * 2 + 12 + 8
+
+
+# ------------------------------------------------------------------ planted mistakes
+
+def _pins_pass():
+    """The brute-force and placement pins, as a function of the current oracle."""
+    lens = (1, 5, 23)
+    q, K, V, kc, vc, tables = paged_case(0, lens=lens)
+    ours = oracle.decode_attention(q, kc, vc, tables, np.array(lens), 0.25, "fp16", 4)
+    return np.all(np.isfinite(ours)) and np.abs(ours - brute_force(q, K, V, lens, 0.25, "fp16")).max() < 1e-13
+
+
+MUTATIONS = {
+    "kv head h % Hkv": ("kv_head_of", lambda h, g: h % 2),
+    "offset reversed in block": ("gather_kv", lambda c, row, L, kv, bs: c[np.asarray(row, np.int64)[np.arange(L) // bs], kv, bs - 1 - np.arange(L) % bs, :]),
+    "logical block not translated": ("gather_kv", lambda c, row, L, kv, bs: c[np.arange(L) // bs, kv, np.arange(L) % bs, :]),
+    "scale dropped": ("attend_one", lambda q, K, V, s, f=oracle.attend_one: f(q, K, V, 1.0)),
+    "last token dropped": ("gather_kv", lambda c, row, L, kv, bs, f=oracle.gather_kv: f(c, row, max(L - 1, 1), kv, bs)),
+    "K and V swapped": ("attend_one", lambda q, K, V, s, f=oracle.attend_one: f(q, V, K, s)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(monkeypatch, name):
+    assert _pins_pass()
+    attr, bad = MUTATIONS[name]
+    monkeypatch.setattr(oracle, attr, bad)
+    assert not _pins_pass()
