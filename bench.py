@@ -1,0 +1,484 @@
+#!/usr/bin/env python
+"""Decode-step benchmark for the paged KV cache.
+
+One step = the per-token KV append plus paged decode attention (and the split
+merge when the context is split) for a whole batch, on inputs resident in HBM.
+Metric: achieved HBM GB/s of the step's algorithmic bytes, with decode steps/s.
+
+Algorithmic bytes of one attention call (the spec formula):
+    sum_b L_b * Hkv * D * 2 * sizeof(T)      K and V of every cached token
+  + 2 * B * Hq * D * sizeof(T)               q read, out written
+  + 4 * sum_b ceil(L_b / 16) + 4 * B          block-table entries used, context lengths
+and of one append: 2 * (2 * B * Hkv * D * sizeof(T)) + 4 * B (read + write of
+the new K/V rows, the slot mapping).
+
+    python bench.py [--config llama3_8b_b64] [--steps K] [--warmup W] [--splits 0]
+    python bench.py --impl reference      # the fp64 oracle on the host cores
+
+Under torchrun each rank runs its own batch (seed + rank): the path shards by
+sequence with no exchange, so scaling is weak and `value` sums all ranks' bytes
+over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "paged decode attention HBM GB/s (% of ~8 TB/s roofline); decode steps/sec"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 129 * 2 ** 20
+
+
+# ----------------------------------------------------------------------------- bytes model
+
+def attention_bytes(lens, batch, num_q_heads, num_kv_heads, head_dim, elem_bytes, block_size=16) -> int:
+    lens = np.asarray(lens, np.int64)
+    kv = int(lens.sum()) * num_kv_heads * head_dim * 2 * elem_bytes
+    q_out = 2 * batch * num_q_heads * head_dim * elem_bytes
+    tables = 4 * int(((lens + block_size - 1) // block_size).sum())
+    return kv + q_out + tables + 4 * batch
+
+
+def append_bytes(batch, num_kv_heads, head_dim, elem_bytes) -> int:
+    return 2 * (2 * batch * num_kv_heads * head_dim * elem_bytes) + 4 * batch
+
+
+def unique_kv_bytes(w) -> int:
+    """K+V bytes of distinct physical blocks read (shared prefix blocks once)."""
+    s = w.spec
+    n_tok = 0
+    seen = set()
+    for b in range(s.batch):
+        L = int(w.context_lens[b])
+        for j in range(-(-L // s.block_size)):
+            blk = int(w.block_tables[b, j])
+            if blk in seen:
+                continue
+            seen.add(blk)
+            n_tok += min(s.block_size, L - j * s.block_size)
+    return n_tok * s.num_kv_heads * s.head_dim * 2 * 2
+
+
+# ----------------------------------------------------------------------------- environment
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "paged_kv_cache_26_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary of this
+    workload, if it was captured from the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_bytes = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not (m_hash and m_bytes) or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        ident = str(device_index)
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", ident], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 8:
+                continue
+            try:
+                self.samples.append((time.time(), float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        window = [s for s in self.samples if t0 - 0.15 <= s[0] <= t1 + 0.15] or self.samples
+        if not window:
+            return None
+        reasons = sorted({name for s in window for name, v in zip(self.REASONS, s[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(s[1] for s in window), "sm_max_mhz": max(s[2] for s in window),
+                "reasons": reasons, "samples": len(window)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def host_sample(w, seqs, layer=0):
+    """Host copies (16-bit patterns) of q and of the K/V blocks the listed
+    sequences use, with their block tables renumbered into the copy."""
+    s = w.spec
+    blocks = sorted({int(x) for b in seqs for x in w.block_tables[b, :-(-int(w.context_lens[b]) // s.block_size)]})
+    remap = {blk: i for i, blk in enumerate(blocks)}
+    idx = torch.tensor(blocks, dtype=torch.long, device=w.k_cache[layer].device)
+
+    def bits(t):
+        return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+    kc = bits(w.k_cache[layer].index_select(0, idx)) if blocks else np.zeros((0,), np.uint16)
+    vc = bits(w.v_cache[layer].index_select(0, idx)) if blocks else np.zeros((0,), np.uint16)
+    tables = np.full((len(seqs), w.block_tables.shape[1]), -1, np.int32)
+    for i, b in enumerate(seqs):
+        n = -(-int(w.context_lens[b]) // s.block_size)
+        tables[i, :n] = [remap[int(x)] for x in w.block_tables[b, :n]]
+    q = bits(w.q[layer][list(seqs)])
+    return q, kc, vc, tables, w.context_lens[list(seqs)]
+
+
+def oracle_rows_timed(w, sample, rows):
+    import oracle
+    q, kc, vc, tables, lens = sample
+    t0 = time.perf_counter()
+    oracle.decode_attention_rows(q, kc, vc, tables, lens, w.scale, w.spec.dtype, w.spec.block_size, rows)
+    return time.perf_counter() - t0
+
+
+def row_bytes(w, lens_rows) -> int:
+    """Algorithmic bytes of attention for individual (sequence, query head)
+    rows: each row's share of its KV head's K/V, plus its q and out."""
+    s = w.spec
+    g = s.group
+    return sum(int(L) * s.head_dim * 2 * 2 / g + 2 * s.head_dim * 2 for L in lens_rows)
+
+
+def cpu_baseline(w, budget_s: float):
+    """The oracle, as it stands, over the batch's first sequences (all query
+    heads) until about budget_s seconds of single-threaded CPU work."""
+    s = w.spec
+    spent, done_bytes, seqs_done = 0.0, 0.0, 0
+    for b in range(s.batch):
+        sample = host_sample(w, [b])
+        rows = [(0, h) for h in range(s.num_q_heads)]
+        spent += oracle_rows_timed(w, sample, rows)
+        done_bytes += row_bytes(w, [w.context_lens[b]] * s.num_q_heads)
+        seqs_done += 1
+        if spent >= budget_s:
+            break
+    return {"value": done_bytes / spent / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {seqs_done} of {s.batch} sequences, all {s.num_q_heads} query heads, layer 0; "
+                      f"{spent:.1f} s of numpy fp64 on one host thread"}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local):
+    import paged_kv_cache_26_gb300 as pkv
+    from paged_kv_cache_26_gb300 import build as pkv_build
+    from paged_kv_cache_26_gb300._native import PkvDims, PkvStepBuffers, lib
+
+    pkv_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    spec = wl.CONFIGS[args.config]
+    layers = spec.num_layers if args.layers is None else args.layers
+    w = wl.generate(spec, seed=args.seed + rank, device=dev, layers=layers)
+    s = w.spec
+    nl = len(w.q)
+    elem = 2
+    L = lib()
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+
+    slots_np = pkv.paged_kv_slot_mapping(w.block_tables, w.context_lens, s.block_size)
+    slots = torch.from_numpy(slots_np).to(dev)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    outs = [torch.empty_like(q) for q in w.q]
+    dims = PkvDims(num_seqs=s.batch, num_q_heads=s.num_q_heads, num_kv_heads=s.num_kv_heads, head_dim=s.head_dim,
+                   block_size=s.block_size, num_blocks=w.num_blocks, max_blocks_per_seq=w.max_blocks,
+                   dtype=0 if s.dtype == "fp16" else 1)
+    splits = int(L.paged_decode_resolve_splits(ctypes.byref(dims), args.splits))
+    ws_bytes = int(L.paged_decode_workspace_bytes(ctypes.byref(dims), args.splits))
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    P = ctypes.c_void_p
+    scale = ctypes.c_float(w.scale)
+    append_args = [(P(w.k_new[l].data_ptr()), P(w.v_new[l].data_ptr()), P(slots.data_ptr()), s.batch,
+                    P(w.k_cache[l].data_ptr()), P(w.v_cache[l].data_ptr()), ctypes.byref(dims), sp) for l in range(nl)]
+    attn_args = [(P(w.q[l].data_ptr()), P(w.k_cache[l].data_ptr()), P(w.v_cache[l].data_ptr()), P(bt.data_ptr()),
+                  P(cl.data_ptr()), scale, P(outs[l].data_ptr()), args.splits, P(ws.data_ptr()), ws_bytes,
+                  ctypes.byref(dims), sp) for l in range(nl)]
+    f_append, f_attn = L.paged_kv_append, L.paged_decode_attention
+
+    def step(ev=None):
+        for l in range(nl):
+            if f_append(*append_args[l]):
+                raise RuntimeError(L.paged_kv_last_error().decode())
+            if ev is not None:
+                ev[0].record(stream)
+            if f_attn(*attn_args[l]):
+                raise RuntimeError(L.paged_kv_last_error().decode())
+            if ev is not None:
+                ev[1].record(stream)
+
+    K, W = args.steps, args.warmup
+    sampler = ClockSampler(local) if rank == 0 else None
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    pkv.paged_kv_check_status(stream)
+
+    # ---- timed region: exactly K steps
+    n_ev = K * nl
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(stream)
+    i = 0
+    for _ in range(K):
+        for l in range(nl):
+            f_append(*append_args[l])
+            ev_a[i].record(stream)
+            f_attn(*attn_args[l])
+            ev_b[i].record(stream)
+            i += 1
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    pkv.paged_kv_check_status(stream)
+    elapsed_ms = start.elapsed_time(end)
+    attn_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
+    clocks = sampler.stop(t_wall0, t_wall1) if sampler else None
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+
+    attn_b = attention_bytes(w.context_lens, s.batch, s.num_q_heads, s.num_kv_heads, s.head_dim, elem) * nl
+    app_b = append_bytes(s.batch, s.num_kv_heads, s.head_dim, elem) * nl
+    step_bytes = attn_b + app_b
+    ms_per_step = elapsed_ms / K
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = load_peaks()
+    attn_avg_s = statistics.mean(attn_ms) * 1e-3
+    achieved = (attn_b / nl) / attn_avg_s / 1e9
+    launches_per_attn = 1 + (1 if splits > 1 else 0)
+
+    # ---- end to end through the C ABI from pinned host buffers
+    h = {"q": w.q[0].cpu(), "k_new": w.k_new[0].cpu(), "v_new": w.v_new[0].cpu(),
+         "slot_mapping": torch.from_numpy(slots_np), "block_tables": torch.from_numpy(w.block_tables),
+         "context_lens": torch.from_numpy(w.context_lens), "out": torch.empty_like(w.q[0], device="cpu")}
+    h = {k: v.contiguous().pin_memory() for k, v in h.items()}
+    dstage = [{"q": w.q[l], "k_new": w.k_new[l], "v_new": w.v_new[l], "slot_mapping": slots,
+               "block_tables": bt, "context_lens": cl, "out": outs[l]} for l in range(nl)]
+    keys = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens", "out")
+    e2e_args = []
+    for l in range(nl):
+        bufs = PkvStepBuffers(**{f"{k}_host": h[k].data_ptr() for k in keys},
+                              **{f"{k}_dev": dstage[l][k].data_ptr() for k in keys})
+        e2e_args.append((bufs, P(w.k_cache[l].data_ptr()), P(w.v_cache[l].data_ptr()), scale, args.splits,
+                         P(ws.data_ptr()), ws_bytes, ctypes.byref(dims), sp))
+    f_e2e = L.paged_decode_step_from_host
+    for _ in range(min(W, 10)):
+        for a in e2e_args:
+            f_e2e(ctypes.byref(a[0]), *a[1:])
+    torch.cuda.synchronize()
+    K_e2e = K
+    barrier(world)
+    start.record(stream)
+    for _ in range(K_e2e):
+        for a in e2e_args:
+            if f_e2e(ctypes.byref(a[0]), *a[1:]):
+                raise RuntimeError(L.paged_kv_last_error().decode())
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    pkv.paged_kv_check_status(stream)
+    e2e_ms = max_over_ranks(start.elapsed_time(end), world, dev) / K_e2e
+    h2d = sum(h[k].numel() * h[k].element_size() for k in keys if k != "out") * nl
+    d2h = h["out"].numel() * h["out"].element_size() * nl
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": s.dtype, "data": "synthetic (seeded N(0,1) values, scattered block placement)",
+        "config": {"workload": s.name, "batch": s.batch, "num_q_heads": s.num_q_heads,
+                   "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size,
+                   "layers_per_step": nl, "context_tokens": int(w.context_lens.sum()),
+                   "num_blocks": w.num_blocks, "num_splits": splits,
+                   "l2": f"no flush: each call streams {attn_b / nl / 2**20:.0f} MiB of K/V, "
+                         f"{attn_b / nl / L2_BYTES:.1f}x the 129 MiB L2",
+                   "step": "KV append + paged decode attention" + (" + split merge" if splits > 1 else "")},
+        "steps_per_s": round(1e3 / ms_per_step, 2),
+        "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (decode_kernel"
+                     + (" + merge_kernel)" if splits > 1 else ")"),
+                     "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic(s.name),
+                     "bytes_per_launch": attn_b // nl, "avg_launch_us": round(attn_avg_s * 1e6, 2)},
+        "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": K * nl * (1 + launches_per_attn),
+        "clocks": clocks,
+    }
+    if s.shared_prefix:
+        result["config"]["unique_kv_bytes_per_call"] = unique_kv_bytes(w)
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    """The fp64 oracle on the host cores, on this arm's workload.  Each step is
+    a bounded sample of (sequence, query head) rows, sized so that the whole
+    run stays within about args.ref_budget seconds."""
+    if rank != 0:
+        return
+    spec = wl.CONFIGS[args.config]
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    w = wl.generate(spec, seed=args.seed, device=device, layers=1)
+    s = w.spec
+    rng = np.random.default_rng(args.seed)
+    seqs = sorted(rng.choice(s.batch, size=min(4, s.batch), replace=False).tolist())
+    sample = host_sample(w, seqs)
+    all_rows = [(i, h) for i in range(len(seqs)) for h in range(s.num_q_heads)]
+    t_row = oracle_rows_timed(w, sample, all_rows[:4]) / 4
+    per_step = args.ref_budget / max(1, args.steps + args.warmup)
+    n_rows = int(min(len(all_rows), max(1, per_step / max(t_row, 1e-6))))
+    rows = all_rows[:n_rows]
+    lens_rows = [int(sample[4][i]) for i, _ in rows]
+    for _ in range(args.warmup):
+        oracle_rows_timed(w, sample, rows)
+    spent = sum(oracle_rows_timed(w, sample, rows) for _ in range(args.steps))
+    step_s = spent / args.steps
+    value = row_bytes(w, lens_rows) / step_s / 1e9
+    desc = (f"{n_rows} (sequence, query head) rows of sequences {seqs} per step, layer 0; "
+            f"numpy fp64 on one host thread")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) values, scattered block placement)",
+        "config": {"workload": s.name, "batch": s.batch, "num_q_heads": s.num_q_heads,
+                   "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="llama3_8b_b64", choices=sorted(wl.CONFIGS))
+    ap.add_argument("--splits", type=int, default=0, help="0 = automatic, 1 = single pass, n = n splits")
+    ap.add_argument("--layers", type=int, default=None, help="cap on layer caches (multi-layer configs)")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds of oracle work for --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

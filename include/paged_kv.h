@@ -1,0 +1,215 @@
+/*
+ * paged_kv.h -- C ABI of libpagedkv.so: single-token decode attention over a
+ * paged KV cache, the per-step slot-mapped KV append, and the host block
+ * allocator that produces block tables.  One GPU, sm_103a (GB300).
+ *
+ * The method (vLLM-style PagedAttention) is stated on these pages:
+ *  - kasblo.com "vLLMとは？LLMサーバーを高速化する仕組み", section
+ *    "PagedAttentionはKV Cacheをblockで管理する": logical blocks of a request
+ *    map to non-contiguous physical blocks through a per-request block table,
+ *    and the attention kernel reads K/V through that table;
+ *    section "blockはrequestの成長に合わせて割り当てる": blocks come from a pool,
+ *    one more is added when the current block fills, and they return to the
+ *    pool when the request ends; section "block共有とAutomatic Prefix Caching":
+ *    blocks carry a reference count and can be shared by several sequences.
+ *  - youngju.dev "LLM サービング最適化完全ガイド": the AttentionWithKVCache
+ *    listing (one new query token against all cached K/V:
+ *    softmax(Q K^T / sqrt(d_k)) V) and the PagedAttention memory-layout figure
+ *    (fixed 16-token physical blocks, virtual slot -> block table -> physical block).
+ *  - notes on "How to Scale Your Model, Part 7: Inference": section
+ *    "Transformer 推論の基礎: Prefill と Generation" (each generated token's K/V
+ *    is appended to the cache) and the GQA figure in section
+ *    "生成スループット/レイテンシ改善のテクニック" (groups of query heads share one KV head).
+ *
+ * Layouts (all row-major, T = fp16 or bf16 as given by pkv_dims.dtype):
+ *   k_cache, v_cache : T[num_blocks][num_kv_heads][block_size][head_dim]
+ *                      token slot s lives in block s / block_size at offset
+ *                      s % block_size.
+ *   q, out           : T[num_seqs][num_q_heads][head_dim]
+ *   k_new, v_new     : T[num_tokens][num_kv_heads][head_dim]
+ *   block_tables     : int32[num_seqs][max_blocks_per_seq]; entry j of row b is
+ *                      the physical block of sequence b's logical block j.
+ *                      Entries at or past ceil(context_lens[b] / block_size) are
+ *                      never read.
+ *   context_lens     : int32[num_seqs], tokens attended by each sequence
+ *                      (including the token appended this step).
+ * Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *
+ * Ownership: the caller allocates and owns every buffer.  Functions marked
+ * "device" take device pointers; the library allocates no device memory.
+ * Kernels run asynchronously on the given stream (a cudaStream_t passed as
+ * void*, NULL = the legacy default stream).  Argument errors are reported
+ * synchronously by the return value; errors found by the kernels themselves
+ * (an out-of-range block id or slot, a context longer than its table, a device
+ * wait that gave up) set a per-device error word that paged_kv_check_status()
+ * reads and clears.
+ *
+ * Every function returns PKV_OK (0) or a negative PKV_ERR_* code;
+ * paged_kv_last_error() gives a message for the calling thread's last failure.
+ */
+#ifndef PAGED_KV_H_
+#define PAGED_KV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = -1,   /* null/misaligned pointer, bad shape, Hkv does not divide Hq */
+  PKV_ERR_UNSUPPORTED = -2,   /* head_dim, block_size, group size or dtype not compiled in */
+  PKV_ERR_CUDA = -3,          /* a CUDA runtime call or launch failed (message kept) */
+  PKV_ERR_TIMEOUT = -4,       /* a kernel's bounded wait gave up */
+  PKV_ERR_NO_BLOCKS = -5,     /* block allocator has too few free blocks */
+  PKV_ERR_OUT_OF_RANGE = -6,  /* a kernel met a block id, slot or length outside its buffers */
+  PKV_ERR_SHARED_BLOCK = -7   /* a write would land in a block other sequences share */
+};
+
+enum { PKV_DTYPE_FP16 = 0, PKV_DTYPE_BF16 = 1 };
+
+typedef struct pkv_dims {
+  int32_t num_seqs;            /* batch size B (also num_tokens for the append) */
+  int32_t num_q_heads;         /* Hq */
+  int32_t num_kv_heads;        /* Hkv; must divide Hq */
+  int32_t head_dim;            /* D: 64 or 128 */
+  int32_t block_size;          /* tokens per physical block: 16 */
+  int32_t num_blocks;          /* physical blocks in each of k_cache / v_cache */
+  int32_t max_blocks_per_seq;  /* width of block_tables */
+  int32_t dtype;               /* PKV_DTYPE_FP16 or PKV_DTYPE_BF16 */
+} pkv_dims;
+
+/*
+ * KV append (device).  For each token i in [0, num_tokens) with
+ * slot_mapping[i] >= 0, copies k_new[i][:][:] into k_cache at slot
+ * slot_mapping[i] (block slot / block_size, offset slot % block_size, every KV
+ * head) and v_new[i] into v_cache likewise.  A negative slot skips the token.
+ * Bit-exact copy.  Uses dims->num_kv_heads, head_dim, block_size, num_blocks,
+ * dtype.  A slot >= num_blocks * block_size is skipped and flagged
+ * (PKV_ERR_OUT_OF_RANGE from paged_kv_check_status).  All value pointers must
+ * be 16-byte aligned.
+ */
+int paged_kv_append(const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                    int32_t num_tokens, void* k_cache, void* v_cache,
+                    const pkv_dims* dims, void* stream);
+
+/*
+ * Paged decode attention (device).  For every sequence b and query head h,
+ *   out[b][h] = sum_t softmax_t(scale * q[b][h] . K_t) V_t,  t in [0, context_lens[b]),
+ * where K_t / V_t is token t of sequence b for KV head h / g, read from
+ * physical block block_tables[b][t / block_size] at offset t % block_size.
+ * Softmax and accumulation run in fp32 (online softmax); out is rounded once
+ * to T.  context_lens[b] == 0 gives an all-zero row.
+ *
+ * num_splits: 1 = one pass per (sequence, KV head); n > 1 = each sequence is
+ * cut into splits of ceil(max_blocks_per_seq / n) blocks, each split writes a
+ * normalised fp32 partial and its log-sum-exp into the workspace, and a merge
+ * kernel combines them; 0 = choose automatically.  The workspace (device) must
+ * hold paged_decode_workspace_bytes(dims, num_splits) bytes and be 16-byte
+ * aligned; it may be NULL when that size is 0.  Concurrent calls must not
+ * share a workspace.
+ *
+ * Requirements: head_dim 64 or 128, block_size 16, 1 <= Hq/Hkv <= 8,
+ * caches and q/out 16-byte aligned, num_blocks * num_kv_heads * 16 < 2^31.
+ * A block id outside [0, num_blocks) reads zeros and is flagged; a context
+ * longer than max_blocks_per_seq * block_size is clamped and flagged.
+ */
+int paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int32_t* context_lens,
+                           float scale, void* out, int32_t num_splits,
+                           void* workspace, size_t workspace_bytes,
+                           const pkv_dims* dims, void* stream);
+
+/* The split count paged_decode_attention will use for this num_splits
+ * argument (resolves 0 = automatic).  Returns >= 1, or a PKV_ERR_* code. */
+int32_t paged_decode_resolve_splits(const pkv_dims* dims, int32_t num_splits);
+
+/* Workspace bytes paged_decode_attention needs for these dims and num_splits
+ * (0 when it runs in one pass). */
+size_t paged_decode_workspace_bytes(const pkv_dims* dims, int32_t num_splits);
+
+/*
+ * One whole decode step from host memory: copies q, k_new, v_new,
+ * slot_mapping, block_tables and context_lens from host buffers (pinned for
+ * asynchronous copies) into the caller's device staging buffers, runs the
+ * append and the attention on `stream`, and copies out back to out_host.
+ * The step is complete when the stream is.  num_tokens = dims->num_seqs.
+ */
+typedef struct pkv_step_buffers {
+  const void* q_host;  const void* k_new_host;  const void* v_new_host;
+  const int32_t* slot_mapping_host;  const int32_t* block_tables_host;
+  const int32_t* context_lens_host;  void* out_host;
+  void* q_dev;  void* k_new_dev;  void* v_new_dev;
+  int32_t* slot_mapping_dev;  int32_t* block_tables_dev;  int32_t* context_lens_dev;
+  void* out_dev;
+} pkv_step_buffers;
+
+int paged_decode_step_from_host(const pkv_step_buffers* bufs, void* k_cache, void* v_cache,
+                                float scale, int32_t num_splits,
+                                void* workspace, size_t workspace_bytes,
+                                const pkv_dims* dims, void* stream);
+
+/* Synchronises `stream`, then reads and clears this device's error word.
+ * Returns PKV_OK, PKV_ERR_OUT_OF_RANGE, PKV_ERR_TIMEOUT or PKV_ERR_CUDA. */
+int paged_kv_check_status(void* stream);
+
+/* Message for the calling thread's last non-OK return (never NULL). */
+const char* paged_kv_last_error(void);
+
+/* Host helper: slot of each sequence's newest token,
+ * slot_mapping[b] = block_tables[b][(L-1) / block_size] * block_size + (L-1) % block_size
+ * with L = context_lens[b]; -1 when L == 0.  Host pointers. */
+int paged_kv_slot_mapping(const int32_t* block_tables, const int32_t* context_lens,
+                          int32_t num_seqs, int32_t max_blocks, int32_t block_size,
+                          int32_t* slot_mapping);
+
+/* ------------------------------------------------------------------------
+ * Host block allocator (no device memory).  A pool of num_blocks physical
+ * blocks of block_size tokens.  Free blocks are handed out in a seeded random
+ * order so that a sequence's blocks are scattered through the pool.  Each
+ * block has a reference count; a sequence may share whole leading blocks of
+ * another (a common prefix).  Not thread-safe: one allocator per thread.
+ * ---------------------------------------------------------------------- */
+typedef struct pkv_block_allocator pkv_block_allocator;
+
+/* Returns NULL if num_blocks <= 0 or block_size <= 0. */
+pkv_block_allocator* block_allocator_create(int32_t num_blocks, int32_t block_size, uint64_t seed);
+void block_allocator_destroy(pkv_block_allocator* a);
+
+/* New sequence holding num_tokens tokens: ceil(num_tokens / block_size) blocks.
+ * PKV_ERR_NO_BLOCKS (and no change) if the pool is short. */
+int block_allocator_add_seq(pkv_block_allocator* a, int32_t num_tokens, int32_t* seq_id);
+
+/* New sequence of num_tokens tokens whose first prefix_tokens tokens are the
+ * blocks of src_seq (reference counts raised, nothing copied).  prefix_tokens
+ * must be a multiple of block_size and <= the length of src_seq. */
+int block_allocator_fork_prefix(pkv_block_allocator* a, int32_t src_seq, int32_t prefix_tokens,
+                                int32_t num_tokens, int32_t* seq_id);
+
+/* Grow seq_id by one token and return its slot (block * block_size + offset).
+ * Takes a new block when the last one is full.  PKV_ERR_SHARED_BLOCK if the
+ * token would land in a partly filled block that another sequence shares. */
+int block_allocator_append_slot(pkv_block_allocator* a, int32_t seq_id, int32_t* slot);
+
+/* Drop seq_id; blocks whose count reaches zero return to the pool. */
+int block_allocator_free_seq(pkv_block_allocator* a, int32_t seq_id);
+
+/* Export rows for seq_ids[0..n): tables int32[n][max_blocks] (-1 padded) and
+ * context_lens int32[n].  PKV_ERR_INVALID_ARG if a sequence needs more than
+ * max_blocks blocks. */
+int block_allocator_block_tables(const pkv_block_allocator* a, const int32_t* seq_ids, int32_t n,
+                                 int32_t max_blocks, int32_t* tables, int32_t* context_lens);
+
+int32_t block_allocator_num_free(const pkv_block_allocator* a);
+/* Reference count of a physical block (0 = free); -1 if out of range. */
+int32_t block_allocator_refcount(const pkv_block_allocator* a, int32_t block);
+/* Tokens held by a live sequence; -1 if seq_id is not live. */
+int32_t block_allocator_seq_len(const pkv_block_allocator* a, int32_t seq_id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_H_ */

@@ -1,0 +1,219 @@
+"""Python binding of libpagedkv.so: the same calls as the C ABI, taking torch
+tensors.  Only argument marshalling happens here; every step of the decode
+path runs in the library's CUDA kernels (or, for the allocator and slot
+mapping, its host C++)."""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from ._native import PkvDims, PkvStepBuffers, c_int32_p, lib
+
+PKV_OK = 0
+ERROR_NAMES = {
+    -1: "PKV_ERR_INVALID_ARG", -2: "PKV_ERR_UNSUPPORTED", -3: "PKV_ERR_CUDA", -4: "PKV_ERR_TIMEOUT",
+    -5: "PKV_ERR_NO_BLOCKS", -6: "PKV_ERR_OUT_OF_RANGE", -7: "PKV_ERR_SHARED_BLOCK",
+}
+_DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1}
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        msg = lib().paged_kv_last_error().decode(errors="replace")
+        super().__init__(f"{where}: {ERROR_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+def _check(code: int, where: str) -> int:
+    if code < 0:
+        raise PagedKVError(code, where)
+    return code
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need_cuda(name: str, t: torch.Tensor, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def make_dims(q_or_new: torch.Tensor, k_cache: torch.Tensor, block_tables: Optional[torch.Tensor] = None,
+              num_q_heads: Optional[int] = None) -> PkvDims:
+    nb, hkv, bs, d = k_cache.shape
+    if k_cache.dtype not in _DTYPE_CODE:
+        raise ValueError("caches must be float16 or bfloat16")
+    return PkvDims(num_seqs=q_or_new.shape[0],
+                   num_q_heads=num_q_heads if num_q_heads is not None else q_or_new.shape[1],
+                   num_kv_heads=hkv, head_dim=d, block_size=bs, num_blocks=nb,
+                   max_blocks_per_seq=block_tables.shape[1] if block_tables is not None else 0,
+                   dtype=_DTYPE_CODE[k_cache.dtype])
+
+
+def paged_kv_append(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                    k_cache: torch.Tensor, v_cache: torch.Tensor, stream=None) -> None:
+    """Store token i's K/V (k_new[i], v_new[i]: [Hkv][D]) at slot slot_mapping[i]
+    of the paged caches ([NB][Hkv][16][D]); negative slots are skipped."""
+    for n, t in (("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need_cuda(n, t, k_cache.dtype)
+    _need_cuda("slot_mapping", slot_mapping, torch.int32)
+    if k_new.shape != v_new.shape or k_new.shape[1:] != (k_cache.shape[1], k_cache.shape[3]):
+        raise ValueError("k_new / v_new must be [num_tokens][num_kv_heads][head_dim] matching the cache")
+    if k_cache.shape != v_cache.shape or slot_mapping.shape != (k_new.shape[0],):
+        raise ValueError("cache shapes differ or slot_mapping is not [num_tokens]")
+    dims = make_dims(k_new, k_cache, num_q_heads=k_cache.shape[1])
+    _check(lib().paged_kv_append(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), k_new.shape[0],
+                                 _ptr(k_cache), _ptr(v_cache), ctypes.byref(dims), _stream(stream)),
+           "paged_kv_append")
+
+
+def paged_decode_resolve_splits(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
+                                num_splits: int = 0) -> int:
+    dims = make_dims(q, k_cache, block_tables)
+    return _check(lib().paged_decode_resolve_splits(ctypes.byref(dims), num_splits), "paged_decode_resolve_splits")
+
+
+def paged_decode_workspace_bytes(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
+                                 num_splits: int = 0) -> int:
+    dims = make_dims(q, k_cache, block_tables)
+    return int(lib().paged_decode_workspace_bytes(ctypes.byref(dims), num_splits))
+
+
+def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                           out: Optional[torch.Tensor] = None, num_splits: int = 0,
+                           workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out[b][h] = softmax(scale * q[b][h] K^T) V over the first context_lens[b]
+    tokens of sequence b, K/V read through block_tables.  Returns out."""
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need_cuda(n, t, k_cache.dtype)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda("out", out, q.dtype)
+    if out.shape != q.shape or q.dim() != 3 or q.shape[2] != k_cache.shape[3]:
+        raise ValueError("q / out must be [num_seqs][num_q_heads][head_dim]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != q.shape[0] or context_lens.shape != (q.shape[0],):
+        raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
+    dims = make_dims(q, k_cache, block_tables)
+    need = int(lib().paged_decode_workspace_bytes(ctypes.byref(dims), num_splits))
+    if need and workspace is None:
+        # Caller did not supply one: allocate through torch (the library itself never allocates).
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().paged_decode_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                        _ptr(context_lens), float(scale), _ptr(out), num_splits,
+                                        _ptr(workspace), ws_bytes, ctypes.byref(dims), _stream(stream)),
+           "paged_decode_attention")
+    return out
+
+
+def paged_decode_step_from_host(host: dict, dev: dict, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                scale: float, num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+                                stream=None) -> None:
+    """One decode step from (pinned) host buffers: copies q, k_new, v_new,
+    slot_mapping, block_tables, context_lens into the device staging tensors in
+    ``dev``, runs append + attention, and copies out back into host['out'].
+    Keys of both dicts: q, k_new, v_new, slot_mapping, block_tables, context_lens, out."""
+    keys = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens", "out")
+    bufs = PkvStepBuffers(**{f"{k}_host": host[k].data_ptr() for k in keys},
+                          **{f"{k}_dev": dev[k].data_ptr() for k in keys})
+    dims = make_dims(dev["q"], k_cache, dev["block_tables"])
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().paged_decode_step_from_host(ctypes.byref(bufs), _ptr(k_cache), _ptr(v_cache), float(scale),
+                                             num_splits, _ptr(workspace), ws_bytes, ctypes.byref(dims),
+                                             _stream(stream)),
+           "paged_decode_step_from_host")
+
+
+def paged_kv_check_status(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel flagged an error."""
+    _check(lib().paged_kv_check_status(_stream(stream)), "paged_kv_check_status")
+
+
+def paged_kv_slot_mapping(block_tables: np.ndarray, context_lens: np.ndarray, block_size: int = 16) -> np.ndarray:
+    """Host: slot of each sequence's newest token (position context_len - 1)."""
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    out = np.empty(cl.shape[0], dtype=np.int32)
+    _check(lib().paged_kv_slot_mapping(bt.ctypes.data_as(c_int32_p), cl.ctypes.data_as(c_int32_p), cl.shape[0],
+                                       bt.shape[1] if bt.ndim == 2 else 0, block_size,
+                                       out.ctypes.data_as(c_int32_p)),
+           "paged_kv_slot_mapping")
+    return out
+
+
+class BlockAllocator:
+    """Host block pool: seeded scattered placement, reference counts, shared
+    prefixes and per-token growth (the C++ allocator behind the C ABI)."""
+
+    def __init__(self, num_blocks: int, block_size: int = 16, seed: int = 0):
+        self._h = lib().block_allocator_create(num_blocks, block_size, seed)
+        if not self._h:
+            raise PagedKVError(-1, "block_allocator_create")
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def close(self):
+        if self._h:
+            lib().block_allocator_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add_seq(self, num_tokens: int) -> int:
+        sid = ctypes.c_int32()
+        _check(lib().block_allocator_add_seq(self._h, num_tokens, ctypes.byref(sid)), "add_seq")
+        return sid.value
+
+    def fork_prefix(self, src_seq: int, prefix_tokens: int, num_tokens: int) -> int:
+        sid = ctypes.c_int32()
+        _check(lib().block_allocator_fork_prefix(self._h, src_seq, prefix_tokens, num_tokens, ctypes.byref(sid)),
+               "fork_prefix")
+        return sid.value
+
+    def append_slot(self, seq_id: int) -> int:
+        slot = ctypes.c_int32()
+        _check(lib().block_allocator_append_slot(self._h, seq_id, ctypes.byref(slot)), "append_slot")
+        return slot.value
+
+    def free_seq(self, seq_id: int) -> None:
+        _check(lib().block_allocator_free_seq(self._h, seq_id), "free_seq")
+
+    def block_tables(self, seq_ids: Sequence[int], max_blocks: int):
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+        tables = np.empty((ids.shape[0], max_blocks), dtype=np.int32)
+        lens = np.empty(ids.shape[0], dtype=np.int32)
+        _check(lib().block_allocator_block_tables(self._h, ids.ctypes.data_as(c_int32_p), ids.shape[0], max_blocks,
+                                                  tables.ctypes.data_as(c_int32_p), lens.ctypes.data_as(c_int32_p)),
+               "block_tables")
+        return tables, lens
+
+    @property
+    def num_free(self) -> int:
+        return int(lib().block_allocator_num_free(self._h))
+
+    def refcount(self, block: int) -> int:
+        return int(lib().block_allocator_refcount(self._h, block))
+
+    def seq_len(self, seq_id: int) -> int:
+        return int(lib().block_allocator_seq_len(self._h, seq_id))

@@ -1,0 +1,348 @@
+// C ABI of libpagedkv.so: argument validation, split selection, TMA tensor
+// maps and kernel launches.  The declarations and their contracts are in
+// include/paged_kv.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "paged_kv.h"
+#include "paged_kv_kernels.cuh"
+#include "pkv_errors.h"
+
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kStages = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kAutoSplitBlocks = 32;  // 512-token splits when splitting automatically
+constexpr int kMaxDevices = 64;
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return pkv_fail(PKV_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_dims(const pkv_dims* d, bool need_q_heads) {
+  if (!d) return pkv_fail(PKV_ERR_INVALID_ARG, "dims is NULL");
+  if (d->num_seqs < 0 || d->num_kv_heads <= 0 || d->num_blocks <= 0 || d->max_blocks_per_seq < 0)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "dims: negative or zero size");
+  if (d->dtype != PKV_DTYPE_FP16 && d->dtype != PKV_DTYPE_BF16)
+    return pkv_fail(PKV_ERR_UNSUPPORTED, "dims: dtype must be fp16 or bf16");
+  if (d->head_dim != 64 && d->head_dim != 128) return pkv_fail(PKV_ERR_UNSUPPORTED, "dims: head_dim must be 64 or 128");
+  if (d->block_size != pkv::kBlockSize) return pkv_fail(PKV_ERR_UNSUPPORTED, "dims: block_size must be 16");
+  if (static_cast<int64_t>(d->num_blocks) * d->num_kv_heads * pkv::kBlockSize >= (int64_t(1) << 31))
+    return pkv_fail(PKV_ERR_UNSUPPORTED, "dims: num_blocks * num_kv_heads * 16 must be < 2^31");
+  if (need_q_heads) {
+    if (d->num_q_heads <= 0 || d->num_q_heads % d->num_kv_heads != 0)
+      return pkv_fail(PKV_ERR_INVALID_ARG, "dims: num_kv_heads must divide num_q_heads");
+    if (d->num_q_heads / d->num_kv_heads > 8)
+      return pkv_fail(PKV_ERR_UNSUPPORTED, "dims: at most 8 query heads per KV head");
+  }
+  return PKV_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// The pool as a 2-D tensor: rows = num_blocks * Hkv * 16 of head_dim elements;
+// boxes of 16 rows x 64 elements (128 bytes) with the 128-byte swizzle.
+int make_cache_map(CUtensorMap* map, const void* cache, const pkv_dims* d) {
+  auto fn = encode_fn();
+  if (!fn) return pkv_fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d->head_dim),
+                              static_cast<cuuint64_t>(d->num_blocks) * d->num_kv_heads * pkv::kBlockSize};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d->head_dim) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(pkv::kBlockSize)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      d->dtype == PKV_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = fn(map, dt, 2, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return pkv_fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string(r) + ")");
+  return PKV_OK;
+}
+
+// Small cache of encoded maps keyed by (address, shape, dtype): a decode loop
+// reuses the same pool every step.
+struct MapCache {
+  struct Entry {
+    const void* ptr = nullptr;
+    int32_t nb = 0, hkv = 0, hd = 0, dt = -1;
+    CUtensorMap map;
+  };
+  static constexpr int kEntries = 16;
+  Entry e[kEntries];
+  int next = 0;
+  std::mutex mu;
+
+  int get(const void* ptr, const pkv_dims* d, CUtensorMap* out) {
+    std::lock_guard<std::mutex> lock(mu);
+    for (auto& x : e)
+      if (x.ptr == ptr && x.nb == d->num_blocks && x.hkv == d->num_kv_heads && x.hd == d->head_dim && x.dt == d->dtype) {
+        *out = x.map;
+        return PKV_OK;
+      }
+    Entry& n = e[next];
+    int rc = make_cache_map(&n.map, ptr, d);
+    if (rc != PKV_OK) return rc;
+    n.ptr = ptr;
+    n.nb = d->num_blocks;
+    n.hkv = d->num_kv_heads;
+    n.hd = d->head_dim;
+    n.dt = d->dtype;
+    next = (next + 1) % kEntries;
+    *out = n.map;
+    return PKV_OK;
+  }
+};
+MapCache g_maps;
+
+// ------------------------------------------------------------------ splits
+
+struct SplitPlan {
+  int32_t num_splits;
+  int32_t split_blocks;
+};
+
+int plan_splits(const pkv_dims* d, int32_t requested, SplitPlan* plan) {
+  if (requested < 0) return pkv_fail(PKV_ERR_INVALID_ARG, "num_splits must be >= 0");
+  const int32_t mb = d->max_blocks_per_seq;
+  if (mb <= 1) {
+    *plan = {1, mb > 0 ? mb : 1};
+    return PKV_OK;
+  }
+  int32_t n = requested == 0 ? (mb + kAutoSplitBlocks - 1) / kAutoSplitBlocks : requested;
+  if (n > mb) n = mb;
+  if (n < 1) n = 1;
+  const int32_t per = (mb + n - 1) / n;
+  *plan = {(mb + per - 1) / per, per};
+  return PKV_OK;
+}
+
+size_t workspace_for(const pkv_dims* d, const SplitPlan& p) {
+  if (p.num_splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(d->num_seqs) * d->num_q_heads * p.num_splits;
+  return rows * d->head_dim * sizeof(float) + rows * sizeof(float);
+}
+
+// ------------------------------------------------------------------ launches
+
+template <typename T, int D>
+int launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::DecodeArgs& args, const pkv_dims* d,
+                  cudaStream_t stream) {
+  using Shape = pkv::DecodeShape<D>;
+  constexpr int kSmem = kStages * Shape::kStageBytes + 1024;
+  auto kern = pkv::decode_kernel<T, D, kConsumerWarps, kStages>;
+  static bool configured[kMaxDevices] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < kMaxDevices && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_kernel)");
+    configured[dev] = true;
+  }
+  dim3 grid(args.num_splits, d->num_kv_heads, d->num_seqs);
+  kern<<<grid, kThreads, kSmem, stream>>>(mk, mv, args);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "decode_kernel launch");
+  if (args.num_splits > 1) {
+    const int rows = d->num_seqs * d->num_q_heads;
+    pkv::merge_kernel<T, D><<<(rows + 3) / 4, 128, 0, stream>>>(
+        args.o_part, args.lse_part, args.context_lens, static_cast<T*>(args.out), d->num_seqs, d->num_q_heads,
+        args.num_splits, args.split_blocks, args.max_blocks);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "merge_kernel launch");
+  }
+  return PKV_OK;
+}
+
+int decode_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                const int32_t* context_lens, float scale, void* out, int32_t num_splits, void* workspace,
+                size_t workspace_bytes, const pkv_dims* d, cudaStream_t stream) {
+  int rc = check_dims(d, true);
+  if (rc != PKV_OK) return rc;
+  if (d->num_seqs == 0) return PKV_OK;
+  if (d->max_blocks_per_seq <= 0) return pkv_fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be >= 1");
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "decode_attention: NULL pointer");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "decode_attention: misaligned pointer (q/out/caches need 16 bytes)");
+  if (!std::isfinite(scale)) return pkv_fail(PKV_ERR_INVALID_ARG, "decode_attention: scale is not finite");
+  SplitPlan plan;
+  rc = plan_splits(d, num_splits, &plan);
+  if (rc != PKV_OK) return rc;
+  const size_t need = workspace_for(d, plan);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "decode_attention: workspace missing, too small (" +
+                                             std::to_string(need) + " bytes needed) or misaligned");
+  CUtensorMap mk, mv;
+  if ((rc = g_maps.get(k_cache, d, &mk)) != PKV_OK) return rc;
+  if ((rc = g_maps.get(v_cache, d, &mv)) != PKV_OK) return rc;
+
+  pkv::DecodeArgs args;
+  args.q = q;
+  args.out = out;
+  const size_t rows = static_cast<size_t>(d->num_seqs) * d->num_q_heads * plan.num_splits;
+  args.o_part = need ? static_cast<float*>(workspace) : nullptr;
+  args.lse_part = need ? static_cast<float*>(workspace) + rows * d->head_dim : nullptr;
+  args.block_tables = block_tables;
+  args.context_lens = context_lens;
+  args.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  args.num_q_heads = d->num_q_heads;
+  args.num_kv_heads = d->num_kv_heads;
+  args.group = d->num_q_heads / d->num_kv_heads;
+  args.max_blocks = d->max_blocks_per_seq;
+  args.num_blocks = d->num_blocks;
+  args.num_splits = plan.num_splits;
+  args.split_blocks = plan.split_blocks;
+
+  const bool bf16 = d->dtype == PKV_DTYPE_BF16;
+  if (d->head_dim == 128)
+    return bf16 ? launch_decode<__nv_bfloat16, 128>(mk, mv, args, d, stream)
+                : launch_decode<__half, 128>(mk, mv, args, d, stream);
+  return bf16 ? launch_decode<__nv_bfloat16, 64>(mk, mv, args, d, stream)
+              : launch_decode<__half, 64>(mk, mv, args, d, stream);
+}
+
+int append_impl(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t num_tokens,
+                void* k_cache, void* v_cache, const pkv_dims* d, cudaStream_t stream) {
+  int rc = check_dims(d, false);
+  if (rc != PKV_OK) return rc;
+  if (num_tokens < 0) return pkv_fail(PKV_ERR_INVALID_ARG, "append: num_tokens < 0");
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "append: NULL pointer");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 4))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "append: misaligned pointer (values need 16 bytes)");
+  const int32_t chunks = d->head_dim * 2 / 16;
+  const int64_t total = static_cast<int64_t>(num_tokens) * d->num_kv_heads * chunks;
+  const int threads = 256;
+  const int64_t blocks64 = (total + threads - 1) / threads;
+  const int blocks = static_cast<int>(blocks64 < 65536 ? blocks64 : 65536);
+  pkv::append_kernel<<<blocks, threads, 0, stream>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, num_tokens, d->num_kv_heads,
+      chunks, static_cast<int64_t>(d->num_blocks) * pkv::kBlockSize, static_cast<uint4*>(k_cache),
+      static_cast<uint4*>(v_cache));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "append_kernel launch");
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int paged_kv_append(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t num_tokens,
+                    void* k_cache, void* v_cache, const pkv_dims* dims, void* stream) {
+  return append_impl(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache, dims,
+                     static_cast<cudaStream_t>(stream));
+}
+
+int paged_decode_attention(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                           const int32_t* context_lens, float scale, void* out, int32_t num_splits, void* workspace,
+                           size_t workspace_bytes, const pkv_dims* dims, void* stream) {
+  return decode_impl(q, k_cache, v_cache, block_tables, context_lens, scale, out, num_splits, workspace,
+                     workspace_bytes, dims, static_cast<cudaStream_t>(stream));
+}
+
+int32_t paged_decode_resolve_splits(const pkv_dims* dims, int32_t num_splits) {
+  int rc = check_dims(dims, true);
+  if (rc != PKV_OK) return rc;
+  SplitPlan p;
+  rc = plan_splits(dims, num_splits, &p);
+  return rc != PKV_OK ? rc : p.num_splits;
+}
+
+size_t paged_decode_workspace_bytes(const pkv_dims* dims, int32_t num_splits) {
+  if (check_dims(dims, true) != PKV_OK) return 0;
+  SplitPlan p;
+  if (plan_splits(dims, num_splits, &p) != PKV_OK) return 0;
+  return workspace_for(dims, p);
+}
+
+int paged_decode_step_from_host(const pkv_step_buffers* s, void* k_cache, void* v_cache, float scale,
+                                int32_t num_splits, void* workspace, size_t workspace_bytes, const pkv_dims* d,
+                                void* stream_v) {
+  int rc = check_dims(d, true);
+  if (rc != PKV_OK) return rc;
+  if (!s) return pkv_fail(PKV_ERR_INVALID_ARG, "step: buffers is NULL");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  const size_t elem = 2;
+  const size_t B = d->num_seqs;
+  const size_t q_bytes = B * d->num_q_heads * d->head_dim * elem;
+  const size_t kv_bytes = B * d->num_kv_heads * d->head_dim * elem;
+  const size_t tbl_bytes = B * d->max_blocks_per_seq * sizeof(int32_t);
+  struct Copy {
+    void* dst;
+    const void* src;
+    size_t n;
+  } h2d[] = {{s->q_dev, s->q_host, q_bytes},
+             {s->k_new_dev, s->k_new_host, kv_bytes},
+             {s->v_new_dev, s->v_new_host, kv_bytes},
+             {s->slot_mapping_dev, s->slot_mapping_host, B * sizeof(int32_t)},
+             {s->block_tables_dev, s->block_tables_host, tbl_bytes},
+             {s->context_lens_dev, s->context_lens_host, B * sizeof(int32_t)}};
+  for (const auto& c : h2d) {
+    if (c.n == 0) continue;
+    if (!c.dst || !c.src) return pkv_fail(PKV_ERR_INVALID_ARG, "step: NULL staging or host buffer");
+    cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "step: host-to-device copy");
+  }
+  rc = append_impl(s->k_new_dev, s->v_new_dev, s->slot_mapping_dev, d->num_seqs, k_cache, v_cache, d, stream);
+  if (rc != PKV_OK) return rc;
+  rc = decode_impl(s->q_dev, k_cache, v_cache, s->block_tables_dev, s->context_lens_dev, scale, s->out_dev,
+                   num_splits, workspace, workspace_bytes, d, stream);
+  if (rc != PKV_OK) return rc;
+  if (q_bytes) {
+    if (!s->out_host) return pkv_fail(PKV_ERR_INVALID_ARG, "step: out_host is NULL");
+    cudaError_t e = cudaMemcpyAsync(s->out_host, s->out_dev, q_bytes, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "step: device-to-host copy");
+  }
+  return PKV_OK;
+}
+
+int paged_kv_check_status(void* stream_v) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "check_status: stream synchronize");
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_pkv_error_word, sizeof(word));
+  if (e != cudaSuccess) return cuda_fail(e, "check_status: read error word");
+  if (word == 0) return PKV_OK;
+  const unsigned int zero = 0;
+  e = cudaMemcpyToSymbol(g_pkv_error_word, &zero, sizeof(zero));
+  if (e != cudaSuccess) return cuda_fail(e, "check_status: clear error word");
+  std::string msg = "kernel reported:";
+  if (word & pkv::kErrBlockId) msg += " block id out of range;";
+  if (word & pkv::kErrSlot) msg += " append slot out of range;";
+  if (word & pkv::kErrContext) msg += " context length out of range;";
+  if (word & pkv::kErrTimeout) msg += " a bounded wait gave up;";
+  return pkv_fail((word & pkv::kErrTimeout) ? PKV_ERR_TIMEOUT : PKV_ERR_OUT_OF_RANGE, msg);
+}
+
+const char* paged_kv_last_error(void) { return pkv_error_slot().c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,146 @@
+"""Host-side checks that need no GPU: the library builds for sm_103a, loads,
+exports every function include/paged_kv.h declares; the block allocator and
+the host slot mapping behave as the pages describe (compared with the oracle
+and the pages' block-table example)."""
+import ctypes
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_cache_26_gb300 import BlockAllocator, PagedKVError, paged_kv_slot_mapping
+from paged_kv_cache_26_gb300 import build as pkv_build
+from paged_kv_cache_26_gb300._native import EXPORTED
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    pkv_build.build()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "paged_kv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)) - {"if", "sizeof"})
+
+
+def test_library_exports_every_declared_function():
+    lib = ctypes.CDLL(pkv_build.LIB_PATH)
+    declared = header_functions()
+    assert len(declared) >= 17
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(declared) == set(EXPORTED)
+
+
+def test_library_is_built_for_sm_103a_only():
+    out = os.popen(f"cuobjdump --list-elf {pkv_build.LIB_PATH} 2>/dev/null").read()
+    if not out:
+        pytest.skip("cuobjdump unavailable")
+    arches = set(re.findall(r"sm_(\d+a?)", out))
+    assert arches == {"103a"}, arches
+
+
+def test_slot_mapping_matches_oracle_and_page_example(golden_dir):
+    gold = json.load(open(os.path.join(golden_dir, "block_tables.json")))
+    t = gold["kasblo"]["tables"]
+    tables = np.array([t["A"], t["B"] + [-1]], np.int32)
+    lens = np.array([48, 18], np.int32)
+    assert list(paged_kv_slot_mapping(tables, lens)) == list(oracle.slot_mapping(tables, lens, 16)) == [159, 129]
+    rng = np.random.default_rng(0)
+    for _ in range(20):
+        B, mb = 9, 7
+        tables = rng.integers(0, 500, size=(B, mb)).astype(np.int32)
+        lens = rng.integers(0, mb * 16 + 1, size=B).astype(np.int32)
+        assert np.array_equal(paged_kv_slot_mapping(tables, lens), oracle.slot_mapping(tables, lens, 16))
+
+
+def test_slot_mapping_rejects_bad_tables():
+    with pytest.raises(PagedKVError):
+        paged_kv_slot_mapping(np.array([[3, -1]], np.int32), np.array([20], np.int32))
+    with pytest.raises(PagedKVError):
+        paged_kv_slot_mapping(np.array([[3]], np.int32), np.array([17], np.int32))
+
+
+def test_allocator_lifecycle_and_scatter():
+    a = BlockAllocator(64, 16, seed=1)
+    s0 = a.add_seq(40)              # 3 blocks
+    s1 = a.add_seq(16)              # 1 block
+    assert a.num_free == 60
+    tables, lens = a.block_tables([s0, s1], 4)
+    assert list(lens) == [40, 16]
+    assert list(tables[1, 1:]) == [-1, -1, -1]
+    used = [int(x) for x in tables[tables >= 0]]
+    assert len(set(used)) == 4                                    # no double allocation
+    assert sorted(used) != list(range(min(used), min(used) + 4))  # scattered
+    # growth: positions 40..47 stay in block 2, position 48 opens block 3
+    slots = [a.append_slot(s0) for _ in range(9)]
+    t2, l2 = a.block_tables([s0], 4)
+    assert l2[0] == 49 and a.num_free == 59
+    for pos, slot in zip(range(40, 49), slots):
+        assert slot == oracle.slot_of_position(t2[0], pos, 16)
+    # s1 is full: the next token takes a fresh block
+    a.append_slot(s1)
+    assert a.num_free == 58
+    a.free_seq(s0)
+    assert a.num_free == 62
+    assert all(a.refcount(int(b)) == 0 for b in t2[0])
+    # freed blocks are reused
+    s2 = a.add_seq(62 * 16)
+    assert a.num_free == 0
+    with pytest.raises(PagedKVError) as e:
+        a.add_seq(1)
+    assert e.value.code == -5
+    a.free_seq(s2)
+    a.free_seq(s1)
+    assert a.num_free == 64
+
+
+def test_allocator_shared_prefix_refcounts():
+    a = BlockAllocator(100, 16, seed=3)
+    src = a.add_seq(513)
+    forks = [a.fork_prefix(src, 512, 600) for _ in range(3)]
+    t, _ = a.block_tables([src] + forks, 40)
+    for f in range(1, 4):
+        assert np.array_equal(t[f, :32], t[0, :32])
+        assert len(set(t[f, 32:38]) & set(t[0, :33])) == 0
+    assert all(a.refcount(int(b)) == 4 for b in t[0, :32])
+    assert a.refcount(int(t[0, 32])) == 1
+    a.free_seq(src)
+    assert all(a.refcount(int(b)) == 3 for b in t[0, :32])
+    for f in forks:
+        a.free_seq(f)
+    assert a.num_free == 100
+    with pytest.raises(PagedKVError):
+        a.fork_prefix(a.add_seq(20), 8, 30)      # prefix must be whole blocks
+
+
+def test_appends_after_a_fork_never_write_shared_blocks():
+    """Forks share whole blocks only, so every later append lands in a block
+    whose reference count is 1."""
+    a = BlockAllocator(40, 16, seed=0)
+    src = a.add_seq(48)
+    kids = [a.fork_prefix(src, 32, 32), a.fork_prefix(src, 48, 50), a.fork_prefix(src, 16, 16)]
+    shared = set(int(b) for b in a.block_tables([src], 3)[0][0])
+    for sid in [src] + kids:
+        for _ in range(20):
+            slot = a.append_slot(sid)
+            assert slot // 16 not in shared
+            assert a.refcount(slot // 16) == 1
+
+
+def test_allocator_waste_below_one_block():
+    a = BlockAllocator(4096, 16, seed=5)
+    rng = np.random.default_rng(2)
+    lens = rng.integers(1, 2000, size=50)
+    ids = [a.add_seq(int(L)) for L in lens]
+    t, l = a.block_tables(ids, 125)
+    for row, L in zip(t, l):
+        n = int((row >= 0).sum())
+        assert n == oracle.blocks_needed(int(L), 16)
+        assert 0 <= n * 16 - L < 16
