@@ -390,14 +390,15 @@ def run_ours(args, rank, world, local):
         "config": {"workload": s.name, "batch": s.batch, "num_q_heads": s.num_q_heads,
                    "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size,
                    "layers_per_step": nl, "context_tokens": int(w.context_lens.sum()),
-                   "num_blocks": w.num_blocks, "num_splits": splits,
+                   "num_blocks": w.num_blocks,
+                   "partition": "persistent, equal blocks per warp" if splits == 0 else f"{splits} splits",
                    "l2": f"no flush: each call streams {attn_b / nl / 2**20:.0f} MiB of K/V, "
                          f"{attn_b / nl / L2_BYTES:.1f}x the 129 MiB L2",
                    "step": "KV append + paged decode attention" + (" + split merge" if splits > 1 else "")},
         "steps_per_s": round(1e3 / ms_per_step, 2),
         "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (decode_kernel"
-                     + (" + merge_kernel)" if splits > 1 else ")"),
+        "roofline": {"bound": "hbm", "kernel": "decode_persistent_kernel" if splits == 0 else
+                     "decode_split_kernel" + (" + merge_split_kernel" if splits > 1 else ""),
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": ncu_traffic(s.name),
                      "bytes_per_launch": attn_b // nl, "avg_launch_us": round(attn_avg_s * 1e6, 2)},

@@ -103,13 +103,19 @@ int paged_kv_append(const void* k_new, const void* v_new, const int32_t* slot_ma
  * Softmax and accumulation run in fp32 (online softmax); out is rounded once
  * to T.  context_lens[b] == 0 gives an all-zero row.
  *
- * num_splits: 1 = one pass per (sequence, KV head); n > 1 = each sequence is
- * cut into splits of ceil(max_blocks_per_seq / n) blocks, each split writes a
+ * num_splits: 0 = automatic: when num_seqs <= 2048 a persistent kernel (one
+ * CTA per SM) cuts the batch's (sequence, KV head, block) space into equal
+ * contiguous ranges, one per warp, whatever the length mix, and merges a
+ * sequence cut across warps in the same launch; larger batches use 512-token
+ * splits.  1 = one pass per (sequence, KV head).  n > 1 = each sequence is cut
+ * into splits of ceil(max_blocks_per_seq / n) blocks, each split writes a
  * normalised fp32 partial and its log-sum-exp into the workspace, and a merge
- * kernel combines them; 0 = choose automatically.  The workspace (device) must
- * hold paged_decode_workspace_bytes(dims, num_splits) bytes and be 16-byte
- * aligned; it may be NULL when that size is 0.  Concurrent calls must not
- * share a workspace.
+ * kernel combines them.
+ * The workspace (device) must hold paged_decode_workspace_bytes(dims,
+ * num_splits) bytes, be 256-byte aligned, and be zero-filled before its first
+ * use (and again after a call that reported an error); the kernels leave the
+ * counters in it at zero.  It may be NULL when that size is 0.  Calls that share
+ * a workspace must not run concurrently.
  *
  * Requirements: head_dim 64 or 128, block_size 16, 1 <= Hq/Hkv <= 8,
  * caches and q/out 16-byte aligned, num_blocks * num_kv_heads * 16 < 2^31.
@@ -123,7 +129,8 @@ int paged_decode_attention(const void* q, const void* k_cache, const void* v_cac
                            const pkv_dims* dims, void* stream);
 
 /* The split count paged_decode_attention will use for this num_splits
- * argument (resolves 0 = automatic).  Returns >= 1, or a PKV_ERR_* code. */
+ * argument: 0 for the persistent balanced kernel, >= 1 for the split kernel,
+ * or a PKV_ERR_* code. */
 int32_t paged_decode_resolve_splits(const pkv_dims* dims, int32_t num_splits);
 
 /* Workspace bytes paged_decode_attention needs for these dims and num_splits

@@ -93,6 +93,13 @@ def paged_decode_workspace_bytes(q: torch.Tensor, k_cache: torch.Tensor, block_t
     return int(lib().paged_decode_workspace_bytes(ctypes.byref(dims), num_splits))
 
 
+def make_workspace(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
+                   num_splits: int = 0) -> Optional[torch.Tensor]:
+    """A zero-filled workspace of the size paged_decode_attention needs (None if none)."""
+    need = paged_decode_workspace_bytes(q, k_cache, block_tables, num_splits)
+    return torch.zeros(need, dtype=torch.uint8, device=q.device) if need else None
+
+
 def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                            block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
                            out: Optional[torch.Tensor] = None, num_splits: int = 0,
@@ -113,8 +120,9 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     dims = make_dims(q, k_cache, block_tables)
     need = int(lib().paged_decode_workspace_bytes(ctypes.byref(dims), num_splits))
     if need and workspace is None:
-        # Caller did not supply one: allocate through torch (the library itself never allocates).
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        # Caller did not supply one: allocate through torch (the library itself
+        # never allocates).  Zero-filled: the kernels expect zeroed counters.
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().paged_decode_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                         _ptr(context_lens), float(scale), _ptr(out), num_splits,

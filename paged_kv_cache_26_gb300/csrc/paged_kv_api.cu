@@ -17,11 +17,27 @@
 
 namespace {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kStages = 8;
+constexpr int kConsumerWarps = 4;   // split kernel
+constexpr int kStages = 8;          // split kernel ring depth
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kAutoSplitBlocks = 32;  // 512-token splits when splitting automatically
+constexpr int kAutoSplitBlocks = 32;  // 512-token splits when the split path is chosen automatically
+constexpr int kMaxPersistentSeqs = 2048;  // prefix sums of the persistent kernel live in shared memory
 constexpr int kMaxDevices = 64;
+
+int device_sms() {
+  static int sms[kMaxDevices] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= kMaxDevices) dev = kMaxDevices - 1;
+  if (sms[dev] == 0) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    sms[dev] = v > 0 ? v : 1;
+  }
+  return sms[dev];
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 int cuda_fail(cudaError_t e, const char* what) {
   return pkv_fail(PKV_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
@@ -121,58 +137,108 @@ MapCache g_maps;
 // ------------------------------------------------------------------ splits
 
 struct SplitPlan {
-  int32_t num_splits;
-  int32_t split_blocks;
+  bool persistent;        // balanced persistent kernel (no fixed split)
+  int32_t num_splits;     // split kernel: splits per sequence
+  int32_t split_blocks;   // split kernel: blocks per split
 };
+
+bool persistent_eligible(const pkv_dims* d) {
+  return d->num_seqs <= kMaxPersistentSeqs &&
+         static_cast<int64_t>(d->num_seqs) * d->num_kv_heads * d->max_blocks_per_seq < (int64_t(1) << 31);
+}
 
 int plan_splits(const pkv_dims* d, int32_t requested, SplitPlan* plan) {
   if (requested < 0) return pkv_fail(PKV_ERR_INVALID_ARG, "num_splits must be >= 0");
   const int32_t mb = d->max_blocks_per_seq;
+  if (requested == 0 && persistent_eligible(d)) {
+    *plan = {true, 0, 0};
+    return PKV_OK;
+  }
   if (mb <= 1) {
-    *plan = {1, mb > 0 ? mb : 1};
+    *plan = {false, 1, mb > 0 ? mb : 1};
     return PKV_OK;
   }
   int32_t n = requested == 0 ? (mb + kAutoSplitBlocks - 1) / kAutoSplitBlocks : requested;
   if (n > mb) n = mb;
   if (n < 1) n = 1;
   const int32_t per = (mb + n - 1) / n;
-  *plan = {(mb + per - 1) / per, per};
+  *plan = {false, (mb + per - 1) / per, per};
   return PKV_OK;
 }
 
-size_t workspace_for(const pkv_dims* d, const SplitPlan& p) {
-  if (p.num_splits <= 1) return 0;
-  const size_t rows = static_cast<size_t>(d->num_seqs) * d->num_q_heads * p.num_splits;
-  return rows * d->head_dim * sizeof(float) + rows * sizeof(float);
+// Workspace regions: [partial outputs][partial log-sum-exps][unit counters].
+struct WorkspaceLayout {
+  size_t o_bytes = 0, lse_bytes = 0, cnt_bytes = 0;
+  size_t total() const { return o_bytes + lse_bytes + cnt_bytes; }
+};
+
+WorkspaceLayout workspace_layout(const pkv_dims* d, const SplitPlan& p) {
+  WorkspaceLayout w;
+  if (p.persistent) {
+    const size_t warps = static_cast<size_t>(device_sms()) * pkv::PersistentShape<128>::kWarps;
+    w.o_bytes = align256(warps * 2 * pkv::kMaxGroup * d->head_dim * sizeof(float));
+    w.lse_bytes = align256(warps * 2 * pkv::kMaxGroup * sizeof(float));
+    w.cnt_bytes = align256(static_cast<size_t>(d->num_seqs) * d->num_kv_heads * sizeof(int32_t));
+  } else if (p.num_splits > 1) {
+    const size_t rows = static_cast<size_t>(d->num_seqs) * d->num_q_heads * p.num_splits;
+    w.o_bytes = align256(rows * d->head_dim * sizeof(float));
+    w.lse_bytes = align256(rows * sizeof(float));
+  }
+  return w;
 }
 
 // ------------------------------------------------------------------ launches
 
-template <typename T, int D>
-int launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::DecodeArgs& args, const pkv_dims* d,
-                  cudaStream_t stream) {
-  using Shape = pkv::DecodeShape<D>;
-  constexpr int kSmem = kStages * Shape::kStageBytes + 1024;
-  auto kern = pkv::decode_kernel<T, D, kConsumerWarps, kStages>;
-  static bool configured[kMaxDevices] = {};
+// Raise a kernel's dynamic shared-memory limit once per device (and ask for
+// the largest shared-memory carveout).  Kern is a distinct function per
+// template instantiation, so each kernel keeps its own flags.
+template <typename Kern>
+cudaError_t configure_smem(Kern kern, int bytes) {
+  static bool done[kMaxDevices] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < kMaxDevices && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_kernel)");
-    configured[dev] = true;
-  }
-  dim3 grid(args.num_splits, d->num_kv_heads, d->num_seqs);
-  kern<<<grid, kThreads, kSmem, stream>>>(mk, mv, args);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "decode_kernel launch");
-  if (args.num_splits > 1) {
-    const int rows = d->num_seqs * d->num_q_heads;
-    pkv::merge_kernel<T, D><<<(rows + 3) / 4, 128, 0, stream>>>(
-        args.o_part, args.lse_part, args.context_lens, static_cast<T*>(args.out), d->num_seqs, d->num_q_heads,
-        args.num_splits, args.split_blocks, args.max_blocks);
+  if (dev < kMaxDevices && done[dev]) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess && dev < kMaxDevices) done[dev] = true;
+  return e;
+}
+
+template <typename T, int D>
+int launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::DecodeArgs& args, const SplitPlan& plan,
+                  const pkv_dims* d, cudaStream_t stream) {
+  using Shape = pkv::TileShape<D>;
+  cudaError_t e;
+  if (plan.persistent) {
+    auto kern = pkv::decode_persistent_kernel<T, D>;
+    e = configure_smem(kern, static_cast<int>(pkv::persistent_smem_bytes<D>(kMaxPersistentSeqs)));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_persistent_kernel)");
+    const int64_t upper_blocks = static_cast<int64_t>(d->num_seqs) * d->num_kv_heads * d->max_blocks_per_seq;
+    int64_t grid = (upper_blocks + pkv::PersistentShape<D>::kWarps - 1) / pkv::PersistentShape<D>::kWarps;
+    if (grid > device_sms()) grid = device_sms();
+    if (grid < 1) grid = 1;
+    kern<<<static_cast<int>(grid), pkv::PersistentShape<D>::kWarps * 32, pkv::persistent_smem_bytes<D>(d->num_seqs),
+           stream>>>(mk, mv, args);
     e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "merge_kernel launch");
+    if (e != cudaSuccess) return cuda_fail(e, "decode_persistent_kernel launch");
+  } else {
+    constexpr int kSmem = kStages * Shape::kStageBytes + 1024;
+    auto kern = pkv::decode_split_kernel<T, D, kConsumerWarps, kStages>;
+    e = configure_smem(kern, kSmem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_split_kernel)");
+    dim3 grid(plan.num_splits, d->num_kv_heads, d->num_seqs);
+    kern<<<grid, kThreads, kSmem, stream>>>(mk, mv, args);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "decode_split_kernel launch");
+    if (plan.num_splits > 1) {
+      const int rows = d->num_seqs * d->num_q_heads;
+      pkv::merge_split_kernel<T, D><<<(rows + 3) / 4, 128, 0, stream>>>(
+          args.part_o, args.part_lse, args.context_lens, static_cast<T*>(args.out), d->num_seqs, d->num_q_heads,
+          plan.num_splits, plan.split_blocks, args.max_blocks);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return cuda_fail(e, "merge_split_kernel launch");
+    }
   }
   return PKV_OK;
 }
@@ -193,10 +259,11 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const i
   SplitPlan plan;
   rc = plan_splits(d, num_splits, &plan);
   if (rc != PKV_OK) return rc;
-  const size_t need = workspace_for(d, plan);
-  if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
+  const WorkspaceLayout wl = workspace_layout(d, plan);
+  const size_t need = wl.total();
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
     return pkv_fail(PKV_ERR_INVALID_ARG, "decode_attention: workspace missing, too small (" +
-                                             std::to_string(need) + " bytes needed) or misaligned");
+                                             std::to_string(need) + " bytes needed) or not 256-byte aligned");
   CUtensorMap mk, mv;
   if ((rc = g_maps.get(k_cache, d, &mk)) != PKV_OK) return rc;
   if ((rc = g_maps.get(v_cache, d, &mv)) != PKV_OK) return rc;
@@ -204,12 +271,14 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const i
   pkv::DecodeArgs args;
   args.q = q;
   args.out = out;
-  const size_t rows = static_cast<size_t>(d->num_seqs) * d->num_q_heads * plan.num_splits;
-  args.o_part = need ? static_cast<float*>(workspace) : nullptr;
-  args.lse_part = need ? static_cast<float*>(workspace) + rows * d->head_dim : nullptr;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  args.part_o = need ? reinterpret_cast<float*>(ws) : nullptr;
+  args.part_lse = need ? reinterpret_cast<float*>(ws + wl.o_bytes) : nullptr;
+  args.counters = wl.cnt_bytes ? reinterpret_cast<int32_t*>(ws + wl.o_bytes + wl.lse_bytes) : nullptr;
   args.block_tables = block_tables;
   args.context_lens = context_lens;
   args.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  args.num_seqs = d->num_seqs;
   args.num_q_heads = d->num_q_heads;
   args.num_kv_heads = d->num_kv_heads;
   args.group = d->num_q_heads / d->num_kv_heads;
@@ -220,10 +289,10 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const i
 
   const bool bf16 = d->dtype == PKV_DTYPE_BF16;
   if (d->head_dim == 128)
-    return bf16 ? launch_decode<__nv_bfloat16, 128>(mk, mv, args, d, stream)
-                : launch_decode<__half, 128>(mk, mv, args, d, stream);
-  return bf16 ? launch_decode<__nv_bfloat16, 64>(mk, mv, args, d, stream)
-              : launch_decode<__half, 64>(mk, mv, args, d, stream);
+    return bf16 ? launch_decode<__nv_bfloat16, 128>(mk, mv, args, plan, d, stream)
+                : launch_decode<__half, 128>(mk, mv, args, plan, d, stream);
+  return bf16 ? launch_decode<__nv_bfloat16, 64>(mk, mv, args, plan, d, stream)
+              : launch_decode<__half, 64>(mk, mv, args, plan, d, stream);
 }
 
 int append_impl(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t num_tokens,
@@ -273,14 +342,14 @@ int32_t paged_decode_resolve_splits(const pkv_dims* dims, int32_t num_splits) {
   if (rc != PKV_OK) return rc;
   SplitPlan p;
   rc = plan_splits(dims, num_splits, &p);
-  return rc != PKV_OK ? rc : p.num_splits;
+  return rc != PKV_OK ? rc : (p.persistent ? 0 : p.num_splits);
 }
 
 size_t paged_decode_workspace_bytes(const pkv_dims* dims, int32_t num_splits) {
   if (check_dims(dims, true) != PKV_OK) return 0;
   SplitPlan p;
   if (plan_splits(dims, num_splits, &p) != PKV_OK) return 0;
-  return workspace_for(dims, p);
+  return workspace_layout(dims, p).total();
 }
 
 int paged_decode_step_from_host(const pkv_step_buffers* s, void* k_cache, void* v_cache, float scale,

@@ -163,7 +163,7 @@ def generate(spec: WorkloadSpec, seed: int = 0, device="cpu", layers: Optional[i
     if spec.pool[0] == "fixed":
         num_blocks = int(spec.pool[1])
     else:
-        num_blocks = int(math.ceil(spec.pool[1] * unique_needed))
+        num_blocks = max(1, int(math.ceil(spec.pool[1] * unique_needed)))
     assert num_blocks >= unique_needed, "pool too small for the batch"
 
     # Scattered physical placement: walk a seeded permutation of the pool.
