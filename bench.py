@@ -265,6 +265,8 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     spec = wl.CONFIGS[args.config]
+    if args.batch:
+        spec = spec.replace(name=f"{spec.name}_b{args.batch}", batch=args.batch)
     layers = spec.num_layers if args.layers is None else args.layers
     w = wl.generate(spec, seed=args.seed + rank, device=dev, layers=layers)
     s = w.spec
@@ -464,6 +466,7 @@ def main():
     ap.add_argument("--config", default="llama3_8b_b64", choices=sorted(wl.CONFIGS))
     ap.add_argument("--splits", type=int, default=0, help="0 = automatic, 1 = single pass, n = n splits")
     ap.add_argument("--layers", type=int, default=None, help="cap on layer caches (multi-layer configs)")
+    ap.add_argument("--batch", type=int, default=None, help="override the configuration's batch size")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds of oracle work for --impl reference")

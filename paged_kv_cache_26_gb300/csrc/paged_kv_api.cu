@@ -190,10 +190,10 @@ WorkspaceLayout workspace_layout(const pkv_dims* d, const SplitPlan& p) {
 // ------------------------------------------------------------------ launches
 
 // Raise a kernel's dynamic shared-memory limit once per device (and ask for
-// the largest shared-memory carveout).  Kern is a distinct function per
-// template instantiation, so each kernel keeps its own flags.
-template <typename Kern>
-cudaError_t configure_smem(Kern kern, int bytes) {
+// the largest shared-memory carveout).  The kernel is a template argument so
+// that every kernel instantiation keeps its own flags.
+template <auto kern>
+cudaError_t configure_smem(int bytes) {
   static bool done[kMaxDevices] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -211,8 +211,8 @@ int launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::Decod
   using Shape = pkv::TileShape<D>;
   cudaError_t e;
   if (plan.persistent) {
-    auto kern = pkv::decode_persistent_kernel<T, D>;
-    e = configure_smem(kern, static_cast<int>(pkv::persistent_smem_bytes<D>(kMaxPersistentSeqs)));
+    constexpr auto kern = pkv::decode_persistent_kernel<T, D>;
+    e = configure_smem<kern>(static_cast<int>(pkv::persistent_smem_bytes<D>(kMaxPersistentSeqs)));
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_persistent_kernel)");
     const int64_t upper_blocks = static_cast<int64_t>(d->num_seqs) * d->num_kv_heads * d->max_blocks_per_seq;
     int64_t grid = (upper_blocks + pkv::PersistentShape<D>::kWarps - 1) / pkv::PersistentShape<D>::kWarps;
@@ -224,8 +224,8 @@ int launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::Decod
     if (e != cudaSuccess) return cuda_fail(e, "decode_persistent_kernel launch");
   } else {
     constexpr int kSmem = kStages * Shape::kStageBytes + 1024;
-    auto kern = pkv::decode_split_kernel<T, D, kConsumerWarps, kStages>;
-    e = configure_smem(kern, kSmem);
+    constexpr auto kern = pkv::decode_split_kernel<T, D, kConsumerWarps, kStages>;
+    e = configure_smem<kern>(kSmem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_split_kernel)");
     dim3 grid(plan.num_splits, d->num_kv_heads, d->num_seqs);
     kern<<<grid, kThreads, kSmem, stream>>>(mk, mv, args);
@@ -249,8 +249,9 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const i
   int rc = check_dims(d, true);
   if (rc != PKV_OK) return rc;
   if (d->num_seqs == 0) return PKV_OK;
-  if (d->max_blocks_per_seq <= 0) return pkv_fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be >= 1");
-  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+  // A zero-width table means every context is empty (contexts are clamped to
+  // the table): the table pointer is then never read.
+  if (!q || !k_cache || !v_cache || (!block_tables && d->max_blocks_per_seq > 0) || !context_lens || !out)
     return pkv_fail(PKV_ERR_INVALID_ARG, "decode_attention: NULL pointer");
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
       !aligned(block_tables, 4) || !aligned(context_lens, 4))

@@ -190,11 +190,20 @@ def test_shared_prefix_blocks_equal_private_copies():
 
 def test_single_pass_and_splits_agree():
     w = wl.generate(wl.LLAMA3_8B.replace(batch=8), seed=4)
+    rk, rv = oracle_caches(w)
+    ref = oracle_rows(w, rk, rv, [(b, h) for b in range(8) for h in range(32)]).reshape(8, 32, -1)
     one = widen_out(run_gpu_step(w, 0, 1)[0], "bf16")
+    assert_close(one, ref, "single pass")
     for n in (0, 2, 8, 256):
         many = widen_out(run_gpu_step(w, 0, n)[0], "bf16")
-        # within one bf16 rounding step of each other
-        assert np.all(np.abs(one - many) <= 2 ** -7 * np.maximum(np.abs(one), np.abs(many)) + 1e-6)
+        assert_close(many, ref, f"{n} splits")
+        # Each partition rounds its softmax weights to bf16 relative to its own
+        # running max and rounds the output once more: two partitions differ
+        # by a few bf16 steps of the output, far inside the oracle tolerance.
+        diff = np.abs(one - many)
+        bound = 2 ** -6 * np.maximum(np.abs(one), np.abs(many)) + 2 ** -11
+        k = np.unravel_index(np.argmax(diff - bound), diff.shape)
+        assert diff[k] <= bound[k], f"splits={n}: at {k} one={one[k]} many={many[k]} ref={ref[k]}"
 
 
 def test_gqa_equals_mha_with_repeated_heads():
