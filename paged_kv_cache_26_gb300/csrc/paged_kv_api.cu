@@ -166,19 +166,25 @@ int plan_splits(const pkv_dims* d, int32_t requested, SplitPlan* plan) {
   return PKV_OK;
 }
 
-// Workspace regions: [partial outputs][partial log-sum-exps][unit counters].
+// Workspace regions: [partial outputs][partial log-sum-exps][block prefix][scheduler counters].
 struct WorkspaceLayout {
-  size_t o_bytes = 0, lse_bytes = 0, cnt_bytes = 0;
-  size_t total() const { return o_bytes + lse_bytes + cnt_bytes; }
+  size_t o_bytes = 0, lse_bytes = 0, plan_bytes = 0, sched_bytes = 0;
+  size_t total() const { return o_bytes + lse_bytes + plan_bytes + sched_bytes; }
 };
+
+// Segments of the persistent partition for the largest grid (one CTA per SM).
+size_t persistent_segments() {
+  return static_cast<size_t>(device_sms()) * pkv::PersistentShape<128>::kWarps * (1 + pkv::Partition::kTailChunks);
+}
 
 WorkspaceLayout workspace_layout(const pkv_dims* d, const SplitPlan& p) {
   WorkspaceLayout w;
   if (p.persistent) {
-    const size_t warps = static_cast<size_t>(device_sms()) * pkv::PersistentShape<128>::kWarps;
-    w.o_bytes = align256(warps * 2 * pkv::kMaxGroup * d->head_dim * sizeof(float));
-    w.lse_bytes = align256(warps * 2 * pkv::kMaxGroup * sizeof(float));
-    w.cnt_bytes = align256(static_cast<size_t>(d->num_seqs) * d->num_kv_heads * sizeof(int32_t));
+    const size_t seg = persistent_segments();
+    w.o_bytes = align256(seg * 2 * pkv::kMaxGroup * d->head_dim * sizeof(float));
+    w.lse_bytes = align256(seg * 2 * pkv::kMaxGroup * sizeof(float));
+    w.plan_bytes = align256((static_cast<size_t>(d->num_seqs) + 1) * sizeof(int32_t));
+    w.sched_bytes = 256;
   } else if (p.num_splits > 1) {
     const size_t rows = static_cast<size_t>(d->num_seqs) * d->num_q_heads * p.num_splits;
     w.o_bytes = align256(rows * d->head_dim * sizeof(float));
@@ -222,6 +228,22 @@ int launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::Decod
            stream>>>(mk, mv, args);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "decode_persistent_kernel launch");
+    // The merge is a programmatic dependent launch: its CTAs become resident
+    // while the decode kernel runs and wait in-kernel for it to finish.
+    const int rows = d->num_seqs * d->num_q_heads;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((rows + 3) / 4);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, pkv::merge_persistent_kernel<T, D>, args,
+                           static_cast<int32_t>(grid) * pkv::PersistentShape<D>::kWarps);
+    if (e != cudaSuccess) return cuda_fail(e, "merge_persistent_kernel launch");
   } else {
     constexpr int kSmem = kStages * Shape::kStageBytes + 1024;
     constexpr auto kern = pkv::decode_split_kernel<T, D, kConsumerWarps, kStages>;
@@ -275,7 +297,8 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const i
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   args.part_o = need ? reinterpret_cast<float*>(ws) : nullptr;
   args.part_lse = need ? reinterpret_cast<float*>(ws + wl.o_bytes) : nullptr;
-  args.counters = wl.cnt_bytes ? reinterpret_cast<int32_t*>(ws + wl.o_bytes + wl.lse_bytes) : nullptr;
+  args.plan = wl.plan_bytes ? reinterpret_cast<int32_t*>(ws + wl.o_bytes + wl.lse_bytes) : nullptr;
+  args.sched = wl.sched_bytes ? reinterpret_cast<int32_t*>(ws + wl.o_bytes + wl.lse_bytes + wl.plan_bytes) : nullptr;
   args.block_tables = block_tables;
   args.context_lens = context_lens;
   args.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);

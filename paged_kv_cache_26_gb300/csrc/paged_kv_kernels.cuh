@@ -7,10 +7,11 @@
 //                              appended to the cache).
 //  decode_persistent_kernel -- the automatic path.  One CTA per SM; the flattened
 //                              (sequence, KV head, block) space is cut into equal
-//                              contiguous ranges, one per warp, so every warp
-//                              streams the same number of K/V blocks whatever the
-//                              length mix.  A unit (sequence, KV head) cut across
-//                              warps is merged by the last warp to finish it.
+//                              shares, one per warp, whatever the length mix.  A
+//                              warp streams the head of its share, then claims
+//                              tail chunks of any share from a counter, so SMs
+//                              with more memory bandwidth take more work.
+//  merge_persistent_kernel  -- log-sum-exp merge of the units it left in pieces.
 //  decode_split_kernel      -- explicit sequence partitioning: one CTA per
 //                              (split, KV head, sequence), followed by
 //  merge_split_kernel       -- the log-sum-exp merge of the split partials.
@@ -229,9 +230,10 @@ struct DecodeArgs {
   void* out;                  // T[B][Hq][D]
   const int32_t* block_tables;
   const int32_t* context_lens;
-  float* part_o;              // split: f32[B][Hq][splits][D]; persistent: f32[warps][2][8][D]
-  float* part_lse;            // split: f32[B][Hq][splits];    persistent: f32[warps][2][8]
-  int32_t* counters;          // persistent: int32[B][Hkv], zero between calls
+  float* part_o;              // split: f32[B][Hq][splits][D]; persistent: f32[segments][2][8][D]
+  float* part_lse;            // split: f32[B][Hq][splits];    persistent: f32[segments][2][8]
+  int32_t* plan;              // persistent: int32[B+1] block prefix, written by the decode kernel
+  int32_t* sched;             // persistent: int32[2] chunk counter and finished-warp counter, zero between calls
   float scale_log2;           // scale * log2(e)
   int32_t num_seqs;
   int32_t num_q_heads;
@@ -291,6 +293,82 @@ constexpr size_t persistent_smem_bytes(int num_seqs) {
   return PersistentShape<D>::kRingBytes + (2 * static_cast<size_t>(num_seqs) + 1) * 4 + 1024;
 }
 
+// Work partition of the persistent kernel.  The flattened block space
+// [0, total) is cut into equal shares of R blocks, one per warp.  Each share
+// is a static head, processed by its own warp, followed by four tail chunks
+// (4/10, 3/10, 2/10, 1/10 of the tail).  Chunk k of share w is segment
+// nwarps + k * nwarps + w; warps claim chunks in that order from a counter
+// once their head is done, so SMs with more memory bandwidth take more of the
+// tails.  The head is 7/10 of a share, or all of it when shares are shorter
+// than kMinDynamicShare blocks (there the chunks would be too small to pay for
+// their hand-over).  Every segment is a contiguous block range; the decode and
+// merge kernels derive all boundaries from (total, nwarps) alone.
+struct Partition {
+  static constexpr int kTailChunks = 4;
+  static constexpr int kMinDynamicShare = 48;
+  int total, nwarps, R;
+
+  __device__ __forceinline__ Partition(int total_, int nwarps_)
+      : total(total_), nwarps(nwarps_), R(total_ > 0 ? (total_ + nwarps_ - 1) / nwarps_ : 1) {}
+  __device__ __forceinline__ static int cum(int k) { return k == 0 ? 0 : k == 1 ? 4 : k == 2 ? 7 : k == 3 ? 9 : 10; }
+  __device__ __forceinline__ void head(int w, int& s, int& e) const {
+    s = min(total, w * R);
+    const int len = min(total, (w + 1) * R) - s;
+    e = s + (R < kMinDynamicShare ? len : len * 7 / 10);
+  }
+  __device__ __forceinline__ void chunk(int k, int w, int& s, int& e) const {
+    int hs, he;
+    head(w, hs, he);
+    const int tail = min(total, (w + 1) * R) - he;
+    s = he + tail * cum(k) / 10;
+    e = he + tail * cum(k + 1) / 10;
+  }
+  __device__ __forceinline__ int num_chunks() const { return nwarps * kTailChunks; }
+  __device__ __forceinline__ int num_segments() const { return nwarps * (1 + kTailChunks); }
+  // Segment holding block p (0 <= p < total): its id and [s, e).
+  __device__ __forceinline__ int segment_of(int p, int& s, int& e) const {
+    const int w = p / R;
+    head(w, s, e);
+    if (p < e) return w;
+    for (int k = 0; k < kTailChunks; ++k) {
+      chunk(k, w, s, e);
+      if (p < e) return nwarps + k * nwarps + w;
+    }
+    return -1;  // unreachable for p < total
+  }
+};
+
+// Exclusive prefix of blocks per sequence into s_P[0..B] and clamped contexts
+// into s_ctx[0..B), computed by the whole CTA (nthreads threads).
+__device__ __forceinline__ void context_prefix(const DecodeArgs& a, int* s_P, int* s_ctx, int* s_warp_sum,
+                                               int nthreads, bool flag) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, B = a.num_seqs;
+  const int per = (B + nthreads - 1) / nthreads;
+  const int lo = min(B, tid * per), hi = min(B, lo + per);
+  int local = 0;
+  for (int b = lo; b < hi; ++b) {
+    const int ctx = clamped_context(a.context_lens, b, a.max_blocks, flag);
+    s_ctx[b] = ctx;
+    local += (ctx + kBlockSize - 1) / kBlockSize;
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_warp_sum[warp] = incl;
+  __syncthreads();
+  int run = incl - local;
+  for (int w = 0; w < warp; ++w) run += s_warp_sum[w];
+  for (int b = lo; b < hi; ++b) {
+    s_P[b] = run;
+    run += (s_ctx[b] + kBlockSize - 1) / kBlockSize;
+  }
+  if (tid == nthreads - 1) s_P[B] = run;
+  __syncthreads();
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
     decode_persistent_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
@@ -300,6 +378,7 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
   constexpr int SW = PersistentShape<D>::kStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[NW][SW];
+  __shared__ int4 s_desc[NW][SW];  // per stage: unit, block j, segment id, flags
   __shared__ int s_warp_sum[NW];
 
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -309,53 +388,18 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = a.num_seqs, Hkv = a.num_kv_heads, g = a.group;
 
-  // ---- context lengths and the exclusive prefix P[b] of blocks per sequence
-  {
-    const int per = (B + NW * 32 - 1) / (NW * 32);
-    const int lo = min(B, tid * per), hi = min(B, lo + per);
-    int local = 0;
-    for (int b = lo; b < hi; ++b) {
-      const int ctx = clamped_context(a.context_lens, b, a.max_blocks, blockIdx.x == 0);
-      s_ctx[b] = ctx;
-      local += (ctx + kBlockSize - 1) / kBlockSize;
-    }
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) s_warp_sum[warp] = incl;
-    if (lane == 0) {
-      for (int s = 0; s < SW; ++s) mbar_init(smem_u32(&full_bar[warp][s]), 1);
-      fence_mbar_init();
-    }
-    __syncthreads();
-    int run = incl - local;
-    for (int w = 0; w < warp; ++w) run += s_warp_sum[w];
-    for (int b = lo; b < hi; ++b) {
-      s_P[b] = run;
-      run += (s_ctx[b] + kBlockSize - 1) / kBlockSize;
-    }
-    if (tid == NW * 32 - 1) s_P[B] = run;
-    __syncthreads();
+  // The merge kernel may launch now; it waits for this grid to complete.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (lane == 0) {
+    for (int s = 0; s < SW; ++s) mbar_init(smem_u32(&full_bar[warp][s]), 1);
+    fence_mbar_init();
   }
+  context_prefix(a, s_P, s_ctx, s_warp_sum, NW * 32, blockIdx.x == 0);
+  if (blockIdx.x == 0)  // the merge kernel reads the prefix
+    for (int b = tid; b <= B; b += NW * 32) a.plan[b] = s_P[b];
 
-  // Empty contexts produce zero rows (CTA 0 writes them).
-  if (blockIdx.x == 0) {
-    for (int b = 0; b < B; ++b) {
-      if (s_ctx[b] != 0) continue;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(a.out) + static_cast<int64_t>(b) * a.num_q_heads * D);
-      for (int i = tid; i < a.num_q_heads * D / 8; i += NW * 32) dst[i] = make_uint4(0, 0, 0, 0);
-    }
-  }
-
-  const int total = Hkv * s_P[B];                       // blocks of all units
-  const int nwarps = gridDim.x * NW;
-  const int R = (total + nwarps - 1) / nwarps;          // blocks per warp
+  const Partition part(Hkv * s_P[B], gridDim.x * NW);
   const int gw = blockIdx.x * NW + warp;
-  const int start = min(total, gw * R);
-  const int n = min(total, start + R) - start;
 
   // Unit (b, kvh) and block j of flattened block f: units are ordered
   // (b, kvh) and unit (b, kvh) holds blocks [Hkv*P[b] + kvh*nb, +nb).
@@ -372,177 +416,273 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
     j = rem - kvh * nb;
   };
 
-  if (warp == 0 && lane == 0 && n > 0) {
-    // Warm L2 with the query rows this CTA will read (contiguous: units are in q order).
-    const int cta_lo = min(total, blockIdx.x * NW * R), cta_hi = min(total, (blockIdx.x + 1) * NW * R);
-    if (cta_hi > cta_lo) {
+  if (warp == 0 && lane == 0 && part.total > 0) {
+    // Warm L2 with the query rows of this CTA's heads (contiguous: units are in q order).
+    int s0, e0, s1, e1;
+    part.head(blockIdx.x * NW, s0, e0);
+    part.head(blockIdx.x * NW + NW - 1, s1, e1);
+    if (e1 > s0) {
       int b0, h0, j0, b1, h1, j1;
-      locate(cta_lo, b0, h0, j0);
-      locate(cta_hi - 1, b1, h1, j1);
+      locate(s0, b0, h0, j0);
+      locate(e1 - 1, b1, h1, j1);
       const int64_t u0 = static_cast<int64_t>(b0) * Hkv + h0, u1 = static_cast<int64_t>(b1) * Hkv + h1;
       prefetch_l2_bulk(static_cast<const T*>(a.q) + u0 * g * D,
                        static_cast<uint32_t>((u1 - u0 + 1) * g * D * sizeof(T)));
     }
   }
 
-  if (n > 0) {
-    uint8_t* wring = ring + warp * SW * Shape::kStageBytes;
-    const uint64_t policy = l2_evict_first_policy();
-    if (lane == 0) {
-      prefetch_tensormap(&tmap_k);
-      prefetch_tensormap(&tmap_v);
+  uint8_t* wring = ring + warp * SW * Shape::kStageBytes;
+  const uint64_t policy = l2_evict_first_policy();
+  if (lane == 0) {
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
+
+  // ---- issue side: current segment [seg_s, seg_e) and a 32-block window of it,
+  // lane i describing block win_s + i (unit, block j, pool row).
+  int seg, seg_s, seg_e;
+  part.head(gw, seg_s, seg_e);
+  seg = gw;
+  int win_s = seg_s, win_e = seg_s, ip = seg_s;
+  int wu = -1, wj = 0, wrow = -kBlockSize;
+  bool more = true;
+  // A chunk claim made while the last window of a segment is being issued, so
+  // that the counter's round trip overlaps that work.
+  int q_pending = 0;
+  bool claim_pending = false;
+  auto fill_window = [&]() {
+    win_s = ip;
+    win_e = min(seg_e, ip + 32);
+    wu = -1; wj = 0; wrow = -kBlockSize;
+    if (win_s + lane < win_e) {
+      int b, kvh, j;
+      locate(win_s + lane, b, kvh, j);
+      wu = b * Hkv + kvh;
+      wj = j;
+      wrow = tile_row(__ldg(a.block_tables + static_cast<int64_t>(b) * a.max_blocks + j), kvh, a);
+      if (j == 0 || lane == 0)  // a unit starts here: bring its query rows into L2
+        prefetch_l2_bulk(static_cast<const T*>(a.q) + static_cast<int64_t>(wu) * g * D,
+                         static_cast<uint32_t>(g * D * sizeof(T)));
     }
-    // Per-lane block info for a 32-block chunk of this warp's range: lane i
-    // describes block base + i (unit id, block index j, pool row).
-    auto chunk_info = [&](int base, int& u, int& jj, int& row) {
-      u = -1; jj = 0; row = -kBlockSize;
-      if (base + lane < n) {
-        int b, kvh, j;
-        locate(start + base + lane, b, kvh, j);
-        u = b * Hkv + kvh;
-        jj = j;
-        row = tile_row(__ldg(a.block_tables + static_cast<int64_t>(b) * a.max_blocks + j), kvh, a);
-      }
-    };
-    int cu, cj, crow, nu = -1, nj = 0, nrow = -kBlockSize;
-    chunk_info(0, cu, cj, crow);
-    if (n > 32) chunk_info(32, nu, nj, nrow);
-
-    // Fill the ring.
-    for (int k = 0; k < min(SW, n); ++k) {
-      const int row = __shfl_sync(0xffffffffu, crow, k);
-      if (lane == 0)
-        issue_block<D>(smem_u32(wring + k * Shape::kStageBytes), smem_u32(&full_bar[warp][k]), &tmap_k, &tmap_v,
-                       row, policy);
+    if (win_e == seg_e && !claim_pending) {
+      if (lane == 0) q_pending = atomicAdd(a.sched, 1);
+      claim_pending = true;
     }
-
-    WarpAttn<T, D> at;
-    bool first_unit = true;
-    int unit_first_j = 0;
-    for (int k = 0; k < n; ++k) {
-      if ((k & 31) == 0 && k > 0) {  // advance the chunk window
-        cu = nu; cj = nj; crow = nrow;
-        if (k + 32 < n) chunk_info(k + 32, nu, nj, nrow);
+  };
+  // Next window: the rest of this segment, else the next claimed chunk.
+  auto advance = [&]() {
+    if (ip < seg_e) {
+      fill_window();
+      return;
+    }
+    while (true) {
+      int q = 0;
+      if (claim_pending) {
+        q = q_pending;
+        claim_pending = false;
+      } else if (lane == 0) {
+        q = atomicAdd(a.sched, 1);
       }
-      const int st = k % SW;
-      if (!mbar_wait(smem_u32(&full_bar[warp][st]), (k / SW) & 1)) break;  // timed out: flagged
-      const int u = __shfl_sync(0xffffffffu, cu, k & 31);
-      const int j = __shfl_sync(0xffffffffu, cj, k & 31);
-      const int b = u / Hkv, kvh = u - b * Hkv;
-      const int ctx = s_ctx[b];
-      const int nb = (ctx + kBlockSize - 1) / kBlockSize;
-      if (k == 0 || j == 0) {
-        unit_first_j = j;
-        at.load_q(static_cast<const T*>(a.q) + (static_cast<int64_t>(b) * a.num_q_heads + kvh * g) * D, g, lane);
-        at.reset();
+      q = __shfl_sync(0xffffffffu, q, 0);
+      if (q >= part.num_chunks()) {
+        more = false;
+        // The last warp to run out of chunks resets the counters for the next call.
+        if (lane == 0 && atomicAdd(a.sched + 1, 1) == part.nwarps - 1) {
+          a.sched[0] = 0;
+          a.sched[1] = 0;
+        }
+        return;
       }
-      const uint8_t* ks = wring + st * Shape::kStageBytes;
-      at.block(ks, ks + Shape::kTileBytes, min(kBlockSize, ctx - j * kBlockSize), a.scale_log2, lane);
+      int s, e;
+      part.chunk(q / part.nwarps, q % part.nwarps, s, e);
+      if (e > s) {
+        seg = part.nwarps + q;
+        seg_s = s;
+        seg_e = e;
+        ip = s;
+        fill_window();
+        return;
+      }
+    }
+  };
 
-      // Refill this stage with block k + SW.
-      const int kn = k + SW;
-      const int src = kn & 31;
-      const int r_cur = __shfl_sync(0xffffffffu, crow, src);
-      const int r_nxt = __shfl_sync(0xffffffffu, nrow, src);
-      __syncwarp();
-      if (lane == 0 && kn < n) {
-        fence_proxy_async_smem();
+  // ---- consume side
+  WarpAttn<T, D> at;
+  int unit_first_j = 0;
+  bool seg_first_flush = true;
+  int issued = 0, consumed = 0;
+  bool ok = true;
+  while (true) {
+    while (more && issued - consumed < SW) {
+      if (ip == win_e) {
+        advance();
+        if (!more) break;
+      }
+      const int src = ip - win_s;
+      const int u = __shfl_sync(0xffffffffu, wu, src);
+      const int j = __shfl_sync(0xffffffffu, wj, src);
+      const int row = __shfl_sync(0xffffffffu, wrow, src);
+      const int st = issued % SW;
+      if (lane == 0) {
+        s_desc[warp][st] = make_int4(u, j, seg, (ip == seg_s ? 1 : 0) | (ip == seg_e - 1 ? 2 : 0));
+        fence_proxy_async_smem();  // earlier generic reads of this stage come before the refill
         issue_block<D>(smem_u32(wring + st * Shape::kStageBytes), smem_u32(&full_bar[warp][st]), &tmap_k, &tmap_v,
-                       (kn & ~31) == (k & ~31) ? r_cur : r_nxt, policy);
+                       row, policy);
       }
+      ++issued;
+      ++ip;
+    }
+    __syncwarp();  // the descriptors written by lane 0 are visible to the warp
+    if (consumed == issued || !ok) break;
 
-      if (j == nb - 1 || k == n - 1) {
-        // ---- the unit ends in this warp's range: write it out or hand it to the merge
-        at.finish_sums();
-        const int gid = lane >> 2, c = lane & 3;
-        if (unit_first_j == 0 && j == nb - 1) {
+    const int st = consumed % SW;
+    if (!mbar_wait(smem_u32(&full_bar[warp][st]), (consumed / SW) & 1)) {  // timed out: flagged
+      ok = false;
+      break;
+    }
+    const int4 dsc = s_desc[warp][st];
+    const int u = dsc.x, j = dsc.y, sid = dsc.z;
+    const bool first_of_seg = dsc.w & 1, last_of_seg = dsc.w & 2;
+    const int b = u / Hkv, kvh = u - b * Hkv;
+    const int ctx = s_ctx[b];
+    const int nb = (ctx + kBlockSize - 1) / kBlockSize;
+    if (first_of_seg || j == 0) {
+      if (first_of_seg) seg_first_flush = true;
+      unit_first_j = j;
+      at.load_q(static_cast<const T*>(a.q) + (static_cast<int64_t>(b) * a.num_q_heads + kvh * g) * D, g, lane);
+      at.reset();
+    }
+    const uint8_t* ks = wring + st * Shape::kStageBytes;
+    at.block(ks, ks + Shape::kTileBytes, min(kBlockSize, ctx - j * kBlockSize), a.scale_log2, lane);
+    ++consumed;
+
+    if (j == nb - 1 || last_of_seg) {
+      // ---- the unit ends here or the segment does: write it out, or leave a piece for the merge
+      at.finish_sums();
+      const int gid = lane >> 2, c = lane & 3;
+      const bool complete = unit_first_j == 0 && j == nb - 1;
+      const int64_t pbase = (static_cast<int64_t>(sid) * 2 + (seg_first_flush ? 0 : 1)) * kMaxGroup;
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int h = 2 * c + e;
-            if (h >= g) continue;
-            T* orow = static_cast<T*>(a.out) + (static_cast<int64_t>(b) * a.num_q_heads + kvh * g + h) * D;
-            const float inv = 1.0f / (e ? at.l1 : at.l0);
+      for (int e = 0; e < 2; ++e) {
+        const int h = 2 * c + e;
+        if (h >= g) continue;
+        const float l = e ? at.l1 : at.l0;
+        if (complete) {
+          T* orow = static_cast<T*>(a.out) + (static_cast<int64_t>(b) * a.num_q_heads + kvh * g + h) * D;
 #pragma unroll
-            for (int kk = 0; kk < WarpAttn<T, D>::kChunks; ++kk) {
-              float v[8];
-              at.chunk_values(e, kk, inv, v);
-              *reinterpret_cast<uint4*>(orow + WarpAttn<T, D>::chunk_dim(lane, kk)) = pack8<T>(v);
-            }
+          for (int kk = 0; kk < WarpAttn<T, D>::kChunks; ++kk) {
+            float v[8];
+            at.chunk_values(e, kk, 1.0f / l, v);
+            *reinterpret_cast<uint4*>(orow + WarpAttn<T, D>::chunk_dim(lane, kk)) = pack8<T>(v);
           }
         } else {
-          const int slot = first_unit ? 0 : 1;
-          const int64_t pbase = (static_cast<int64_t>(gw) * 2 + slot) * kMaxGroup;
+          float* prow = a.part_o + (pbase + h) * D;
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int h = 2 * c + e;
-            const float l = e ? at.l1 : at.l0;
-            float* prow = a.part_o + (pbase + h) * D;
-#pragma unroll
-            for (int kk = 0; kk < WarpAttn<T, D>::kChunks; ++kk) {
-              float v[8];
-              at.chunk_values(e, kk, 1.0f / l, v);
-              float4* dst = reinterpret_cast<float4*>(prow + WarpAttn<T, D>::chunk_dim(lane, kk));
-              dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-              dst[1] = make_float4(v[4], v[5], v[6], v[7]);
-            }
-            if (gid == 0) a.part_lse[pbase + h] = (e ? at.m1 : at.m0) + log2f(l);
+          for (int kk = 0; kk < WarpAttn<T, D>::kChunks; ++kk) {
+            float v[8];
+            at.chunk_values(e, kk, 1.0f / l, v);
+            float4* dst = reinterpret_cast<float4*>(prow + WarpAttn<T, D>::chunk_dim(lane, kk));
+            dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+            dst[1] = make_float4(v[4], v[5], v[6], v[7]);
           }
-          // Count this piece; the warp that completes the unit merges it.
-          const int U = Hkv * s_P[b] + kvh * nb;
-          const int r0 = U / R, r1 = (U + nb - 1) / R;
-          __threadfence();
-          __syncwarp();
-          int last = 0;
-          if (lane == 0) last = atomicAdd(a.counters + u, 1) == r1 - r0;
-          last = __shfl_sync(0xffffffffu, last, 0);
-          if (last) {
-            __threadfence();
-            // lane: head lane / 4, head_dim quarter lane % 4
-            const int h = lane >> 2;
-            if (h < g) {
-              constexpr int kQ = D / 4;
-              const int d0 = (lane & 3) * kQ;
-              float M = -INFINITY;
-              for (int r = r0; r <= r1; ++r) {
-                const int sl = (r == r0 && U > r0 * R) ? 1 : 0;
-                M = fmaxf(M, __ldcg(a.part_lse + (static_cast<int64_t>(r) * 2 + sl) * kMaxGroup + h));
-              }
-              float o[kQ];
-#pragma unroll
-              for (int i = 0; i < kQ; ++i) o[i] = 0.f;
-              float L = 0.f;
-              for (int r = r0; r <= r1; ++r) {
-                const int sl = (r == r0 && U > r0 * R) ? 1 : 0;
-                const int64_t pr = (static_cast<int64_t>(r) * 2 + sl) * kMaxGroup + h;
-                const float w = exp2f(__ldcg(a.part_lse + pr) - M);
-                L += w;
-                const float4* src4 = reinterpret_cast<const float4*>(a.part_o + pr * D + d0);
-#pragma unroll
-                for (int i = 0; i < kQ / 4; ++i) {
-                  const float4 x = __ldcg(src4 + i);
-                  o[4 * i] += w * x.x;
-                  o[4 * i + 1] += w * x.y;
-                  o[4 * i + 2] += w * x.z;
-                  o[4 * i + 3] += w * x.w;
-                }
-              }
-              const float inv = 1.0f / L;
-              T* orow = static_cast<T*>(a.out) + (static_cast<int64_t>(b) * a.num_q_heads + kvh * g + h) * D + d0;
-#pragma unroll
-              for (int i = 0; i < kQ / 8; ++i) {
-                float v[8];
-#pragma unroll
-                for (int x = 0; x < 8; ++x) v[x] = o[8 * i + x] * inv;
-                *reinterpret_cast<uint4*>(orow + 8 * i) = pack8<T>(v);
-              }
-            }
-            if (lane == 0) a.counters[u] = 0;  // ready for the next call
-          }
+          if (gid == 0) a.part_lse[pbase + h] = (e ? at.m1 : at.m0) + log2f(l);
         }
-        first_unit = false;
+      }
+      seg_first_flush = false;
+    }
+  }
+  if (!ok && lane == 0) {
+    // A wait gave up: let this warp's copies in flight land before the CTA exits.
+    for (int i = consumed; i < issued; ++i) mbar_wait(smem_u32(&full_bar[warp][i % SW]), (i / SW) & 1);
+  }
+}
+
+// Merge of the pieces the persistent kernel left: one warp per (sequence,
+// query head).  Units wholly inside one segment were written by the decode
+// kernel; an empty context gives a zero row.  The unit's blocks [U, U+nb)
+// overlap shares w0..w1, each holding 5 segments (head + 4 tail chunks); lanes
+// test those candidates in parallel, then accumulate the overlapping pieces.
+// Launched as a programmatic dependent of the decode kernel: it waits for the
+// decode grid to finish before reading anything.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) merge_persistent_kernel(const DecodeArgs a, int32_t nwarps) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int kPer = D / 32;
+  constexpr int kSegPerShare = 1 + Partition::kTailChunks;
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= a.num_seqs * a.num_q_heads) return;
+  const int b = row / a.num_q_heads, hq = row - b * a.num_q_heads;
+  const int kvh = hq / a.group, h = hq - kvh * a.group;
+  const int ctx = clamped_context(a.context_lens, b, a.max_blocks, false);
+  const int nb = (ctx + kBlockSize - 1) / kBlockSize;
+  T* dst = static_cast<T*>(a.out) + static_cast<int64_t>(row) * D + lane * kPer;
+  if (nb == 0) {
+#pragma unroll
+    for (int k = 0; k < kPer; k += 2) *reinterpret_cast<uint32_t*>(dst + k) = 0u;
+    return;
+  }
+  const Partition part(a.num_kv_heads * a.plan[a.num_seqs], nwarps);
+  const int U = a.num_kv_heads * a.plan[b] + kvh * nb, Uend = U + nb;
+  {
+    int s, e;
+    part.segment_of(U, s, e);
+    if (e >= Uend) return;  // one segment: the decode kernel wrote it
+  }
+  const int w0 = U / part.R, ncand = (( Uend - 1) / part.R - w0 + 1) * kSegPerShare;
+
+  // Candidate c: share w0 + c / 5, segment c % 5 of it.  Returns the partial's
+  // row index (slot included), or -1 when the segment does not overlap the unit.
+  auto piece = [&](int c) -> int64_t {
+    const int w = w0 + c / kSegPerShare, k = c % kSegPerShare;
+    int s, e, sid;
+    if (k == 0) {
+      part.head(w, s, e);
+      sid = w;
+    } else {
+      part.chunk(k - 1, w, s, e);
+      sid = part.nwarps + (k - 1) * part.nwarps + w;
+    }
+    if (e <= s || e <= U || s >= Uend) return -1;
+    return (static_cast<int64_t>(sid) * 2 + (U > s ? 1 : 0)) * kMaxGroup + h;
+  };
+
+  float M = -INFINITY;
+  for (int c = lane; c < ncand; c += 32) {
+    const int64_t pr = piece(c);
+    if (pr >= 0) M = fmaxf(M, a.part_lse[pr]);
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+
+  float o[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) o[k] = 0.f;
+  float L = 0.f;
+  for (int base = 0; base < ncand; base += 32) {
+    const int64_t pr = base + lane < ncand ? piece(base + lane) : -1;
+    const float w = pr >= 0 ? exp2f(a.part_lse[pr] - M) : 0.f;
+    L += w;
+    const int cnt = min(32, ncand - base);
+#pragma unroll 4
+    for (int i = 0; i < cnt; ++i) {
+      const float wi = __shfl_sync(0xffffffffu, w, i);
+      const int64_t pi = __shfl_sync(0xffffffffu, pr, i);
+      if (pi < 0) continue;
+      const float* src = a.part_o + pi * D + lane * kPer;
+#pragma unroll
+      for (int k = 0; k < kPer; k += 2) {
+        const float2 v = *reinterpret_cast<const float2*>(src + k);
+        o[k] += wi * v.x;
+        o[k + 1] += wi * v.y;
       }
     }
   }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  const float inv = 1.0f / L;
+#pragma unroll
+  for (int k = 0; k < kPer; k += 2) *reinterpret_cast<uint32_t*>(dst + k) = pack2<T>(o[k] * inv, o[k + 1] * inv);
 }
 
 // ===================================================================== split kernel
