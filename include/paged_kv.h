@@ -128,6 +128,23 @@ int paged_decode_attention(const void* q, const void* k_cache, const void* v_cac
                            void* workspace, size_t workspace_bytes,
                            const pkv_dims* dims, void* stream);
 
+/*
+ * One decode step (device): the append of each sequence's new token followed
+ * by paged decode attention.  Sequence b's token (k_new[b], v_new[b]:
+ * T[num_seqs][num_kv_heads][head_dim]) is stored at position
+ * context_lens[b] - 1, i.e. slot block_tables[b][(L-1)/16] * 16 + (L-1) % 16
+ * with L = context_lens[b] (nothing for an empty context), and the attention
+ * over positions [0, L) sees it.  Same results as paged_kv_append with that
+ * slot mapping followed by paged_decode_attention.  On the automatic path
+ * (num_splits = 0) the append runs inside the attention kernel, so a step is
+ * one decode launch plus the merge; otherwise it is a separate append launch.
+ * Arguments and requirements otherwise as paged_decode_attention.
+ */
+int paged_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                      const int32_t* block_tables, const int32_t* context_lens, float scale, void* out,
+                      int32_t num_splits, void* workspace, size_t workspace_bytes,
+                      const pkv_dims* dims, void* stream);
+
 /* The split count paged_decode_attention will use for this num_splits
  * argument: 0 for the persistent balanced kernel, >= 1 for the split kernel,
  * or a PKV_ERR_* code. */
@@ -139,18 +156,16 @@ size_t paged_decode_workspace_bytes(const pkv_dims* dims, int32_t num_splits);
 
 /*
  * One whole decode step from host memory: copies q, k_new, v_new,
- * slot_mapping, block_tables and context_lens from host buffers (pinned for
- * asynchronous copies) into the caller's device staging buffers, runs the
- * append and the attention on `stream`, and copies out back to out_host.
- * The step is complete when the stream is.  num_tokens = dims->num_seqs.
+ * block_tables and context_lens from host buffers (pinned for asynchronous
+ * copies) into the caller's device staging buffers, runs paged_decode_step on
+ * `stream`, and copies out back to out_host.  The step is complete when the
+ * stream is.
  */
 typedef struct pkv_step_buffers {
   const void* q_host;  const void* k_new_host;  const void* v_new_host;
-  const int32_t* slot_mapping_host;  const int32_t* block_tables_host;
-  const int32_t* context_lens_host;  void* out_host;
+  const int32_t* block_tables_host;  const int32_t* context_lens_host;  void* out_host;
   void* q_dev;  void* k_new_dev;  void* v_new_dev;
-  int32_t* slot_mapping_dev;  int32_t* block_tables_dev;  int32_t* context_lens_dev;
-  void* out_dev;
+  int32_t* block_tables_dev;  int32_t* context_lens_dev;  void* out_dev;
 } pkv_step_buffers;
 
 int paged_decode_step_from_host(const pkv_step_buffers* bufs, void* k_cache, void* v_cache,

@@ -17,9 +17,8 @@ class PkvDims(ctypes.Structure):
 
 class PkvStepBuffers(ctypes.Structure):
     _fields_ = [(name, ctypes.c_void_p) for name in (
-        "q_host", "k_new_host", "v_new_host", "slot_mapping_host", "block_tables_host",
-        "context_lens_host", "out_host", "q_dev", "k_new_dev", "v_new_dev",
-        "slot_mapping_dev", "block_tables_dev", "context_lens_dev", "out_dev")]
+        "q_host", "k_new_host", "v_new_host", "block_tables_host", "context_lens_host", "out_host",
+        "q_dev", "k_new_dev", "v_new_dev", "block_tables_dev", "context_lens_dev", "out_dev")]
 
 
 _SIGNATURES = {
@@ -29,6 +28,10 @@ _SIGNATURES = {
                                               ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_int32,
                                               ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(PkvDims),
                                               ctypes.c_void_p]),
+    "paged_decode_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
+                                         ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t,
+                                         ctypes.POINTER(PkvDims), ctypes.c_void_p]),
     "paged_decode_resolve_splits": (ctypes.c_int32, [ctypes.POINTER(PkvDims), ctypes.c_int32]),
     "paged_decode_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(PkvDims), ctypes.c_int32]),
     "paged_decode_step_from_host": (ctypes.c_int, [ctypes.POINTER(PkvStepBuffers), ctypes.c_void_p, ctypes.c_void_p,

@@ -18,6 +18,7 @@ ERROR_NAMES = {
     -5: "PKV_ERR_NO_BLOCKS", -6: "PKV_ERR_OUT_OF_RANGE", -7: "PKV_ERR_SHARED_BLOCK",
 }
 _DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1}
+STEP_KEYS = ("q", "k_new", "v_new", "block_tables", "context_lens", "out")
 
 
 class PagedKVError(RuntimeError):
@@ -131,14 +132,46 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     return out
 
 
+def paged_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                      out: Optional[torch.Tensor] = None, num_splits: int = 0,
+                      workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One decode step: store each sequence's new token (k_new[b], v_new[b])
+    at position context_lens[b] - 1 through its block table, then attend over
+    positions [0, context_lens[b]).  Returns out."""
+    for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need_cuda(n, t, k_cache.dtype)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda("out", out, q.dtype)
+    if k_new.shape != (q.shape[0], k_cache.shape[1], k_cache.shape[3]) or v_new.shape != k_new.shape:
+        raise ValueError("k_new / v_new must be [num_seqs][num_kv_heads][head_dim]")
+    if out.shape != q.shape or q.dim() != 3 or q.shape[2] != k_cache.shape[3]:
+        raise ValueError("q / out must be [num_seqs][num_q_heads][head_dim]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != q.shape[0] or context_lens.shape != (q.shape[0],):
+        raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
+    dims = make_dims(q, k_cache, block_tables)
+    need = int(lib().paged_decode_workspace_bytes(ctypes.byref(dims), num_splits))
+    if need and workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().paged_decode_step(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(block_tables), _ptr(context_lens), float(scale), _ptr(out), num_splits,
+                                   _ptr(workspace), ws_bytes, ctypes.byref(dims), _stream(stream)),
+           "paged_decode_step")
+    return out
+
+
 def paged_decode_step_from_host(host: dict, dev: dict, k_cache: torch.Tensor, v_cache: torch.Tensor,
                                 scale: float, num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
                                 stream=None) -> None:
     """One decode step from (pinned) host buffers: copies q, k_new, v_new,
-    slot_mapping, block_tables, context_lens into the device staging tensors in
-    ``dev``, runs append + attention, and copies out back into host['out'].
-    Keys of both dicts: q, k_new, v_new, slot_mapping, block_tables, context_lens, out."""
-    keys = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens", "out")
+    block_tables, context_lens into the device staging tensors in ``dev``,
+    runs paged_decode_step, and copies out back into host['out'].
+    Keys of both dicts: q, k_new, v_new, block_tables, context_lens, out."""
+    keys = STEP_KEYS
     bufs = PkvStepBuffers(**{f"{k}_host": host[k].data_ptr() for k in keys},
                           **{f"{k}_dev": dev[k].data_ptr() for k in keys})
     dims = make_dims(dev["q"], k_cache, dev["block_tables"])

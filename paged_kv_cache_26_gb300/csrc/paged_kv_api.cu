@@ -224,23 +224,25 @@ int launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::Decod
     int64_t grid = (upper_blocks + pkv::PersistentShape<D>::kWarps - 1) / pkv::PersistentShape<D>::kWarps;
     if (grid > device_sms()) grid = device_sms();
     if (grid < 1) grid = 1;
-    kern<<<static_cast<int>(grid), pkv::PersistentShape<D>::kWarps * 32, pkv::persistent_smem_bytes<D>(d->num_seqs),
-           stream>>>(mk, mv, args);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "decode_persistent_kernel launch");
-    // The merge is a programmatic dependent launch: its CTAs become resident
-    // while the decode kernel runs and wait in-kernel for it to finish.
-    const int rows = d->num_seqs * d->num_q_heads;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((rows + 3) / 4);
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
+    // Both kernels are programmatic dependent launches: each may start while
+    // the kernel before it in the stream finishes, and waits in-kernel
+    // (griddepcontrol.wait) before touching anything that kernel writes.
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(pkv::PersistentShape<D>::kWarps * 32);
+    cfg.dynamicSmemBytes = pkv::persistent_smem_bytes<D>(d->num_seqs);
+    cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, mk, mv, args);
+    if (e != cudaSuccess) return cuda_fail(e, "decode_persistent_kernel launch");
+    const int rows = d->num_seqs * d->num_q_heads;
+    cfg.gridDim = dim3((rows + 3) / 4);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
     e = cudaLaunchKernelEx(&cfg, pkv::merge_persistent_kernel<T, D>, args,
                            static_cast<int32_t>(grid) * pkv::PersistentShape<D>::kWarps);
     if (e != cudaSuccess) return cuda_fail(e, "merge_persistent_kernel launch");
@@ -265,9 +267,17 @@ int launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::Decod
   return PKV_OK;
 }
 
-int decode_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
-                const int32_t* context_lens, float scale, void* out, int32_t num_splits, void* workspace,
-                size_t workspace_bytes, const pkv_dims* d, cudaStream_t stream) {
+int append_at_end_impl(const void* k_new, const void* v_new, const int32_t* block_tables,
+                       const int32_t* context_lens, void* k_cache, void* v_cache, const pkv_dims* d,
+                       cudaStream_t stream);
+
+// Attention, optionally preceded by the append of each sequence's token at
+// position context_lens[b] - 1 (k_new / v_new non-null): fused into the
+// persistent kernel when that path runs, else a separate append launch.
+int decode_impl(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                const int32_t* block_tables, const int32_t* context_lens, float scale, void* out,
+                int32_t num_splits, void* workspace, size_t workspace_bytes, const pkv_dims* d,
+                cudaStream_t stream) {
   int rc = check_dims(d, true);
   if (rc != PKV_OK) return rc;
   if (d->num_seqs == 0) return PKV_OK;
@@ -287,11 +297,24 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const i
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
     return pkv_fail(PKV_ERR_INVALID_ARG, "decode_attention: workspace missing, too small (" +
                                              std::to_string(need) + " bytes needed) or not 256-byte aligned");
+  const bool append = k_new != nullptr;
+  if (append != (v_new != nullptr))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "decode_step: k_new and v_new must both be given");
+  if (append && (!aligned(k_new, 16) || !aligned(v_new, 16)))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "decode_step: k_new / v_new must be 16-byte aligned");
+  if (append && !plan.persistent) {
+    rc = append_at_end_impl(k_new, v_new, block_tables, context_lens, k_cache, v_cache, d, stream);
+    if (rc != PKV_OK) return rc;
+  }
   CUtensorMap mk, mv;
   if ((rc = g_maps.get(k_cache, d, &mk)) != PKV_OK) return rc;
   if ((rc = g_maps.get(v_cache, d, &mv)) != PKV_OK) return rc;
 
   pkv::DecodeArgs args;
+  args.k_new = append && plan.persistent ? k_new : nullptr;
+  args.v_new = append && plan.persistent ? v_new : nullptr;
+  args.k_cache_w = k_cache;
+  args.v_cache_w = v_cache;
   args.q = q;
   args.out = out;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -317,6 +340,24 @@ int decode_impl(const void* q, const void* k_cache, const void* v_cache, const i
                 : launch_decode<__half, 128>(mk, mv, args, plan, d, stream);
   return bf16 ? launch_decode<__nv_bfloat16, 64>(mk, mv, args, plan, d, stream)
               : launch_decode<__half, 64>(mk, mv, args, plan, d, stream);
+}
+
+int append_at_end_impl(const void* k_new, const void* v_new, const int32_t* block_tables,
+                       const int32_t* context_lens, void* k_cache, void* v_cache, const pkv_dims* d,
+                       cudaStream_t stream) {
+  if (d->num_seqs == 0 || d->max_blocks_per_seq == 0) return PKV_OK;
+  const int32_t chunks = d->head_dim * 2 / 16;
+  const int64_t total = static_cast<int64_t>(d->num_seqs) * d->num_kv_heads * chunks;
+  const int threads = 256;
+  const int64_t blocks64 = (total + threads - 1) / threads;
+  const int blocks = static_cast<int>(blocks64 < 65536 ? blocks64 : 65536);
+  pkv::append_at_end_kernel<<<blocks, threads, 0, stream>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), block_tables, context_lens, d->num_seqs,
+      d->max_blocks_per_seq, d->num_kv_heads, chunks, d->num_blocks, static_cast<uint4*>(k_cache),
+      static_cast<uint4*>(v_cache));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "append_at_end_kernel launch");
+  return PKV_OK;
 }
 
 int append_impl(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t num_tokens,
@@ -357,8 +398,18 @@ int paged_kv_append(const void* k_new, const void* v_new, const int32_t* slot_ma
 int paged_decode_attention(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
                            const int32_t* context_lens, float scale, void* out, int32_t num_splits, void* workspace,
                            size_t workspace_bytes, const pkv_dims* dims, void* stream) {
-  return decode_impl(q, k_cache, v_cache, block_tables, context_lens, scale, out, num_splits, workspace,
-                     workspace_bytes, dims, static_cast<cudaStream_t>(stream));
+  return decode_impl(q, nullptr, nullptr, const_cast<void*>(k_cache), const_cast<void*>(v_cache), block_tables,
+                     context_lens, scale, out, num_splits, workspace, workspace_bytes, dims,
+                     static_cast<cudaStream_t>(stream));
+}
+
+int paged_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                      const int32_t* block_tables, const int32_t* context_lens, float scale, void* out,
+                      int32_t num_splits, void* workspace, size_t workspace_bytes, const pkv_dims* dims,
+                      void* stream) {
+  if (!k_new || !v_new) return pkv_fail(PKV_ERR_INVALID_ARG, "decode_step: NULL k_new / v_new");
+  return decode_impl(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, out, num_splits,
+                     workspace, workspace_bytes, dims, static_cast<cudaStream_t>(stream));
 }
 
 int32_t paged_decode_resolve_splits(const pkv_dims* dims, int32_t num_splits) {
@@ -395,7 +446,6 @@ int paged_decode_step_from_host(const pkv_step_buffers* s, void* k_cache, void* 
   } h2d[] = {{s->q_dev, s->q_host, q_bytes},
              {s->k_new_dev, s->k_new_host, kv_bytes},
              {s->v_new_dev, s->v_new_host, kv_bytes},
-             {s->slot_mapping_dev, s->slot_mapping_host, B * sizeof(int32_t)},
              {s->block_tables_dev, s->block_tables_host, tbl_bytes},
              {s->context_lens_dev, s->context_lens_host, B * sizeof(int32_t)}};
   for (const auto& c : h2d) {
@@ -404,16 +454,13 @@ int paged_decode_step_from_host(const pkv_step_buffers* s, void* k_cache, void* 
     cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return cuda_fail(e, "step: host-to-device copy");
   }
-  rc = append_impl(s->k_new_dev, s->v_new_dev, s->slot_mapping_dev, d->num_seqs, k_cache, v_cache, d, stream);
+  if (B == 0) return PKV_OK;
+  rc = decode_impl(s->q_dev, s->k_new_dev, s->v_new_dev, k_cache, v_cache, s->block_tables_dev,
+                   s->context_lens_dev, scale, s->out_dev, num_splits, workspace, workspace_bytes, d, stream);
   if (rc != PKV_OK) return rc;
-  rc = decode_impl(s->q_dev, k_cache, v_cache, s->block_tables_dev, s->context_lens_dev, scale, s->out_dev,
-                   num_splits, workspace, workspace_bytes, d, stream);
-  if (rc != PKV_OK) return rc;
-  if (q_bytes) {
-    if (!s->out_host) return pkv_fail(PKV_ERR_INVALID_ARG, "step: out_host is NULL");
-    cudaError_t e = cudaMemcpyAsync(s->out_host, s->out_dev, q_bytes, cudaMemcpyDeviceToHost, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "step: device-to-host copy");
-  }
+  if (!s->out_host) return pkv_fail(PKV_ERR_INVALID_ARG, "step: out_host is NULL");
+  cudaError_t e = cudaMemcpyAsync(s->out_host, s->out_dev, q_bytes, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "step: device-to-host copy");
   return PKV_OK;
 }
 

@@ -46,6 +46,7 @@ __global__ void append_kernel(const uint4* __restrict__ k_new, const uint4* __re
                               const int32_t* __restrict__ slots, int32_t num_tokens, int32_t num_kv_heads,
                               int32_t chunks_per_row, int64_t num_slots, uint4* __restrict__ k_cache,
                               uint4* __restrict__ v_cache) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t per_token = static_cast<int64_t>(num_kv_heads) * chunks_per_row;
   const int64_t total = per_token * num_tokens;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
@@ -63,6 +64,41 @@ __global__ void append_kernel(const uint4* __restrict__ k_new, const uint4* __re
     const int64_t head = within / chunks_per_row;
     const int64_t chunk = within - head * chunks_per_row;
     const int64_t dst = ((blk * num_kv_heads + head) * kBlockSize + off) * chunks_per_row + chunk;
+    k_cache[dst] = k_new[idx];
+    v_cache[dst] = v_new[idx];
+  }
+}
+
+// The same copy with each sequence's slot derived from its table: token b goes
+// to position context_lens[b] - 1 (nothing when the context is empty).
+__global__ void append_at_end_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                                     const int32_t* __restrict__ block_tables,
+                                     const int32_t* __restrict__ context_lens, int32_t num_seqs,
+                                     int32_t max_blocks, int32_t num_kv_heads, int32_t chunks_per_row,
+                                     int32_t num_blocks, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int64_t per_token = static_cast<int64_t>(num_kv_heads) * chunks_per_row;
+  const int64_t total = per_token * num_seqs;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t b = idx / per_token;
+    const int L = context_lens[b];
+    if (L <= 0) continue;
+    if (L > max_blocks * kBlockSize) {
+      flag_error(kErrContext);
+      continue;
+    }
+    const int pos = L - 1;
+    const int32_t blk = block_tables[b * max_blocks + pos / kBlockSize];
+    if (blk < 0 || blk >= num_blocks) {
+      flag_error(kErrBlockId);
+      continue;
+    }
+    const int64_t within = idx - b * per_token;
+    const int64_t head = within / chunks_per_row;
+    const int64_t chunk = within - head * chunks_per_row;
+    const int64_t dst =
+        ((static_cast<int64_t>(blk) * num_kv_heads + head) * kBlockSize + pos % kBlockSize) * chunks_per_row + chunk;
     k_cache[dst] = k_new[idx];
     v_cache[dst] = v_new[idx];
   }
@@ -234,6 +270,10 @@ struct DecodeArgs {
   float* part_lse;            // split: f32[B][Hq][splits];    persistent: f32[segments][2][8]
   int32_t* plan;              // persistent: int32[B+1] block prefix, written by the decode kernel
   int32_t* sched;             // persistent: int32[2] chunk counter and finished-warp counter, zero between calls
+  const void* k_new;          // fused append (persistent only): T[B][Hkv][D], or null for no append
+  const void* v_new;
+  void* k_cache_w;            // the pool, for the appended rows
+  void* v_cache_w;
   float scale_log2;           // scale * log2(e)
   int32_t num_seqs;
   int32_t num_q_heads;
@@ -266,16 +306,24 @@ __device__ __forceinline__ int tile_row(int phys, int kvh, const DecodeArgs& a) 
   return (phys * a.num_kv_heads + kvh) * kBlockSize;
 }
 
+// TMA loads of one block's K and V tiles into a stage, completing on `bar`
+// (whose transaction count the caller has set).
 template <int D>
-__device__ __forceinline__ void issue_block(uint32_t stage, uint32_t bar, const CUtensorMap* mk,
+__device__ __forceinline__ void issue_tiles(uint32_t stage, uint32_t bar, const CUtensorMap* mk,
                                             const CUtensorMap* mv, int row, uint64_t policy) {
   using Shape = TileShape<D>;
-  mbar_arrive_expect_tx(bar, Shape::kStageBytes);
 #pragma unroll
   for (int bx = 0; bx < Shape::kBoxes; ++bx) {
     tma_load_2d(stage + bx * 2048, mk, bx * 64, row, bar, policy);
     tma_load_2d(stage + Shape::kTileBytes + bx * 2048, mv, bx * 64, row, bar, policy);
   }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_block(uint32_t stage, uint32_t bar, const CUtensorMap* mk,
+                                            const CUtensorMap* mv, int row, uint64_t policy) {
+  mbar_arrive_expect_tx(bar, TileShape<D>::kStageBytes);
+  issue_tiles<D>(stage, bar, mk, mv, row, policy);
 }
 
 // ===================================================================== persistent kernel
@@ -287,10 +335,12 @@ struct PersistentShape {
   static constexpr int kRingBytes = kWarps * kStages * TileShape<D>::kStageBytes;
 };
 
-// Dynamic shared memory: [ring][prefix P[B+1]][context ctx[B]] (+1 KB alignment slack).
+// Dynamic shared memory: [ring][appended-token rows][prefix P[B+1]][context ctx[B]]
+// (+1 KB alignment slack).
 template <int D>
 constexpr size_t persistent_smem_bytes(int num_seqs) {
-  return PersistentShape<D>::kRingBytes + (2 * static_cast<size_t>(num_seqs) + 1) * 4 + 1024;
+  return PersistentShape<D>::kRingBytes + PersistentShape<D>::kWarps * PersistentShape<D>::kStages * 4 * D +
+         (2 * static_cast<size_t>(num_seqs) + 1) * 4 + 1024;
 }
 
 // Work partition of the persistent kernel.  The flattened block space
@@ -376,17 +426,20 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
   using Shape = TileShape<D>;
   constexpr int NW = PersistentShape<D>::kWarps;
   constexpr int SW = PersistentShape<D>::kStages;
+  constexpr int kRowBytes = D * 2;  // one token's K (or V) row for one KV head
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[NW][SW];
-  __shared__ int4 s_desc[NW][SW];  // per stage: unit, block j, segment id, flags
+  __shared__ int4 s_desc[NW][SW];  // per stage: unit, block j, segment id | flags << 28, pool row
   __shared__ int s_warp_sum[NW];
 
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  int* s_P = reinterpret_cast<int*>(ring + PersistentShape<D>::kRingBytes);
+  uint8_t* side = ring + PersistentShape<D>::kRingBytes;  // [NW][SW][K row, V row] of appended tokens
+  int* s_P = reinterpret_cast<int*>(side + NW * SW * 2 * kRowBytes);
   int* s_ctx = s_P + a.num_seqs + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = a.num_seqs, Hkv = a.num_kv_heads, g = a.group;
+  const bool fused_append = a.k_new != nullptr;
 
   // The merge kernel may launch now; it waits for this grid to complete.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -394,7 +447,11 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
     for (int s = 0; s < SW; ++s) mbar_init(smem_u32(&full_bar[warp][s]), 1);
     fence_mbar_init();
   }
+  // Inputs only (context lengths): safe before the previous kernel has finished.
   context_prefix(a, s_P, s_ctx, s_warp_sum, NW * 32, blockIdx.x == 0);
+  // From here on this grid reads the cache and writes the workspace and out,
+  // which the previous kernels in the stream (append, merge) touch.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (blockIdx.x == 0)  // the merge kernel reads the prefix
     for (int b = tid; b <= B; b += NW * 32) a.plan[b] = s_P[b];
 
@@ -416,22 +473,8 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
     j = rem - kvh * nb;
   };
 
-  if (warp == 0 && lane == 0 && part.total > 0) {
-    // Warm L2 with the query rows of this CTA's heads (contiguous: units are in q order).
-    int s0, e0, s1, e1;
-    part.head(blockIdx.x * NW, s0, e0);
-    part.head(blockIdx.x * NW + NW - 1, s1, e1);
-    if (e1 > s0) {
-      int b0, h0, j0, b1, h1, j1;
-      locate(s0, b0, h0, j0);
-      locate(e1 - 1, b1, h1, j1);
-      const int64_t u0 = static_cast<int64_t>(b0) * Hkv + h0, u1 = static_cast<int64_t>(b1) * Hkv + h1;
-      prefetch_l2_bulk(static_cast<const T*>(a.q) + u0 * g * D,
-                       static_cast<uint32_t>((u1 - u0 + 1) * g * D * sizeof(T)));
-    }
-  }
-
   uint8_t* wring = ring + warp * SW * Shape::kStageBytes;
+  uint8_t* wside = side + warp * SW * 2 * kRowBytes;
   const uint64_t policy = l2_evict_first_policy();
   if (lane == 0) {
     prefetch_tensormap(&tmap_k);
@@ -446,10 +489,6 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
   int win_s = seg_s, win_e = seg_s, ip = seg_s;
   int wu = -1, wj = 0, wrow = -kBlockSize;
   bool more = true;
-  // A chunk claim made while the last window of a segment is being issued, so
-  // that the counter's round trip overlaps that work.
-  int q_pending = 0;
-  bool claim_pending = false;
   auto fill_window = [&]() {
     win_s = ip;
     win_e = min(seg_e, ip + 32);
@@ -464,10 +503,6 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
         prefetch_l2_bulk(static_cast<const T*>(a.q) + static_cast<int64_t>(wu) * g * D,
                          static_cast<uint32_t>(g * D * sizeof(T)));
     }
-    if (win_e == seg_e && !claim_pending) {
-      if (lane == 0) q_pending = atomicAdd(a.sched, 1);
-      claim_pending = true;
-    }
   };
   // Next window: the rest of this segment, else the next claimed chunk.
   auto advance = [&]() {
@@ -477,12 +512,7 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
     }
     while (true) {
       int q = 0;
-      if (claim_pending) {
-        q = q_pending;
-        claim_pending = false;
-      } else if (lane == 0) {
-        q = atomicAdd(a.sched, 1);
-      }
+      if (lane == 0) q = atomicAdd(a.sched, 1);
       q = __shfl_sync(0xffffffffu, q, 0);
       if (q >= part.num_chunks()) {
         more = false;
@@ -524,16 +554,28 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
       const int row = __shfl_sync(0xffffffffu, wrow, src);
       const int st = issued % SW;
       if (lane == 0) {
-        s_desc[warp][st] = make_int4(u, j, seg, (ip == seg_s ? 1 : 0) | (ip == seg_e - 1 ? 2 : 0));
-        fence_proxy_async_smem();  // earlier generic reads of this stage come before the refill
-        issue_block<D>(smem_u32(wring + st * Shape::kStageBytes), smem_u32(&full_bar[warp][st]), &tmap_k, &tmap_v,
-                       row, policy);
+        const int b = u / Hkv;
+        const bool unit_last = j == (s_ctx[b] + kBlockSize - 1) / kBlockSize - 1;
+        const int flags = (ip == seg_s ? 1 : 0) | (ip == seg_e - 1 ? 2 : 0);
+        s_desc[warp][st] = make_int4(u, j, seg | (flags << 28), row);
+        fence_proxy_async_smem();  // earlier generic accesses of this stage come before the refill
+        const uint32_t bar = smem_u32(&full_bar[warp][st]);
+        if (fused_append && unit_last) {
+          // The block that receives this step's token: fetch the token's K and V rows too.
+          mbar_arrive_expect_tx(bar, Shape::kStageBytes + 2 * kRowBytes);
+          const uint32_t sd = smem_u32(wside + st * 2 * kRowBytes);
+          bulk_load(sd, static_cast<const T*>(a.k_new) + static_cast<int64_t>(u) * D, kRowBytes, bar);
+          bulk_load(sd + kRowBytes, static_cast<const T*>(a.v_new) + static_cast<int64_t>(u) * D, kRowBytes, bar);
+          issue_tiles<D>(smem_u32(wring + st * Shape::kStageBytes), bar, &tmap_k, &tmap_v, row, policy);
+        } else {
+          issue_block<D>(smem_u32(wring + st * Shape::kStageBytes), bar, &tmap_k, &tmap_v, row, policy);
+        }
       }
       ++issued;
       ++ip;
     }
     __syncwarp();  // the descriptors written by lane 0 are visible to the warp
-    if (consumed == issued || !ok) break;
+    if (consumed == issued) break;
 
     const int st = consumed % SW;
     if (!mbar_wait(smem_u32(&full_bar[warp][st]), (consumed / SW) & 1)) {  // timed out: flagged
@@ -541,18 +583,35 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
       break;
     }
     const int4 dsc = s_desc[warp][st];
-    const int u = dsc.x, j = dsc.y, sid = dsc.z;
-    const bool first_of_seg = dsc.w & 1, last_of_seg = dsc.w & 2;
+    const int u = dsc.x, j = dsc.y, sid = dsc.z & 0x0FFFFFFF;
+    const bool first_of_seg = (dsc.z >> 28) & 1, last_of_seg = (dsc.z >> 28) & 2;
     const int b = u / Hkv, kvh = u - b * Hkv;
     const int ctx = s_ctx[b];
     const int nb = (ctx + kBlockSize - 1) / kBlockSize;
+    uint8_t* ks = wring + st * Shape::kStageBytes;
+    if (fused_append && j == nb - 1) {
+      // Append: the token at position ctx - 1 goes into this block's row r, in
+      // the staged tile (for this step's attention) and in the pool.
+      const int r = (ctx - 1) % kBlockSize;
+      constexpr int kChunksPerRow = D / 8;
+      if (lane < 2 * kChunksPerRow) {
+        const int v = lane / kChunksPerRow, c16 = lane % kChunksPerRow;
+        const uint4 val = *reinterpret_cast<const uint4*>(wside + st * 2 * kRowBytes + v * kRowBytes + c16 * 16);
+        uint8_t* tile = ks + v * Shape::kTileBytes;
+        *reinterpret_cast<uint4*>(tile + (c16 >> 3) * 2048 + r * 128 + (((c16 & 7) ^ (r & 7)) << 4)) = val;
+        if (dsc.w >= 0) {
+          T* cache = static_cast<T*>(v ? a.v_cache_w : a.k_cache_w);
+          *reinterpret_cast<uint4*>(cache + (static_cast<int64_t>(dsc.w) + r) * D + c16 * 8) = val;
+        }
+      }
+      __syncwarp();
+    }
     if (first_of_seg || j == 0) {
       if (first_of_seg) seg_first_flush = true;
       unit_first_j = j;
       at.load_q(static_cast<const T*>(a.q) + (static_cast<int64_t>(b) * a.num_q_heads + kvh * g) * D, g, lane);
       at.reset();
     }
-    const uint8_t* ks = wring + st * Shape::kStageBytes;
     at.block(ks, ks + Shape::kTileBytes, min(kBlockSize, ctx - j * kBlockSize), a.scale_log2, lane);
     ++consumed;
 
@@ -606,6 +665,7 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
 // decode grid to finish before reading anything.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) merge_persistent_kernel(const DecodeArgs a, int32_t nwarps) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int kPer = D / 32;
   constexpr int kSegPerShare = 1 + Partition::kTailChunks;

@@ -15,9 +15,11 @@ def bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
-def run_gpu_step(w, layer=0, num_splits=0, device="cuda", slots=None):
-    """Append each sequence's new token, then attend.  Returns (out, k_cache,
-    v_cache) as CPU tensors; the workload's own tensors are not modified."""
+def run_gpu_step(w, layer=0, num_splits=0, device="cuda", slots=None, fused=False):
+    """Append each sequence's new token, then attend: with paged_kv_append +
+    paged_decode_attention, or with the single paged_decode_step call when
+    ``fused``.  Returns (out, k_cache, v_cache) as CPU tensors; the workload's
+    own tensors are not modified."""
     kc = w.k_cache[layer].to(device, copy=True)
     vc = w.v_cache[layer].to(device, copy=True)
     q = w.q[layer].to(device)
@@ -28,8 +30,11 @@ def run_gpu_step(w, layer=0, num_splits=0, device="cuda", slots=None):
     slot_t = torch.from_numpy(np.asarray(slots, np.int32)).to(device)
     bt = torch.from_numpy(w.block_tables).to(device)
     cl = torch.from_numpy(w.context_lens).to(device)
-    pkv.paged_kv_append(kn, vn, slot_t, kc, vc)
-    out = pkv.paged_decode_attention(q, kc, vc, bt, cl, w.scale, num_splits=num_splits)
+    if fused:
+        out = pkv.paged_decode_step(q, kn, vn, kc, vc, bt, cl, w.scale, num_splits=num_splits)
+    else:
+        pkv.paged_kv_append(kn, vn, slot_t, kc, vc)
+        out = pkv.paged_decode_attention(q, kc, vc, bt, cl, w.scale, num_splits=num_splits)
     pkv.paged_kv_check_status()
     return out.cpu(), kc.cpu(), vc.cpu()
 

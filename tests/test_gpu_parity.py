@@ -30,8 +30,8 @@ def built():
     pkv_build.build()
 
 
-def full_check(w, num_splits, layer=0, rows=None):
-    out, kc, vc = run_gpu_step(w, layer, num_splits)
+def full_check(w, num_splits, layer=0, rows=None, fused=False):
+    out, kc, vc = run_gpu_step(w, layer, num_splits, fused=fused)
     rk, rv = oracle_caches(w, layer)
     assert np.array_equal(bits(kc), rk), "K append differs from the oracle"
     assert np.array_equal(bits(vc), rv), "V append differs from the oracle"
@@ -41,7 +41,7 @@ def full_check(w, num_splits, layer=0, rows=None):
         rows = [(b, h) for b in range(B) for h in range(H)]
     ref = oracle_rows(w, rk, rv, rows, layer)
     got = np.stack([gpu[b, h] for b, h in rows])
-    assert_close(got, ref, f"{w.spec.name} splits={num_splits}")
+    assert_close(got, ref, f"{w.spec.name} splits={num_splits} fused={fused}")
     return out
 
 
@@ -251,9 +251,8 @@ def test_step_from_host_matches_device_calls():
     dev = torch.device("cuda")
     kc = w.k_cache[0].to(dev, copy=True)
     vc = w.v_cache[0].to(dev, copy=True)
-    slots = pkv.paged_kv_slot_mapping(w.block_tables, w.context_lens)
     host = {"q": w.q[0], "k_new": w.k_new[0], "v_new": w.v_new[0],
-            "slot_mapping": torch.from_numpy(slots), "block_tables": torch.from_numpy(w.block_tables),
+            "block_tables": torch.from_numpy(w.block_tables),
             "context_lens": torch.from_numpy(w.context_lens), "out": torch.empty_like(w.q[0])}
     host = {k: v.contiguous().pin_memory() for k, v in host.items()}
     devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
@@ -368,3 +367,41 @@ def test_persistent_short_and_uneven_batches(lens):
         assert torch.all(out.float() == 0)
         return
     full_check(w, 0)
+
+
+# ---------------------------------------------------------------- fused decode step
+
+@pytest.mark.parametrize("splits", [0, 5])
+@pytest.mark.parametrize("spec", [wl.TINY] + REDUCED, ids=lambda s: s.name)
+def test_fused_step_every_output(spec, splits):
+    """paged_decode_step (append at position L-1 + attention, one call) gives
+    the oracle's append bit for bit and its attention within tolerance."""
+    w = wl.generate(spec, seed=5)
+    for layer in range(len(w.q)):
+        full_check(w, splits, layer, fused=True)
+
+
+def test_fused_step_llama3_8b_full_every_output():
+    full_check(wl.generate(wl.LLAMA3_8B, seed=2, device="cuda"), 0, fused=True)
+
+
+@pytest.mark.parametrize("spec", [wl.LLAMA70B_TAIL, wl.LONG_CTX, wl.MHA_7B_B64], ids=lambda s: s.name)
+def test_fused_step_full_sampled(spec):
+    w = wl.generate(spec, seed=3, device="cuda", layers=1)
+    rows = sample_rows(w, 64) + [(b, 0) for b in range(min(8, w.spec.batch))]
+    full_check(w, 0, rows=sorted(set(rows)), fused=True)
+
+
+@pytest.mark.parametrize("lens", [(1,), (5, 0, 7), (16,) * 3, (17, 1, 33), (4096, 1, 1, 1)])
+def test_fused_step_edge_lengths(lens):
+    w = _custom(lens, spec=wl.LLAMA3_8B.replace(num_q_heads=8, num_kv_heads=2))
+    full_check(w, 0, fused=True)
+
+
+def test_fused_and_separate_steps_give_identical_bits():
+    w = wl.generate(wl.LLAMA3_8B.replace(batch=12), seed=9)
+    a, ka, va = run_gpu_step(w, 0, 0, fused=False)
+    b, kb, vb = run_gpu_step(w, 0, 0, fused=True)
+    assert torch.equal(ka.view(torch.int16), kb.view(torch.int16))
+    assert torch.equal(va.view(torch.int16), vb.view(torch.int16))
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
