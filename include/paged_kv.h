@@ -173,6 +173,31 @@ int paged_decode_step_from_host(const pkv_step_buffers* bufs, void* k_cache, voi
                                 void* workspace, size_t workspace_bytes,
                                 const pkv_dims* dims, void* stream);
 
+/*
+ * Paged decode attention that allocates nothing (device).  There is no
+ * counterpart on the pages: this is a convenience of this library.  It is for
+ * callers that cannot allocate device memory when they run attention: plugin
+ * hosts that forbid allocation while enqueuing work, processes whose device
+ * memory another allocator already holds in full, and latency-critical paths
+ * that cannot take cudaMalloc's implicit synchronisation.  Same inputs, output
+ * and result as paged_decode_attention with the split kernels (num_splits 0 =
+ * 512-token splits, n >= 1 = n splits), but the split scratch is a fixed
+ * 16 MiB array in the library's device memory, held on every GPU that loads
+ * the library until the process exits.
+ *  - A batch needing more than 16 MiB of scratch (num_seqs * num_q_heads *
+ *    splits * (head_dim + 1) * 4 bytes, each region rounded up to 256) is
+ *    rejected with PKV_ERR_INVALID_ARG and a message giving both sizes.
+ *  - The first call on a device looks up the array's device address (with that
+ *    device current); make that first call before any stream capture.
+ *  - Every call on a device shares the one array and nothing in it needs to
+ *    start at zero, but calls that overlap on the GPU (other streams, other
+ *    host threads) race on it: serialise them, e.g. on one stream.
+ */
+int paged_decode_attention_no_alloc(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, const int32_t* context_lens,
+                                    float scale, void* out, int32_t num_splits,
+                                    const pkv_dims* dims, void* stream);
+
 /* Synchronises `stream`, then reads and clears this device's error word.
  * Returns PKV_OK, PKV_ERR_OUT_OF_RANGE, PKV_ERR_TIMEOUT or PKV_ERR_CUDA. */
 int paged_kv_check_status(void* stream);

@@ -5,12 +5,14 @@ behind a C ABI), plus the host block allocator that produces the tables.
 The shared library loads lazily on the first call; if it has not been built
 every call raises (there is no fallback implementation)."""
 from .api import (BlockAllocator, PagedKVError, make_workspace, paged_decode_attention,
+                  paged_decode_attention_no_alloc,
                   paged_decode_resolve_splits, paged_decode_step, paged_decode_step_from_host,
                   paged_decode_workspace_bytes,
                   paged_kv_append, paged_kv_check_status, paged_kv_slot_mapping)
 
 __all__ = [
-    "BlockAllocator", "PagedKVError", "make_workspace", "paged_decode_attention", "paged_decode_resolve_splits",
+    "BlockAllocator", "PagedKVError", "make_workspace", "paged_decode_attention",
+    "paged_decode_attention_no_alloc", "paged_decode_resolve_splits",
     "paged_decode_step", "paged_decode_step_from_host", "paged_decode_workspace_bytes", "paged_kv_append",
     "paged_kv_check_status", "paged_kv_slot_mapping",
 ]

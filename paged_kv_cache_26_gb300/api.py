@@ -132,6 +132,29 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     return out
 
 
+def paged_decode_attention_no_alloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                    block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                                    out: torch.Tensor, num_splits: int = 0, stream=None) -> torch.Tensor:
+    """paged_decode_attention for callers that cannot allocate device memory
+    while they run (plugin hosts that forbid it, processes whose memory another
+    allocator holds, latency paths that cannot take cudaMalloc's
+    synchronisation): the split scratch is a fixed 16 MiB array inside the
+    library, so neither this wrapper nor the library allocates; ``out`` must be
+    supplied.  Calls that overlap on the GPU share that array and race."""
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out)):
+        _need_cuda(n, t, k_cache.dtype)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    if out.shape != q.shape or q.dim() != 3 or q.shape[2] != k_cache.shape[3]:
+        raise ValueError("q / out must be [num_seqs][num_q_heads][head_dim]")
+    dims = make_dims(q, k_cache, block_tables)
+    _check(lib().paged_decode_attention_no_alloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                                 _ptr(context_lens), float(scale), _ptr(out), num_splits,
+                                                 ctypes.byref(dims), _stream(stream)),
+           "paged_decode_attention_no_alloc")
+    return out
+
+
 def paged_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
                       v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
                       out: Optional[torch.Tensor] = None, num_splits: int = 0,

@@ -486,3 +486,76 @@ int paged_kv_check_status(void* stream_v) {
 const char* paged_kv_last_error(void) { return pkv_error_slot().c_str(); }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ scratch without allocation
+//
+// Some callers cannot allocate device memory at the moment they run attention:
+// plugin hosts that hand a kernel a fixed context and forbid allocation while
+// enqueuing work, processes whose device memory is already reserved in full by
+// another allocator (so a raw cudaMalloc would fail or break that allocator's
+// budget), and latency-critical paths where cudaMalloc's implicit device
+// synchronisation is not acceptable.  paged_decode_attention_no_alloc serves
+// them: its scratch is a fixed array in this library's device memory, so the
+// call allocates nothing.  Every GPU that loads the library holds the array
+// until the process exits.
+
+namespace {
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB per device
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_pkv_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+// Device address of the scratch array for the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device (with that device current) and kept.
+int static_scratch(void** ptr) {
+  static void* addr[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "no_alloc: cudaGetDevice");
+  if (dev >= kMaxDevices) return pkv_fail(PKV_ERR_UNSUPPORTED, "no_alloc: device index too large");
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_pkv_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "no_alloc: cudaGetSymbolAddress(scratch)");
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int paged_decode_attention_no_alloc(const void* q, const void* k_cache, const void* v_cache,
+                                               const int32_t* block_tables, const int32_t* context_lens,
+                                               float scale, void* out, int32_t num_splits, const pkv_dims* dims,
+                                               void* stream) {
+  int rc = check_dims(dims, true);
+  if (rc != PKV_OK) return rc;
+  if (num_splits < 0) return pkv_fail(PKV_ERR_INVALID_ARG, "no_alloc: num_splits must be >= 0");
+  // Always the split kernels: 0 picks 512-token splits.
+  int32_t n = num_splits;
+  if (n == 0) {
+    n = (dims->max_blocks_per_seq + kAutoSplitBlocks - 1) / kAutoSplitBlocks;
+    if (n < 1) n = 1;
+  }
+  SplitPlan plan;
+  rc = plan_splits(dims, n, &plan);
+  if (rc != PKV_OK) return rc;
+  const size_t need = workspace_layout(dims, plan).total();
+  if (need > kStaticScratchBytes)
+    return pkv_fail(PKV_ERR_INVALID_ARG,
+                    "no_alloc: this batch needs " + std::to_string(need) +
+                        " bytes of split scratch; the library's static scratch holds " +
+                        std::to_string(kStaticScratchBytes) + " (use fewer splits or paged_decode_attention)");
+  void* scratch = nullptr;
+  rc = static_scratch(&scratch);
+  if (rc != PKV_OK) return rc;
+  return decode_impl(q, nullptr, nullptr, const_cast<void*>(k_cache), const_cast<void*>(v_cache), block_tables,
+                     context_lens, scale, out, n, scratch, kStaticScratchBytes, dims,
+                     static_cast<cudaStream_t>(stream));
+}
