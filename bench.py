@@ -102,7 +102,7 @@ def kernel_source_hash() -> str:
 def ncu_traffic(workload: str):
     """DRAM bytes per decode launch from the committed ncu summary of this
     workload, if it was captured from the current kernel sources."""
-    path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"decode_persistent_kernel_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
