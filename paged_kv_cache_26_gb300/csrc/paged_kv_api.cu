@@ -166,10 +166,10 @@ int plan_splits(const pkv_dims* d, int32_t requested, SplitPlan* plan) {
   return PKV_OK;
 }
 
-// Workspace regions: [partial outputs][partial log-sum-exps][block prefix][scheduler counters].
+// Workspace regions: [partial outputs][partial log-sum-exps][scheduler counters].
 struct WorkspaceLayout {
-  size_t o_bytes = 0, lse_bytes = 0, plan_bytes = 0, sched_bytes = 0;
-  size_t total() const { return o_bytes + lse_bytes + plan_bytes + sched_bytes; }
+  size_t o_bytes = 0, lse_bytes = 0, sched_bytes = 0;
+  size_t total() const { return o_bytes + lse_bytes + sched_bytes; }
 };
 
 // Segments of the persistent partition for the largest grid (one CTA per SM).
@@ -183,7 +183,6 @@ WorkspaceLayout workspace_layout(const pkv_dims* d, const SplitPlan& p) {
     const size_t seg = persistent_segments();
     w.o_bytes = align256(seg * 2 * pkv::kMaxGroup * d->head_dim * sizeof(float));
     w.lse_bytes = align256(seg * 2 * pkv::kMaxGroup * sizeof(float));
-    w.plan_bytes = align256((static_cast<size_t>(d->num_seqs) + 1) * sizeof(int32_t));
     w.sched_bytes = 256;
   } else if (p.num_splits > 1) {
     const size_t rows = static_cast<size_t>(d->num_seqs) * d->num_q_heads * p.num_splits;
@@ -239,12 +238,15 @@ int launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::Decod
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, mk, mv, args);
     if (e != cudaSuccess) return cuda_fail(e, "decode_persistent_kernel launch");
+    constexpr auto merge = pkv::merge_persistent_kernel<T, D>;
+    const int merge_smem = static_cast<int>((2 * static_cast<size_t>(kMaxPersistentSeqs) + 1) * 4);
+    e = configure_smem<merge>(merge_smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_persistent_kernel)");
     const int rows = d->num_seqs * d->num_q_heads;
-    cfg.gridDim = dim3((rows + 3) / 4);
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = 0;
-    e = cudaLaunchKernelEx(&cfg, pkv::merge_persistent_kernel<T, D>, args,
-                           static_cast<int32_t>(grid) * pkv::PersistentShape<D>::kWarps);
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + pkv::kMergeWarps - 1) / pkv::kMergeWarps));
+    cfg.blockDim = dim3(pkv::kMergeWarps * 32);
+    cfg.dynamicSmemBytes = (2 * static_cast<size_t>(d->num_seqs) + 1) * 4;
+    e = cudaLaunchKernelEx(&cfg, merge, args, static_cast<int32_t>(grid) * pkv::PersistentShape<D>::kWarps);
     if (e != cudaSuccess) return cuda_fail(e, "merge_persistent_kernel launch");
   } else {
     constexpr int kSmem = kStages * Shape::kStageBytes + 1024;
@@ -320,8 +322,7 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, void* k_cac
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   args.part_o = need ? reinterpret_cast<float*>(ws) : nullptr;
   args.part_lse = need ? reinterpret_cast<float*>(ws + wl.o_bytes) : nullptr;
-  args.plan = wl.plan_bytes ? reinterpret_cast<int32_t*>(ws + wl.o_bytes + wl.lse_bytes) : nullptr;
-  args.sched = wl.sched_bytes ? reinterpret_cast<int32_t*>(ws + wl.o_bytes + wl.lse_bytes + wl.plan_bytes) : nullptr;
+  args.sched = wl.sched_bytes ? reinterpret_cast<int32_t*>(ws + wl.o_bytes + wl.lse_bytes) : nullptr;
   args.block_tables = block_tables;
   args.context_lens = context_lens;
   args.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);

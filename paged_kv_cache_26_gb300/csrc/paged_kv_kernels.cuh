@@ -268,7 +268,6 @@ struct DecodeArgs {
   const int32_t* context_lens;
   float* part_o;              // split: f32[B][Hq][splits][D]; persistent: f32[segments][2][8][D]
   float* part_lse;            // split: f32[B][Hq][splits];    persistent: f32[segments][2][8]
-  int32_t* plan;              // persistent: int32[B+1] block prefix, written by the decode kernel
   int32_t* sched;             // persistent: int32[2] chunk counter and finished-warp counter, zero between calls
   const void* k_new;          // fused append (persistent only): T[B][Hkv][D], or null for no append
   const void* v_new;
@@ -452,8 +451,6 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
   // From here on this grid reads the cache and writes the workspace and out,
   // which the previous kernels in the stream (append, merge) touch.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (blockIdx.x == 0)  // the merge kernel reads the prefix
-    for (int b = tid; b <= B; b += NW * 32) a.plan[b] = s_P[b];
 
   const Partition part(Hkv * s_P[B], gridDim.x * NW);
   const int gw = blockIdx.x * NW + warp;
@@ -657,92 +654,114 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
 }
 
 // Merge of the pieces the persistent kernel left: one warp per (sequence,
-// query head).  Units wholly inside one segment were written by the decode
-// kernel; an empty context gives a zero row.  The unit's blocks [U, U+nb)
-// overlap shares w0..w1, each holding 5 segments (head + 4 tail chunks); lanes
-// test those candidates in parallel, then accumulate the overlapping pieces.
-// Launched as a programmatic dependent of the decode kernel: it waits for the
-// decode grid to finish before reading anything.
+// query head) row (warps stride over rows if the grid is smaller).  Units
+// wholly inside one segment were written by the decode kernel; an empty
+// context gives a zero row.  Everything that depends only on the inputs (the block prefix of the
+// contexts) is computed before griddepcontrol.wait, while the decode grid is
+// still running; after it, only the partials are read.  The unit's blocks
+// [U, U+nb) overlap shares w0..w1 of 5 segments each; lanes test those
+// candidates in parallel, the overlapping ones are compacted into a list, and
+// their rows are accumulated with independent loads.
+// Small CTAs (4 warps at <= 64 registers, 8 K registers): one fits beside a
+// decode CTA, and the grid covers every row at once.
+constexpr int kMergeWarps = 4;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(128) merge_persistent_kernel(const DecodeArgs a, int32_t nwarps) {
+__global__ void __launch_bounds__(kMergeWarps * 32, 8)
+    merge_persistent_kernel(const DecodeArgs a, int32_t nwarps) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int kPer = D / 32;
   constexpr int kSegPerShare = 1 + Partition::kTailChunks;
-  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= a.num_seqs * a.num_q_heads) return;
-  const int b = row / a.num_q_heads, hq = row - b * a.num_q_heads;
-  const int kvh = hq / a.group, h = hq - kvh * a.group;
-  const int ctx = clamped_context(a.context_lens, b, a.max_blocks, false);
-  const int nb = (ctx + kBlockSize - 1) / kBlockSize;
-  T* dst = static_cast<T*>(a.out) + static_cast<int64_t>(row) * D + lane * kPer;
-  if (nb == 0) {
-#pragma unroll
-    for (int k = 0; k < kPer; k += 2) *reinterpret_cast<uint32_t*>(dst + k) = 0u;
-    return;
-  }
-  const Partition part(a.num_kv_heads * a.plan[a.num_seqs], nwarps);
-  const int U = a.num_kv_heads * a.plan[b] + kvh * nb, Uend = U + nb;
-  {
-    int s, e;
-    part.segment_of(U, s, e);
-    if (e >= Uend) return;  // one segment: the decode kernel wrote it
-  }
-  const int w0 = U / part.R, ncand = (( Uend - 1) / part.R - w0 + 1) * kSegPerShare;
+  extern __shared__ int merge_smem[];
+  __shared__ int s_warp_sum[kMergeWarps];
+  __shared__ int64_t s_row[kMergeWarps][32];
+  __shared__ float s_w[kMergeWarps][32];
+  int* s_P = merge_smem;
+  int* s_ctx = s_P + a.num_seqs + 1;
+  context_prefix(a, s_P, s_ctx, s_warp_sum, kMergeWarps * 32, false);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // Candidate c: share w0 + c / 5, segment c % 5 of it.  Returns the partial's
-  // row index (slot included), or -1 when the segment does not overlap the unit.
-  auto piece = [&](int c) -> int64_t {
-    const int w = w0 + c / kSegPerShare, k = c % kSegPerShare;
-    int s, e, sid;
-    if (k == 0) {
-      part.head(w, s, e);
-      sid = w;
-    } else {
-      part.chunk(k - 1, w, s, e);
-      sid = part.nwarps + (k - 1) * part.nwarps + w;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hkv = a.num_kv_heads;
+  const Partition part(Hkv * s_P[a.num_seqs], nwarps);
+  const int rows = a.num_seqs * a.num_q_heads;
+  for (int row = blockIdx.x * kMergeWarps + warp; row < rows; row += gridDim.x * kMergeWarps) {
+    const int b = row / a.num_q_heads, hq = row - b * a.num_q_heads;
+    const int kvh = hq / a.group, h = hq - kvh * a.group;
+    const int nb = (s_ctx[b] + kBlockSize - 1) / kBlockSize;
+    T* dst = static_cast<T*>(a.out) + static_cast<int64_t>(row) * D + lane * kPer;
+    if (nb == 0) {
+#pragma unroll
+      for (int k = 0; k < kPer; k += 2) *reinterpret_cast<uint32_t*>(dst + k) = 0u;
+      continue;
     }
-    if (e <= s || e <= U || s >= Uend) return -1;
-    return (static_cast<int64_t>(sid) * 2 + (U > s ? 1 : 0)) * kMaxGroup + h;
-  };
-
-  float M = -INFINITY;
-  for (int c = lane; c < ncand; c += 32) {
-    const int64_t pr = piece(c);
-    if (pr >= 0) M = fmaxf(M, a.part_lse[pr]);
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-
-  float o[kPer];
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) o[k] = 0.f;
-  float L = 0.f;
-  for (int base = 0; base < ncand; base += 32) {
-    const int64_t pr = base + lane < ncand ? piece(base + lane) : -1;
-    const float w = pr >= 0 ? exp2f(a.part_lse[pr] - M) : 0.f;
-    L += w;
-    const int cnt = min(32, ncand - base);
-#pragma unroll 4
-    for (int i = 0; i < cnt; ++i) {
-      const float wi = __shfl_sync(0xffffffffu, w, i);
-      const int64_t pi = __shfl_sync(0xffffffffu, pr, i);
-      if (pi < 0) continue;
-      const float* src = a.part_o + pi * D + lane * kPer;
-#pragma unroll
-      for (int k = 0; k < kPer; k += 2) {
-        const float2 v = *reinterpret_cast<const float2*>(src + k);
-        o[k] += wi * v.x;
-        o[k + 1] += wi * v.y;
+    const int U = Hkv * s_P[b] + kvh * nb, Uend = U + nb;
+    {
+      int s, e;
+      part.segment_of(U, s, e);
+      if (e >= Uend) continue;  // one segment: the decode kernel wrote it
+    }
+    const int w0 = U / part.R, ncand = ((Uend - 1) / part.R - w0 + 1) * kSegPerShare;
+    auto piece = [&](int c) -> int64_t {
+      const int w = w0 + c / kSegPerShare, k = c % kSegPerShare;
+      int s, e, sid;
+      if (k == 0) {
+        part.head(w, s, e);
+        sid = w;
+      } else {
+        part.chunk(k - 1, w, s, e);
+        sid = part.nwarps + (k - 1) * part.nwarps + w;
       }
+      if (e <= s || e <= U || s >= Uend) return -1;
+      return (static_cast<int64_t>(sid) * 2 + (U > s ? 1 : 0)) * kMaxGroup + h;
+    };
+
+    float M = -INFINITY;
+    for (int c = lane; c < ncand; c += 32) {
+      const int64_t pr = piece(c);
+      if (pr >= 0) M = fmaxf(M, __ldcg(a.part_lse + pr));
     }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+
+    float o[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) o[k] = 0.f;
+    float L = 0.f;
+    for (int base = 0; base < ncand; base += 32) {
+      const int64_t pr = base + lane < ncand ? piece(base + lane) : -1;
+      const float w = pr >= 0 ? exp2f(__ldcg(a.part_lse + pr) - M) : 0.f;
+      L += w;
+      const unsigned valid = __ballot_sync(0xffffffffu, pr >= 0);
+      if (pr >= 0) {
+        const int rank = __popc(valid & ((1u << lane) - 1));
+        s_row[warp][rank] = pr;
+        s_w[warp][rank] = w;
+      }
+      __syncwarp();
+      const int cnt = __popc(valid);
+#pragma unroll 4
+      for (int i = 0; i < cnt; ++i) {
+        const float wi = s_w[warp][i];
+        const float* src = a.part_o + s_row[warp][i] * D + lane * kPer;
+        float v[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; k += 2) {
+          const float2 x = __ldcg(reinterpret_cast<const float2*>(src + k));
+          v[k] = x.x;
+          v[k + 1] = x.y;
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) o[k] += wi * v[k];
+      }
+      __syncwarp();
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    const float inv = 1.0f / L;
+#pragma unroll
+    for (int k = 0; k < kPer; k += 2) *reinterpret_cast<uint32_t*>(dst + k) = pack2<T>(o[k] * inv, o[k + 1] * inv);
   }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-  const float inv = 1.0f / L;
-#pragma unroll
-  for (int k = 0; k < kPer; k += 2) *reinterpret_cast<uint32_t*>(dst + k) = pack2<T>(o[k] * inv, o[k + 1] * inv);
 }
 
 // ===================================================================== split kernel
