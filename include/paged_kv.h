@@ -46,6 +46,15 @@
  *
  * Every function returns PKV_OK (0) or a negative PKV_ERR_* code;
  * paged_kv_last_error() gives a message for the calling thread's last failure.
+ *
+ * The automatic (persistent) attention path launches its kernels as
+ * programmatic dependents of the kernel before them in the stream: they may
+ * start while that kernel finishes, and read their inputs q, block_tables and
+ * context_lens before waiting for it; the cache, the workspace and out are
+ * touched only after the wait.  A kernel that writes those inputs right
+ * before the call and signals programmatic launch completion early
+ * (cudaTriggerProgrammaticLaunchCompletion) must not do so before it has
+ * written them; kernels that never signal it, and copies, are always safe.
  */
 #ifndef PAGED_KV_H_
 #define PAGED_KV_H_

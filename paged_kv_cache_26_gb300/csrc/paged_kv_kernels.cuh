@@ -446,11 +446,9 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
     for (int s = 0; s < SW; ++s) mbar_init(smem_u32(&full_bar[warp][s]), 1);
     fence_mbar_init();
   }
-  // Inputs only (context lengths): safe before the previous kernel has finished.
+  // Inputs only (context lengths, and below the block tables and query rows)
+  // are read before the wait for the previous kernel in the stream.
   context_prefix(a, s_P, s_ctx, s_warp_sum, NW * 32, blockIdx.x == 0);
-  // From here on this grid reads the cache and writes the workspace and out,
-  // which the previous kernels in the stream (append, merge) touch.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const Partition part(Hkv * s_P[B], gridDim.x * NW);
   const int gw = blockIdx.x * NW + warp;
@@ -532,6 +530,12 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
       }
     }
   };
+
+  // First window of the head (block-table and query inputs only), then wait:
+  // from here on this grid reads the cache and writes the workspace and out,
+  // which the previous kernels in the stream (append, merge) touch.
+  if (ip < seg_e) fill_window();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- consume side
   WarpAttn<T, D> at;
@@ -716,48 +720,58 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 8)
       return (static_cast<int64_t>(sid) * 2 + (U > s ? 1 : 0)) * kMaxGroup + h;
     };
 
-    float M = -INFINITY;
-    for (int c = lane; c < ncand; c += 32) {
-      const int64_t pr = piece(c);
-      if (pr >= 0) M = fmaxf(M, __ldcg(a.part_lse + pr));
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-
-    float o[kPer];
+    // Pieces are folded in with a running log-sum-exp, in batches of up to 32
+    // candidates; within a batch the log-sum-exps and the partial rows are
+    // loaded together (one round trip), at most kBatch rows in flight.
+    constexpr int kBatch = 8;
+    float m = -INFINITY, L = 0.f, o[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) o[k] = 0.f;
-    float L = 0.f;
     for (int base = 0; base < ncand; base += 32) {
       const int64_t pr = base + lane < ncand ? piece(base + lane) : -1;
-      const float w = pr >= 0 ? exp2f(__ldcg(a.part_lse + pr) - M) : 0.f;
-      L += w;
       const unsigned valid = __ballot_sync(0xffffffffu, pr >= 0);
-      if (pr >= 0) {
-        const int rank = __popc(valid & ((1u << lane) - 1));
-        s_row[warp][rank] = pr;
-        s_w[warp][rank] = w;
-      }
+      const int rank = __popc(valid & ((1u << lane) - 1));
+      if (pr >= 0) s_row[warp][rank] = pr;
+      const float lse = pr >= 0 ? __ldcg(a.part_lse + pr) : -INFINITY;
       __syncwarp();
       const int cnt = __popc(valid);
-#pragma unroll 4
-      for (int i = 0; i < cnt; ++i) {
-        const float wi = s_w[warp][i];
-        const float* src = a.part_o + s_row[warp][i] * D + lane * kPer;
-        float v[kPer];
+      for (int i0 = 0; i0 < cnt; i0 += kBatch) {
+        float v[kBatch][kPer];
 #pragma unroll
-        for (int k = 0; k < kPer; k += 2) {
-          const float2 x = __ldcg(reinterpret_cast<const float2*>(src + k));
-          v[k] = x.x;
-          v[k + 1] = x.y;
+        for (int i = 0; i < kBatch; ++i) {
+          if (i0 + i < cnt) {
+            const float* src = a.part_o + s_row[warp][i0 + i] * D + lane * kPer;
+#pragma unroll
+            for (int k = 0; k < kPer; k += 2) {
+              const float2 x = __ldcg(reinterpret_cast<const float2*>(src + k));
+              v[i][k] = x.x;
+              v[i][k + 1] = x.y;
+            }
+          }
         }
+        if (i0 == 0 && pr >= 0) s_w[warp][rank] = lse;  // the batch's log-sum-exps, by rank
+        __syncwarp();
+        float mb = m;
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) o[k] += wi * v[k];
+        for (int i = 0; i < kBatch; ++i)
+          if (i0 + i < cnt) mb = fmaxf(mb, s_w[warp][i0 + i]);
+        const float sc = exp2f(m - mb);
+        L *= sc;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) o[k] *= sc;
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          if (i0 + i < cnt) {
+            const float w = exp2f(s_w[warp][i0 + i] - mb);
+            L += w;
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) o[k] += w * v[i][k];
+          }
+        }
+        m = mb;
       }
       __syncwarp();
     }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
     const float inv = 1.0f / L;
 #pragma unroll
     for (int k = 0; k < kPer; k += 2) *reinterpret_cast<uint32_t*>(dst + k) = pack2<T>(o[k] * inv, o[k + 1] * inv);
