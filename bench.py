@@ -423,6 +423,89 @@ def run_ours(args, rank, world, local):
         print(json.dumps(result), flush=True)
 
 
+# ----------------------------------------------------------------------------- continuous batching
+
+def run_loop(args, rank, world, local):
+    """Continuous batching at this configuration's shape: args.batch (or the
+    configuration's batch) slots; prompts drawn from its length law, 32..256
+    generated tokens each; finished sequences leave and waiting ones are
+    admitted every step.  Reports steps/s, generated tokens/s, attention GB/s
+    and the allocator's unused tail per sequence."""
+    from paged_kv_cache_26_gb300 import build as pkv_build
+    from paged_kv_cache_26_gb300.loop import DecodeLoop
+    import paged_kv_cache_26_gb300 as pkv
+
+    pkv_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    spec = wl.CONFIGS[args.config]
+    B = args.batch or spec.batch
+    dt = wl.DTYPES[spec.dtype]
+    rng = np.random.default_rng(args.seed + rank)
+    max_prompt = int(wl.draw_lengths(spec.replace(batch=4096), np.random.default_rng(1)).max())
+    max_ctx = max_prompt + 256
+    num_blocks = int(math.ceil(1.25 * B * max_ctx / 16))
+    loop = DecodeLoop(num_blocks, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, B, max_ctx, dt, dev,
+                      args.seed + rank)
+    g = torch.Generator(device=dev).manual_seed(args.seed + rank)
+    prompt_k = torch.randn(max_prompt, spec.num_kv_heads, spec.head_dim, generator=g, device=dev).to(dt)
+    prompt_v = torch.randn_like(prompt_k)
+    q = torch.randn(B, spec.num_q_heads, spec.head_dim, generator=g, device=dev).to(dt)
+    kn = torch.randn(B, spec.num_kv_heads, spec.head_dim, generator=g, device=dev).to(dt)
+    vn = torch.randn_like(kn)
+    counts = {"admitted": 0, "retired": 0}
+
+    def admit_all():
+        while loop.free_slots().size:
+            P = int(wl.draw_lengths(spec.replace(batch=1), rng)[0])
+            if loop.admit(prompt_k[:P], prompt_v[:P], int(rng.integers(32, 257))) is None:
+                break
+            counts["admitted"] += 1
+
+    def one_step():
+        admit_all()
+        loop.step(q, kn, vn)
+        L = loop.context_lengths()
+        counts["retired"] += len(loop.finish_step())
+        return L
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    counts.update(admitted=0, retired=0)
+    kv_bytes, tokens, waste = 0, 0, []
+    barrier(world)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    start.record()
+    for _ in range(args.steps):
+        L = one_step()
+        kv_bytes += attention_bytes(L, B, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, 2)
+        tokens += int((L > 0).sum())
+        waste.append(loop.waste_blocks())
+    end.record()
+    torch.cuda.synchronize()
+    wall_s = time.perf_counter() - t0
+    pkv.paged_kv_check_status()
+    gpu_s = max_over_ranks(start.elapsed_time(end) * 1e-3, world, dev)
+    wall_s = max_over_ranks(wall_s, world, dev)
+    if rank == 0:
+        print(json.dumps({
+            "metric": "continuous-batching decode steps/s (paged_decode_step per step, host scheduling included)",
+            "value": round(world * args.steps / wall_s, 2), "unit": "steps/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall_s / args.steps * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "dtype": spec.dtype, "data": "synthetic",
+            "config": {"workload": f"{spec.name} continuous batching", "batch_slots": B,
+                       "prompt_lengths": str(spec.lengths), "generated_tokens": "U[32,256]",
+                       "num_blocks": num_blocks},
+            "generated_tokens_per_s": round(world * tokens / wall_s, 1),
+            "attention_GBs": round(world * kv_bytes / wall_s / 1e9, 1),
+            "gpu_busy_frac": round(gpu_s / wall_s, 3),
+            "mean_unused_tail_blocks": round(float(np.mean(waste)), 3),
+            "admitted": counts["admitted"], "retired": counts["retired"],
+        }), flush=True)
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args, rank, world):
@@ -477,12 +560,15 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds of oracle work for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--loop", action="store_true", help="continuous-batching loop instead of the fixed batch")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.loop:
+        run_loop(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:

@@ -249,6 +249,21 @@ int block_allocator_fork_prefix(pkv_block_allocator* a, int32_t src_seq, int32_t
  * token would land in a partly filled block that another sequence shares. */
 int block_allocator_append_slot(pkv_block_allocator* a, int32_t seq_id, int32_t* slot);
 
+/* One decode step's growth for a batch: block_allocator_append_slot for each
+ * of seq_ids[0..n), slots[i] receiving sequence i's new slot.  All or nothing:
+ * PKV_ERR_NO_BLOCKS / PKV_ERR_SHARED_BLOCK / PKV_ERR_INVALID_ARG (a sequence
+ * not live or listed twice) leave the allocator unchanged. */
+int block_allocator_append_slots(pkv_block_allocator* a, const int32_t* seq_ids, int32_t n, int32_t* slots);
+
+/* The host side of one continuous-batching decode step, in one call: for a
+ * batch of n slots (slot_seq_ids[i] = a live sequence, or -1 for an empty
+ * slot) grow every listed sequence by one token and write row i of
+ * tables (int32[n][max_blocks], -1 padded) and context_lens[i] (0 for an empty
+ * slot).  All or nothing, like block_allocator_append_slots; also
+ * PKV_ERR_INVALID_ARG if a sequence would outgrow max_blocks. */
+int block_allocator_step_batch(pkv_block_allocator* a, const int32_t* slot_seq_ids, int32_t n, int32_t max_blocks,
+                               int32_t* tables, int32_t* context_lens);
+
 /* Drop seq_id; blocks whose count reaches zero return to the pool. */
 int block_allocator_free_seq(pkv_block_allocator* a, int32_t seq_id);
 
@@ -263,6 +278,53 @@ int32_t block_allocator_num_free(const pkv_block_allocator* a);
 int32_t block_allocator_refcount(const pkv_block_allocator* a, int32_t block);
 /* Tokens held by a live sequence; -1 if seq_id is not live. */
 int32_t block_allocator_seq_len(const pkv_block_allocator* a, int32_t seq_id);
+
+/* ------------------------------------------------------------------------
+ * Continuous-batching decode engine (host; the kernels it launches are the
+ * ones above).  A fixed number of batch slots over one block allocator: a
+ * sequence is admitted with its prompt's K/V, grows by one token per step
+ * (a new block when its last one fills), and frees its blocks when its
+ * generation budget is spent, so later sequences reuse them (kasblo.com
+ * "vLLMとは？" section "blockはrequestの成長に合わせて割り当てる"; magi "Inference
+ * Batching", continuous batching).  One call does a step's host work: growth
+ * of every active sequence, export of every table row into pinned host
+ * staging, the asynchronous copies, and the launch of paged_decode_step.
+ * The engine allocates pinned host memory only; device buffers are the
+ * caller's.  Not thread-safe; one stream per engine.
+ * ---------------------------------------------------------------------- */
+typedef struct pkv_decode_engine pkv_decode_engine;
+
+/* alloc stays owned by the caller and must outlive the engine.  Returns NULL
+ * on a bad argument or if pinned host staging cannot be allocated. */
+pkv_decode_engine* decode_engine_create(pkv_block_allocator* alloc, int32_t max_batch, int32_t max_blocks_per_seq);
+void decode_engine_destroy(pkv_decode_engine* e);
+
+/* Admit a sequence whose prompt_tokens K/V rows (prompt_k, prompt_v: device,
+ * T[prompt_tokens][Hkv][D]) are written into the cache through a slot-mapped
+ * append, and which will take gen_tokens decode steps.  slot_staging_dev is a
+ * device int32 buffer of 4 * max_blocks_per_seq * 16 entries the engine uses
+ * for the prompts' slot mappings.  *batch_slot receives the slot (-1 and
+ * PKV_ERR_NO_BLOCKS when no slot or too few blocks are free). */
+int decode_engine_admit(pkv_decode_engine* e, int32_t prompt_tokens, int32_t gen_tokens, const void* prompt_k,
+                        const void* prompt_v, void* k_cache, void* v_cache, int32_t* slot_staging_dev,
+                        const pkv_dims* dims, void* stream, int32_t* batch_slot);
+
+/* One decode step for every active slot: tables_dev (int32[max_batch][max_blocks_per_seq])
+ * and lens_dev (int32[max_batch]) receive the step's tables, then
+ * paged_decode_step runs with q / k_new / v_new / out covering all max_batch
+ * slots (empty slots: context 0, zero output, nothing appended) and
+ * num_splits 0.  dims->num_seqs must be max_batch. */
+int decode_engine_step(pkv_decode_engine* e, int32_t* tables_dev, int32_t* lens_dev, const void* q,
+                       const void* k_new, const void* v_new, void* k_cache, void* v_cache, float scale, void* out,
+                       void* workspace, size_t workspace_bytes, const pkv_dims* dims, void* stream);
+
+/* Count the step against every active sequence; those that spent their
+ * budget free their blocks.  freed_slots (host, max_batch entries) receives
+ * their slots, *num_freed how many. */
+int decode_engine_finish(pkv_decode_engine* e, int32_t* freed_slots, int32_t* num_freed);
+
+/* Host view: sequence id (or -1) and current context length of every slot. */
+int decode_engine_state(const pkv_decode_engine* e, int32_t* slot_seq_ids, int32_t* context_lens);
 
 #ifdef __cplusplus
 }

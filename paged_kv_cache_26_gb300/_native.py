@@ -51,10 +51,24 @@ _SIGNATURES = {
     "block_allocator_fork_prefix": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                    c_int32_p]),
     "block_allocator_append_slot": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, c_int32_p]),
+    "block_allocator_append_slots": (ctypes.c_int, [ctypes.c_void_p, c_int32_p, ctypes.c_int32, c_int32_p]),
+    "block_allocator_step_batch": (ctypes.c_int, [ctypes.c_void_p, c_int32_p, ctypes.c_int32, ctypes.c_int32,
+                                                  c_int32_p, c_int32_p]),
     "block_allocator_free_seq": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
     "block_allocator_block_tables": (ctypes.c_int, [ctypes.c_void_p, c_int32_p, ctypes.c_int32, ctypes.c_int32,
                                                     c_int32_p, c_int32_p]),
     "block_allocator_num_free": (ctypes.c_int32, [ctypes.c_void_p]),
+    "decode_engine_create": (ctypes.c_void_p, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32]),
+    "decode_engine_destroy": (None, [ctypes.c_void_p]),
+    "decode_engine_admit": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                           ctypes.POINTER(PkvDims), ctypes.c_void_p, c_int32_p]),
+    "decode_engine_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                          ctypes.POINTER(PkvDims), ctypes.c_void_p]),
+    "decode_engine_finish": (ctypes.c_int, [ctypes.c_void_p, c_int32_p, c_int32_p]),
+    "decode_engine_state": (ctypes.c_int, [ctypes.c_void_p, c_int32_p, c_int32_p]),
     "block_allocator_refcount": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_int32]),
     "block_allocator_seq_len": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_int32]),
 }

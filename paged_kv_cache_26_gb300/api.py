@@ -260,6 +260,22 @@ class BlockAllocator:
         _check(lib().block_allocator_append_slot(self._h, seq_id, ctypes.byref(slot)), "append_slot")
         return slot.value
 
+    def append_slots(self, seq_ids: Sequence[int], out: Optional[np.ndarray] = None) -> np.ndarray:
+        """One new token for each listed sequence (all or nothing); returns the slots."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+        slots = out if out is not None else np.empty(ids.shape[0], dtype=np.int32)
+        _check(lib().block_allocator_append_slots(self._h, ids.ctypes.data_as(c_int32_p), ids.shape[0],
+                                                  slots.ctypes.data_as(c_int32_p)), "append_slots")
+        return slots
+
+    def step_batch(self, slot_seq_ids: np.ndarray, max_blocks: int, tables: np.ndarray, lens: np.ndarray) -> None:
+        """Grow every live sequence of the batch by one token and write all
+        rows of ``tables`` / ``lens`` (int32, C-contiguous, filled in place)."""
+        ids = np.ascontiguousarray(slot_seq_ids, dtype=np.int32)
+        _check(lib().block_allocator_step_batch(self._h, ids.ctypes.data_as(c_int32_p), ids.shape[0], max_blocks,
+                                                tables.ctypes.data_as(c_int32_p), lens.ctypes.data_as(c_int32_p)),
+               "step_batch")
+
     def free_seq(self, seq_id: int) -> None:
         _check(lib().block_allocator_free_seq(self._h, seq_id), "free_seq")
 

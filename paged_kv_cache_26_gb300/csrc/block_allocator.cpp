@@ -27,8 +27,10 @@ struct pkv_block_allocator {
     std::vector<int32_t> blocks;
     int32_t len = 0;
     bool live = false;
+    uint64_t stamp = 0;  // last batch call that listed this sequence
   };
   std::vector<Seq> seqs;
+  uint64_t batch_calls = 0;
   std::vector<int32_t> dead_ids;    // reusable sequence ids
 
   uint64_t next_u64() {
@@ -140,6 +142,76 @@ int block_allocator_append_slot(pkv_block_allocator* a, int32_t seq_id, int32_t*
   }
   *slot = s.blocks[j] * a->block_size + pos % a->block_size;
   s.len = pos + 1;
+  return PKV_OK;
+}
+
+int block_allocator_append_slots(pkv_block_allocator* a, const int32_t* seq_ids, int32_t n, int32_t* slots) {
+  if (!a || n < 0 || (n > 0 && (!seq_ids || !slots))) return pkv_fail(PKV_ERR_INVALID_ARG, "append_slots: bad argument");
+  // Check first, so that a failure changes nothing: each sequence is live,
+  // appears once, and the pool holds the blocks the batch needs.
+  int32_t need = 0;
+  const uint64_t stamp = ++a->batch_calls;
+  for (int32_t i = 0; i < n; ++i) {
+    if (!a->live(seq_ids[i])) return pkv_fail(PKV_ERR_INVALID_ARG, "append_slots: sequence not live");
+    auto& s = a->seqs[seq_ids[i]];
+    if (s.stamp == stamp) return pkv_fail(PKV_ERR_INVALID_ARG, "append_slots: sequence listed twice");
+    s.stamp = stamp;
+    const int32_t j = s.len / a->block_size;
+    if (j == static_cast<int32_t>(s.blocks.size())) {
+      ++need;
+    } else if (a->refcount[s.blocks[j]] > 1) {
+      return pkv_fail(PKV_ERR_SHARED_BLOCK, "append_slots: a last block is shared with another sequence");
+    }
+  }
+  if (need > static_cast<int32_t>(a->free_list.size()))
+    return pkv_fail(PKV_ERR_NO_BLOCKS, "append_slots: pool has too few free blocks for this step");
+  for (int32_t i = 0; i < n; ++i) {
+    const int rc = block_allocator_append_slot(a, seq_ids[i], &slots[i]);
+    if (rc != PKV_OK) return rc;  // unreachable after the checks above
+  }
+  return PKV_OK;
+}
+
+int block_allocator_step_batch(pkv_block_allocator* a, const int32_t* slot_seq_ids, int32_t n, int32_t max_blocks,
+                               int32_t* tables, int32_t* context_lens) {
+  if (!a || n < 0 || max_blocks < 0 || (n > 0 && (!slot_seq_ids || !tables || !context_lens)))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "step_batch: bad argument");
+  // Same checks as append_slots, plus the table width, before changing anything.
+  int32_t need = 0;
+  const uint64_t stamp = ++a->batch_calls;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t id = slot_seq_ids[i];
+    if (id < 0) continue;
+    if (!a->live(id)) return pkv_fail(PKV_ERR_INVALID_ARG, "step_batch: sequence not live");
+    auto& s = a->seqs[id];
+    if (s.stamp == stamp) return pkv_fail(PKV_ERR_INVALID_ARG, "step_batch: sequence listed twice");
+    s.stamp = stamp;
+    if (a->blocks_for(s.len + 1) > max_blocks)
+      return pkv_fail(PKV_ERR_INVALID_ARG, "step_batch: a sequence would outgrow max_blocks");
+    const int32_t j = s.len / a->block_size;
+    if (j == static_cast<int32_t>(s.blocks.size())) {
+      ++need;
+    } else if (a->refcount[s.blocks[j]] > 1) {
+      return pkv_fail(PKV_ERR_SHARED_BLOCK, "step_batch: a last block is shared with another sequence");
+    }
+  }
+  if (need > static_cast<int32_t>(a->free_list.size()))
+    return pkv_fail(PKV_ERR_NO_BLOCKS, "step_batch: pool has too few free blocks for this step");
+  for (int32_t i = 0; i < n; ++i) {
+    int32_t* row = tables + static_cast<int64_t>(i) * max_blocks;
+    const int32_t id = slot_seq_ids[i];
+    int32_t k = 0;
+    if (id >= 0) {
+      int32_t slot;
+      block_allocator_append_slot(a, id, &slot);  // cannot fail after the checks above
+      const auto& s = a->seqs[id];
+      for (; k < static_cast<int32_t>(s.blocks.size()); ++k) row[k] = s.blocks[k];
+      context_lens[i] = s.len;
+    } else {
+      context_lens[i] = 0;
+    }
+    for (; k < max_blocks; ++k) row[k] = -1;
+  }
   return PKV_OK;
 }
 

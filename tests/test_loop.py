@@ -1,0 +1,138 @@
+"""Continuous batching: the allocator's batched growth (CPU) and a multi-step
+decode loop checked end to end against the oracle (GPU).
+
+The GPU test keeps, on the host, every token each sequence received (its
+prompt plus one token per step).  After many steps with admissions,
+retirements and block reuse, every live sequence's K/V read back through its
+block table must equal that record bit for bit, and the last step's output
+must match the oracle's attention over the record."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_26_gb300 import BlockAllocator, PagedKVError
+from paged_kv_cache_26_gb300 import build as pkv_build
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    pkv_build.build()
+
+
+def test_append_slots_batch_equals_single_appends():
+    a1, a2 = BlockAllocator(50, 16, seed=4), BlockAllocator(50, 16, seed=4)
+    ids1 = [a1.add_seq(n) for n in (0, 15, 16, 31, 40)]
+    ids2 = [a2.add_seq(n) for n in (0, 15, 16, 31, 40)]
+    for _ in range(40):
+        batch = a1.append_slots(ids1)
+        single = [a2.append_slot(s) for s in ids2]
+        assert list(batch) == single
+    assert a1.num_free == a2.num_free
+
+
+def test_append_slots_is_all_or_nothing():
+    a = BlockAllocator(4, 16, seed=0)
+    ids = [a.add_seq(16), a.add_seq(16), a.add_seq(16)]     # 3 of 4 blocks used, all full
+    before = [a.seq_len(s) for s in ids]
+    with pytest.raises(PagedKVError) as e:
+        a.append_slots(ids)                                 # needs 3 new blocks, 1 free
+    assert e.value.code == -5
+    assert [a.seq_len(s) for s in ids] == before and a.num_free == 1
+    with pytest.raises(PagedKVError):
+        a.append_slots([ids[0], ids[0]])                    # listed twice
+    assert a.seq_len(ids[0]) == 16
+    a.free_seq(ids[2])
+    a.append_slots(ids[:2])
+    assert [a.seq_len(s) for s in ids[:2]] == [17, 17]
+
+
+def test_step_batch_grows_and_exports_every_slot():
+    a, b = BlockAllocator(60, 16, seed=8), BlockAllocator(60, 16, seed=8)
+    lens0 = (5, 16, 0, 47)
+    ida = [a.add_seq(n) for n in lens0]
+    idb = [b.add_seq(n) for n in lens0]
+    slot_ids = np.array([ida[0], -1, ida[1], ida[2], -1, ida[3]], np.int32)
+    tables = np.empty((6, 8), np.int32)
+    lens = np.empty(6, np.int32)
+    for _ in range(20):
+        a.step_batch(slot_ids, 8, tables, lens)
+        b.append_slots(idb)
+        t_ref, l_ref = b.block_tables(idb, 8)
+        live = [0, 2, 3, 5]
+        assert np.array_equal(tables[live], t_ref) and np.array_equal(lens[live], l_ref)
+        assert np.all(tables[[1, 4]] == -1) and np.all(lens[[1, 4]] == 0)
+    with pytest.raises(PagedKVError):
+        a.step_batch(slot_ids, 4, np.empty((6, 4), np.int32), lens)   # 47+20 tokens > 4 blocks
+    assert a.seq_len(ida[3]) == 67
+
+
+@pytest.mark.gpu
+def test_decode_loop_end_to_end_against_the_oracle():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_26_gb300.loop import DecodeLoop
+
+    dev = torch.device("cuda")
+    Hq, Hk, D, B = 8, 2, 64, 6
+    rng = np.random.default_rng(0)
+    g = torch.Generator(device=dev).manual_seed(0)
+    loop = DecodeLoop(num_blocks=40, num_q_heads=Hq, num_kv_heads=Hk, head_dim=D, max_batch=B,
+                      max_context=200, dtype=torch.float16, device=dev, seed=3)
+    history = {}                                            # sequence id -> list of (k, v) rows [Hk][D]
+
+    def bits(t):
+        return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+    admitted = retired = 0
+    q = None
+    for step in range(70):
+        # admit while there is room (prompts of 0..45 tokens, 3..30 steps each)
+        while loop.free_slots().size:
+            P = int(rng.integers(0, 46))
+            pk = torch.randn(P, Hk, D, generator=g, device=dev).half()
+            pv = torch.randn(P, Hk, D, generator=g, device=dev).half()
+            slot = loop.admit(pk, pv, int(rng.integers(3, 31)))
+            if slot is None:
+                break
+            sid = int(loop.seq[slot])
+            history[sid] = [(r[0], r[1]) for r in zip(bits(pk), bits(pv))]
+            admitted += 1
+        q = torch.randn(B, Hq, D, generator=g, device=dev).half()
+        kn = torch.randn(B, Hk, D, generator=g, device=dev).half()
+        vn = torch.randn(B, Hk, D, generator=g, device=dev).half()
+        out = loop.step(q, kn, vn)
+        for slot in loop.active_slots():
+            history[int(loop.seq[slot])].append((bits(kn[slot]), bits(vn[slot])))
+        if step < 69:
+            retired += len(loop.finish_step())
+    torch.cuda.synchronize()
+    assert admitted > 2 * B and retired > B                  # sequences came and went, blocks were reused
+    assert loop.waste_blocks() < 1.0
+
+    kc, vc = bits(loop.k_cache), bits(loop.v_cache)
+    tables, lens = loop.tables.cpu().numpy(), loop.lens.cpu().numpy()
+    ref = np.zeros((B, Hq, D))
+    got = oracle.widen(bits(out), "fp16")
+    for slot in range(B):
+        sid = int(loop.seq[slot])
+        if sid < 0:
+            assert lens[slot] == 0 and np.all(got[slot] == 0)
+            continue
+        hist = history[sid]
+        L = len(hist)
+        assert lens[slot] == L
+        for kv in range(Hk):
+            k_rec = np.stack([h[0][kv] for h in hist])
+            v_rec = np.stack([h[1][kv] for h in hist])
+            assert np.array_equal(oracle.gather_kv(kc, tables[slot], L, kv, 16), k_rec)
+            assert np.array_equal(oracle.gather_kv(vc, tables[slot], L, kv, 16), v_rec)
+            for h in range(kv * (Hq // Hk), (kv + 1) * (Hq // Hk)):
+                ref[slot, h] = oracle.attend_one(oracle.widen(bits(q[slot, h]), "fp16"), oracle.widen(k_rec, "fp16"),
+                                                 oracle.widen(v_rec, "fp16"), 1 / math.sqrt(D))[0]
+    assert np.all(np.abs(got - ref) <= 2e-3 + 1e-2 * np.abs(ref))
+    # every block is either free or held by exactly the live sequences' tables
+    live_blocks = set(int(x) for s in range(B) if loop.seq[s] >= 0 for x in tables[s, :math.ceil(lens[s] / 16)])
+    assert loop.alloc.num_free + len(live_blocks) == 40
