@@ -45,7 +45,7 @@ from typing import Iterable, List, Optional, Sequence, Tuple
 import numpy as np
 
 __all__ = [
-    "widen", "kv_head_of", "slot_of_position", "slot_mapping", "kv_append",
+    "widen", "e4m3_decode", "e4m3_encode", "quantize_e4m3", "dequantize_e4m3", "kv_append_fp8", "kv_head_of", "slot_of_position", "slot_mapping", "kv_append",
     "gather_kv", "attend_one", "decode_attention", "decode_attention_rows",
     "split_partials", "lse_merge", "kv_bytes_per_token", "blocks_needed",
     "allocated_bytes", "wasted_bytes", "kv_cache_bytes", "decode_step_tokens_per_s",
@@ -70,6 +70,65 @@ def widen(bits: np.ndarray, dtype: str) -> np.ndarray:
     raise ValueError(f"unknown dtype {dtype!r}")
 
 
+# ---------------------------------------------------------------- fp8 (E4M3) KV codes
+#
+# The FP8 KV cache (design.babushkai.com "GPU推論の内部構造", section "KVキャッシュの
+# 台帳", and youngju.dev, quantization section: an FP8 KV cache halves the
+# bytes per token) stores each K/V element as an E4M3 code with one float32
+# scale per KV head: value = decode(code) * scale.  E4M3 as used for FP8 KV
+# caches: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, no
+# infinities, S.1111.111 = NaN, largest finite 448, subnormals k * 2^-9.
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    """Exact float64 value of each E4M3 code (NaN for S.1111.111)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * 2.0 ** (e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """E4M3 code of each float32 value: round to nearest, ties to even;
+    magnitudes beyond 448 saturate to 448; NaN -> 0x7F."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)   # exact
+    out = np.zeros(x.shape, dtype=np.uint8)
+    sign = (np.signbit(x)).astype(np.uint8) << 7
+    a = np.abs(x)
+    nan = np.isnan(x)
+    # grid spacing at |x|: 2^-9 below the smallest normal 2^-6, else 2^(e-3)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.clip(e, -6, 8)
+    step = 2.0 ** (e - 3)
+    q = np.rint(a / step) * step          # nearest multiple, ties to even (exact in float64)
+    q = np.minimum(q, E4M3_MAX)           # saturate (also catches rounding up past 448)
+    # code of the (representable) magnitude q
+    qe = np.floor(np.log2(np.where(q > 0, q, 1.0)))
+    normal = q >= 2.0 ** -6
+    exp_field = np.where(normal, qe + 7, 0)
+    mant = np.where(normal, np.rint((q / 2.0 ** qe - 1.0) * 8), np.rint(q / 2.0 ** -9))
+    code = (exp_field.astype(np.int64) << 3) | mant.astype(np.int64)
+    out[:] = np.where(nan, 0x7F, code | sign.astype(np.int64))
+    return out
+
+
+def quantize_e4m3(bits: np.ndarray, dtype: str, scale: float) -> np.ndarray:
+    """The append's quantisation of fp16/bf16 values with a float32 scale:
+    code = e4m3(float32(x) / float32(scale)), the division in float32."""
+    x = widen(bits, dtype).astype(np.float32)                 # exact: fp16/bf16 fit in float32
+    y = x / np.float32(scale)                                 # IEEE float32 division
+    return e4m3_encode(y)
+
+
+def dequantize_e4m3(codes: np.ndarray, scale: float) -> np.ndarray:
+    return e4m3_decode(codes) * float(np.float32(scale))
+
+
 # ---------------------------------------------------------------- indexing
 
 def kv_head_of(q_head: int, group: int) -> int:
@@ -92,6 +151,17 @@ def slot_mapping(block_tables: np.ndarray, context_lens: np.ndarray, block_size:
 
 
 # ---------------------------------------------------------------- append
+
+def kv_append_fp8(k_cache: np.ndarray, v_cache: np.ndarray, k_new: np.ndarray, v_new: np.ndarray,
+                  slots: np.ndarray, block_size: int, k_scale: np.ndarray, v_scale: np.ndarray,
+                  dtype: str) -> Tuple[np.ndarray, np.ndarray]:
+    """kv_append into E4M3 caches: token i's K/V of KV head h are quantised with
+    k_scale[h] / v_scale[h] before they are stored."""
+    Hkv = k_new.shape[1]
+    kq = np.stack([quantize_e4m3(k_new[:, h], dtype, k_scale[h]) for h in range(Hkv)], axis=1)
+    vq = np.stack([quantize_e4m3(v_new[:, h], dtype, v_scale[h]) for h in range(Hkv)], axis=1)
+    return kv_append(k_cache, v_cache, kq, vq, slots, block_size)
+
 
 def kv_append(k_cache: np.ndarray, v_cache: np.ndarray, k_new: np.ndarray, v_new: np.ndarray,
               slots: np.ndarray, block_size: int) -> Tuple[np.ndarray, np.ndarray]:
@@ -146,8 +216,11 @@ def _dims(q_bits, k_cache_bits):
 
 def decode_attention_rows(q_bits, k_cache_bits, v_cache_bits, block_tables, context_lens,
                           scale: float, dtype: str, block_size: int,
-                          rows: Iterable[Tuple[int, int]]) -> np.ndarray:
-    """Attention output (float64 [len(rows)][D]) for the listed (sequence, query head) pairs."""
+                          rows: Iterable[Tuple[int, int]], kv_scales=None) -> np.ndarray:
+    """Attention output (float64 [len(rows)][D]) for the listed (sequence, query head) pairs.
+
+    With ``kv_scales = (k_scale, v_scale)`` the caches hold E4M3 codes and the
+    attention runs on their dequantised values (code value * the KV head's scale)."""
     B, Hq, Hkv, D = _dims(q_bits, k_cache_bits)
     g = Hq // Hkv
     rows = list(rows)
@@ -157,8 +230,12 @@ def decode_attention_rows(q_bits, k_cache_bits, v_cache_bits, block_tables, cont
         if L == 0:
             continue  # empty context: output stays zero
         kv = kv_head_of(h, g)
-        K = widen(gather_kv(k_cache_bits, block_tables[b], L, kv, block_size), dtype)
-        V = widen(gather_kv(v_cache_bits, block_tables[b], L, kv, block_size), dtype)
+        if kv_scales is None:
+            K = widen(gather_kv(k_cache_bits, block_tables[b], L, kv, block_size), dtype)
+            V = widen(gather_kv(v_cache_bits, block_tables[b], L, kv, block_size), dtype)
+        else:
+            K = dequantize_e4m3(gather_kv(k_cache_bits, block_tables[b], L, kv, block_size), kv_scales[0][kv])
+            V = dequantize_e4m3(gather_kv(v_cache_bits, block_tables[b], L, kv, block_size), kv_scales[1][kv])
         q = widen(q_bits[b, h], dtype)
         out[i] = attend_one(q, K, V, scale)[0]
     return out

@@ -7,6 +7,8 @@
 * special cases: one-token context returns V exactly, equal keys give mean(V),
   GQA equals MHA with each KV head repeated g times;
 * number formats: every fp16 / bf16 bit pattern against torch's conversion;
+  every E4M3 code, and E4M3 rounding of in-range values, against torch's
+  float8_e4m3fn; saturation, ties-to-even and subnormals by closed form;
 * page worked examples (tests/golden/*.json, each with its source);
 * planted mistakes: each mutation of the oracle below is caught by a pin.
 """
@@ -375,3 +377,122 @@ def test_planted_mistake_is_caught(monkeypatch, name):
     attr, bad = MUTATIONS[name]
     monkeypatch.setattr(oracle, attr, bad)
     assert not _pins_pass()
+
+
+# ------------------------------------------------------------------ fp8 (E4M3) codes
+
+def test_e4m3_decode_every_code_against_torch_and_closed_forms():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan) and nan.sum() == 2        # 0x7F, 0xFF
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert oracle.e4m3_decode(np.array([0x38]))[0] == 1.0                # 0.0111.000
+    assert oracle.e4m3_decode(np.array([0x7E]))[0] == 448.0              # largest finite
+    assert oracle.e4m3_decode(np.array([0x01]))[0] == 2.0 ** -9          # smallest subnormal
+    assert oracle.e4m3_decode(np.array([0x08]))[0] == 2.0 ** -6          # smallest normal
+    assert oracle.e4m3_decode(np.array([0xC4]))[0] == -3.0               # 1.1000.100
+
+
+def test_e4m3_encode_round_trip_ties_and_saturation():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    vals = oracle.e4m3_decode(codes)
+    # every finite code encodes back to itself (-0 and +0 both map to their own codes)
+    assert np.array_equal(oracle.e4m3_encode(vals.astype(np.float32)), codes)
+    # midpoints between neighbours round to the even mantissa
+    pos = np.sort(vals[vals > 0])
+    mids = (pos[:-1] + pos[1:]) / 2
+    got = oracle.e4m3_decode(oracle.e4m3_encode(mids.astype(np.float32)))
+    even = np.where(oracle.e4m3_encode(pos[:-1].astype(np.float32)) % 2 == 0, pos[:-1], pos[1:])
+    assert np.array_equal(got, even)
+    # saturation instead of overflow, NaN stays NaN, 2^-10 (half the smallest step) rounds to 0
+    assert list(oracle.e4m3_encode(np.array([449.0, 464.0, 1e9, -1e9, np.inf], np.float32))) == [0x7E, 0x7E, 0x7E, 0xFE, 0x7E]
+    assert oracle.e4m3_encode(np.array([np.nan], np.float32))[0] == 0x7F
+    assert oracle.e4m3_encode(np.array([2.0 ** -10], np.float32))[0] == 0
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    rng = np.random.default_rng(0)
+    x = (rng.standard_normal(200000) * np.exp(rng.uniform(-12, 6, 200000))).astype(np.float32)
+    x = x[np.abs(x) < 448]
+    ours = oracle.e4m3_encode(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_quantize_divides_in_float32_then_rounds():
+    bits = torch.tensor([1.0, -2.5, 300.0, 0.0078125, 1000.0], dtype=torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    codes = oracle.quantize_e4m3(bits, "bf16", 0.5)
+    assert list(oracle.e4m3_decode(codes)) == [2.0, -5.0, 448.0, 0.015625, 448.0]   # 600, 2000 saturate
+    # the scale's float32 rounding is what the division sees
+    bits1 = torch.tensor([3.0], dtype=torch.float16).view(torch.int16).numpy().view(np.uint16)
+    s = 0.1  # not exact in float32
+    y = np.float32(3.0) / np.float32(s)
+    assert oracle.quantize_e4m3(bits1, "fp16", s)[0] == oracle.e4m3_encode(np.array([y]))[0]
+
+
+def test_fp8_attention_is_attention_on_dequantised_values():
+    lens = (5, 23)
+    q, K, V, kc, vc, tables = paged_case(13, lens=lens, dtype="bf16")
+    ks, vs = np.array([0.05, 0.03], np.float32), np.array([0.02, 0.04], np.float32)
+    kq = np.stack([oracle.quantize_e4m3(kc[:, h], "bf16", ks[h]) for h in range(2)], axis=1)
+    vq = np.stack([oracle.quantize_e4m3(vc[:, h], "bf16", vs[h]) for h in range(2)], axis=1)
+    rows = [(b, h) for b in range(2) for h in range(8)]
+    out = oracle.decode_attention_rows(q, kq, vq, tables, np.array(lens), 0.25, "bf16", 4, rows, kv_scales=(ks, vs))
+    # the same attention on the dequantised contiguous arrays, by brute force
+    Kd = np.stack([oracle.dequantize_e4m3(oracle.quantize_e4m3(K[:, h], "bf16", ks[h]), ks[h]) for h in range(2)], 1)
+    Vd = np.stack([oracle.dequantize_e4m3(oracle.quantize_e4m3(V[:, h], "bf16", vs[h]), vs[h]) for h in range(2)], 1)
+    qd = oracle.widen(q, "bf16")
+    for i, (b, h) in enumerate(rows):
+        s = [0.25 * float(qd[b, h] @ Kd[b, h // 4, t]) for t in range(lens[b])]
+        e = np.exp(np.array(s) - max(s))
+        ref = (e[:, None] * Vd[b, h // 4, :lens[b]]).sum(0) / e.sum()
+        assert np.abs(out[i] - ref).max() < 1e-12
+    # each code is within half a grid step of the float32 quotient x / scale
+    # (the quotient is rounded to float32 first, so ties are decided there)
+    x = oracle.widen(K, "bf16").astype(np.float32)
+    for h in range(2):
+        y = (x[:, h] / ks[h]).astype(np.float64)
+        c = oracle.e4m3_decode(oracle.quantize_e4m3(K[:, h], "bf16", ks[h]))
+        half = 0.5 * 2.0 ** (np.floor(np.log2(np.maximum(np.abs(y), 2.0 ** -6))) - 3)
+        assert np.all(np.abs(c - y) <= half)
+
+
+def _fp8_pins_pass():
+    """The E4M3 pins above, as a function of the current oracle."""
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ours = oracle.e4m3_decode(codes)
+    if not (np.array_equal(np.isnan(ours), np.isnan(ref)) and np.array_equal(ours[~np.isnan(ref)], ref[~np.isnan(ref)])):
+        return False
+    rng = np.random.default_rng(1)
+    x = (rng.standard_normal(20000) * np.exp(rng.uniform(-12, 6, 20000))).astype(np.float32)
+    x = x[np.abs(x) < 448]
+    if not np.array_equal(oracle.e4m3_encode(x), torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()):
+        return False
+    return list(oracle.e4m3_encode(np.array([1e9, -1e9], np.float32))) == [0x7E, 0xFE]
+
+
+def _truncating_encode(x, f=oracle.e4m3_encode):
+    """Rounds toward zero instead of to nearest."""
+    x = np.asarray(x, np.float32)
+    c = f(x)
+    over = np.abs(oracle.e4m3_decode(c)) > np.abs(x.astype(np.float64))
+    return np.where(over & (c & 0x7F > 0), c - 1, c).astype(np.uint8)
+
+
+FP8_MUTATIONS = {
+    "exponent bias 8": ("e4m3_decode", lambda c, f=oracle.e4m3_decode: f(c) / 2.0),
+    "no saturation": ("e4m3_encode", lambda x, f=oracle.e4m3_encode: np.where(np.abs(np.asarray(x, np.float32)) > 448, 0x7F, f(x)).astype(np.uint8)),
+    "round toward zero": ("e4m3_encode", _truncating_encode),
+    "subnormals flushed": ("e4m3_decode", lambda c, f=oracle.e4m3_decode: np.where((np.asarray(c) & 0x78) == 0, 0.0, f(c))),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FP8_MUTATIONS))
+def test_planted_fp8_mistake_is_caught(monkeypatch, name):
+    assert _fp8_pins_pass()
+    attr, bad = FP8_MUTATIONS[name]
+    monkeypatch.setattr(oracle, attr, bad)
+    assert not _fp8_pins_pass()
