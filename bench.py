@@ -51,19 +51,26 @@ L2_BYTES = 129 * 2 ** 20
 
 # ----------------------------------------------------------------------------- bytes model
 
-def attention_bytes(lens, batch, num_q_heads, num_kv_heads, head_dim, elem_bytes, block_size=16) -> int:
+def attention_bytes(lens, batch, num_q_heads, num_kv_heads, head_dim, elem_bytes, block_size=16,
+                    kv_elem_bytes=None) -> int:
+    """kv_elem_bytes: bytes per cached K/V element (1 for an E4M3 pool);
+    defaults to elem_bytes, the size of q / out elements."""
+    kv_elem = elem_bytes if kv_elem_bytes is None else kv_elem_bytes
     lens = np.asarray(lens, np.int64)
-    kv = int(lens.sum()) * num_kv_heads * head_dim * 2 * elem_bytes
+    kv = int(lens.sum()) * num_kv_heads * head_dim * 2 * kv_elem
     q_out = 2 * batch * num_q_heads * head_dim * elem_bytes
     tables = 4 * int(((lens + block_size - 1) // block_size).sum())
     return kv + q_out + tables + 4 * batch
 
 
-def append_bytes(batch, num_kv_heads, head_dim, elem_bytes) -> int:
-    return 2 * (2 * batch * num_kv_heads * head_dim * elem_bytes) + 4 * batch
+def append_bytes(batch, num_kv_heads, head_dim, elem_bytes, kv_elem_bytes=None) -> int:
+    """New K/V rows read (elem_bytes each) and written into the pool
+    (kv_elem_bytes each, default elem_bytes), plus the slot of each sequence."""
+    kv_elem = elem_bytes if kv_elem_bytes is None else kv_elem_bytes
+    return 2 * batch * num_kv_heads * head_dim * (elem_bytes + kv_elem) + 4 * batch
 
 
-def unique_kv_bytes(w) -> int:
+def unique_kv_bytes(w, kv_elem_bytes=2) -> int:
     """K+V bytes of distinct physical blocks read (shared prefix blocks once)."""
     s = w.spec
     n_tok = 0
@@ -76,7 +83,7 @@ def unique_kv_bytes(w) -> int:
                 continue
             seen.add(blk)
             n_tok += min(s.block_size, L - j * s.block_size)
-    return n_tok * s.num_kv_heads * s.head_dim * 2 * 2
+    return n_tok * s.num_kv_heads * s.head_dim * 2 * kv_elem_bytes
 
 
 # ----------------------------------------------------------------------------- environment
@@ -199,19 +206,23 @@ def max_over_ranks(x: float, world: int, device) -> float:
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def host_sample(w, seqs, layer=0):
-    """Host copies (16-bit patterns) of q and of the K/V blocks the listed
-    sequences use, with their block tables renumbered into the copy."""
+def host_sample(w, seqs, layer=0, caches=None):
+    """Host copies (16-bit patterns, or E4M3 codes for an fp8 pool given as
+    ``caches``) of q and of the K/V blocks the listed sequences use, with their
+    block tables renumbered into the copy."""
     s = w.spec
     blocks = sorted({int(x) for b in seqs for x in w.block_tables[b, :-(-int(w.context_lens[b]) // s.block_size)]})
     remap = {blk: i for i, blk in enumerate(blocks)}
-    idx = torch.tensor(blocks, dtype=torch.long, device=w.k_cache[layer].device)
+    kcache, vcache = caches if caches is not None else (w.k_cache[layer], w.v_cache[layer])
+    idx = torch.tensor(blocks, dtype=torch.long, device=kcache.device)
 
     def bits(t):
+        if t.dtype == torch.uint8:
+            return t.contiguous().cpu().numpy()
         return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
-    kc = bits(w.k_cache[layer].index_select(0, idx)) if blocks else np.zeros((0,), np.uint16)
-    vc = bits(w.v_cache[layer].index_select(0, idx)) if blocks else np.zeros((0,), np.uint16)
+    kc = bits(kcache.index_select(0, idx)) if blocks else np.zeros((0,), np.uint16)
+    vc = bits(vcache.index_select(0, idx)) if blocks else np.zeros((0,), np.uint16)
     tables = np.full((len(seqs), w.block_tables.shape[1]), -1, np.int32)
     for i, b in enumerate(seqs):
         n = -(-int(w.context_lens[b]) // s.block_size)
@@ -220,38 +231,45 @@ def host_sample(w, seqs, layer=0):
     return q, kc, vc, tables, w.context_lens[list(seqs)]
 
 
-def oracle_rows_timed(w, sample, rows):
+def oracle_rows_timed(w, sample, rows, kv_scales=None):
     import oracle
     q, kc, vc, tables, lens = sample
     t0 = time.perf_counter()
-    oracle.decode_attention_rows(q, kc, vc, tables, lens, w.scale, w.spec.dtype, w.spec.block_size, rows)
+    oracle.decode_attention_rows(q, kc, vc, tables, lens, w.scale, w.spec.dtype, w.spec.block_size, rows,
+                                 kv_scales=kv_scales)
     return time.perf_counter() - t0
 
 
-def row_bytes(w, lens_rows) -> int:
+def row_bytes(w, lens_rows, kv_elem_bytes=2) -> int:
     """Algorithmic bytes of attention for individual (sequence, query head)
     rows: each row's share of its KV head's K/V, plus its q and out."""
     s = w.spec
     g = s.group
-    return sum(int(L) * s.head_dim * 2 * 2 / g + 2 * s.head_dim * 2 for L in lens_rows)
+    return sum(int(L) * s.head_dim * 2 * kv_elem_bytes / g + 2 * s.head_dim * 2 for L in lens_rows)
 
 
-def cpu_baseline(w, budget_s: float):
-    """The oracle, as it stands, over the batch's first sequences (all query
-    heads) until about budget_s seconds of single-threaded CPU work."""
+def cpu_baseline(w, budget_s: float, fp8=None):
+    """The oracle, as it stands, over the batch's sequences in order (all query
+    heads; the batch again from its start if it is done early) until about
+    budget_s seconds of single-threaded CPU work.  ``fp8``: the E4M3 pool."""
     s = w.spec
     spent, done_bytes, seqs_done = 0.0, 0.0, 0
-    for b in range(s.batch):
-        sample = host_sample(w, [b])
+    caches = (fp8.k_cache[0], fp8.v_cache[0]) if fp8 is not None else None
+    scales = (fp8.k_scale[0].cpu().numpy(), fp8.v_scale[0].cpu().numpy()) if fp8 is not None else None
+    samples = {}
+    while spent < budget_s:
+        b = seqs_done % s.batch
+        if b not in samples:
+            samples[b] = host_sample(w, [b], caches=caches)
         rows = [(0, h) for h in range(s.num_q_heads)]
-        spent += oracle_rows_timed(w, sample, rows)
-        done_bytes += row_bytes(w, [w.context_lens[b]] * s.num_q_heads)
+        spent += oracle_rows_timed(w, samples[b], rows, kv_scales=scales)
+        done_bytes += row_bytes(w, [w.context_lens[b]] * s.num_q_heads, 1 if fp8 is not None else 2)
         seqs_done += 1
-        if spent >= budget_s:
-            break
+    passes = f"{seqs_done / s.batch:.2f} passes over the {s.batch} sequences" if seqs_done > s.batch else \
+        f"first {seqs_done} of {s.batch} sequences"
     return {"value": done_bytes / spent / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"first {seqs_done} of {s.batch} sequences, all {s.num_q_heads} query heads, layer 0; "
-                      f"{spent:.1f} s of numpy fp64 on one host thread"}
+            "sample": f"{passes}, all {s.num_q_heads} query heads, layer 0"
+                      f"{' (E4M3 pool)' if fp8 is not None else ''}; {spent:.1f} s of numpy fp64 on one host thread"}
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -273,6 +291,15 @@ def run_ours(args, rank, world, local):
     s = w.spec
     nl = len(w.q)
     elem = 2
+    fp8 = args.kv == "fp8"
+    f8 = None
+    if fp8:
+        if args.splits != 0:
+            raise SystemExit("--kv fp8 runs the automatic (persistent) path only: use --splits 0")
+        f8 = wl.fp8_caches(w, seed=args.seed + rank)
+        w.k_cache, w.v_cache = [], []        # the fp16/bf16 pool is not used
+        torch.cuda.empty_cache()
+    kv_elem = 1 if fp8 else elem
     L = lib()
     stream = torch.cuda.current_stream(dev)
     sp = ctypes.c_void_p(stream.cuda_stream)
@@ -290,10 +317,18 @@ def run_ours(args, rank, world, local):
     ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     P = ctypes.c_void_p
     scale = ctypes.c_float(w.scale)
-    step_args = [(P(w.q[l].data_ptr()), P(w.k_new[l].data_ptr()), P(w.v_new[l].data_ptr()), P(w.k_cache[l].data_ptr()),
-                  P(w.v_cache[l].data_ptr()), P(bt.data_ptr()), P(cl.data_ptr()), scale, P(outs[l].data_ptr()),
-                  args.splits, P(ws.data_ptr()), ws_bytes, ctypes.byref(dims), sp) for l in range(nl)]
-    f_step = L.paged_decode_step
+    if fp8:
+        step_args = [(P(w.q[l].data_ptr()), P(w.k_new[l].data_ptr()), P(w.v_new[l].data_ptr()),
+                      P(f8.k_cache[l].data_ptr()), P(f8.v_cache[l].data_ptr()), P(f8.k_scale[l].data_ptr()),
+                      P(f8.v_scale[l].data_ptr()), P(bt.data_ptr()), P(cl.data_ptr()), scale,
+                      P(outs[l].data_ptr()), P(ws.data_ptr()), ws_bytes, ctypes.byref(dims), sp) for l in range(nl)]
+        f_step = L.paged_decode_step_fp8
+    else:
+        step_args = [(P(w.q[l].data_ptr()), P(w.k_new[l].data_ptr()), P(w.v_new[l].data_ptr()),
+                      P(w.k_cache[l].data_ptr()), P(w.v_cache[l].data_ptr()), P(bt.data_ptr()), P(cl.data_ptr()),
+                      scale, P(outs[l].data_ptr()), args.splits, P(ws.data_ptr()), ws_bytes, ctypes.byref(dims),
+                      sp) for l in range(nl)]
+        f_step = L.paged_decode_step
 
     def step():
         for l in range(nl):
@@ -339,8 +374,9 @@ def run_ours(args, rank, world, local):
     pkv.paged_kv_check_status(stream)
     call_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
 
-    attn_b = attention_bytes(w.context_lens, s.batch, s.num_q_heads, s.num_kv_heads, s.head_dim, elem) * nl
-    app_b = append_bytes(s.batch, s.num_kv_heads, s.head_dim, elem) * nl
+    attn_b = attention_bytes(w.context_lens, s.batch, s.num_q_heads, s.num_kv_heads, s.head_dim, elem,
+                             kv_elem_bytes=kv_elem) * nl
+    app_b = append_bytes(s.batch, s.num_kv_heads, s.head_dim, elem, kv_elem_bytes=kv_elem) * nl
     step_bytes = attn_b + app_b
     ms_per_step = elapsed_ms / K
     value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
@@ -362,24 +398,38 @@ def run_ours(args, rank, world, local):
     dstage = [{"q": w.q[l], "k_new": w.k_new[l], "v_new": w.v_new[l], "block_tables": bt, "context_lens": cl,
                "out": outs[l]} for l in range(nl)]
     keys = STEP_KEYS
-    e2e_args = []
-    for l in range(nl):
-        bufs = PkvStepBuffers(**{f"{k}_host": h[k].data_ptr() for k in keys},
-                              **{f"{k}_dev": dstage[l][k].data_ptr() for k in keys})
-        e2e_args.append((bufs, P(w.k_cache[l].data_ptr()), P(w.v_cache[l].data_ptr()), scale, args.splits,
-                         P(ws.data_ptr()), ws_bytes, ctypes.byref(dims), sp))
-    f_e2e = L.paged_decode_step_from_host
+    if fp8:
+        # No single host-buffer entry point for the E4M3 pool: the public
+        # Python API's copies (pinned host <-> device, on the same stream)
+        # around paged_decode_step_fp8.
+        def e2e_once():
+            for l in range(nl):
+                for k in keys[:-1]:
+                    dstage[l][k].copy_(h[k], non_blocking=True)
+                if f_step(*step_args[l]):
+                    raise RuntimeError(L.paged_kv_last_error().decode())
+                h["out"].copy_(outs[l], non_blocking=True)
+    else:
+        e2e_args = []
+        for l in range(nl):
+            bufs = PkvStepBuffers(**{f"{k}_host": h[k].data_ptr() for k in keys},
+                                  **{f"{k}_dev": dstage[l][k].data_ptr() for k in keys})
+            e2e_args.append((bufs, P(w.k_cache[l].data_ptr()), P(w.v_cache[l].data_ptr()), scale, args.splits,
+                             P(ws.data_ptr()), ws_bytes, ctypes.byref(dims), sp))
+        f_e2e = L.paged_decode_step_from_host
+
+        def e2e_once():
+            for a in e2e_args:
+                if f_e2e(ctypes.byref(a[0]), *a[1:]):
+                    raise RuntimeError(L.paged_kv_last_error().decode())
     for _ in range(min(W, 10)):
-        for a in e2e_args:
-            f_e2e(ctypes.byref(a[0]), *a[1:])
+        e2e_once()
     torch.cuda.synchronize()
     K_e2e = K
     barrier(world)
     start.record(stream)
     for _ in range(K_e2e):
-        for a in e2e_args:
-            if f_e2e(ctypes.byref(a[0]), *a[1:]):
-                raise RuntimeError(L.paged_kv_last_error().decode())
+        e2e_once()
     end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -391,23 +441,30 @@ def run_ours(args, rank, world, local):
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": s.dtype, "data": "synthetic (seeded N(0,1) values, scattered block placement)",
-        "config": {"workload": s.name, "batch": s.batch, "num_q_heads": s.num_q_heads,
+        "dtype": "e4m3" if fp8 else s.dtype,
+        "data": "synthetic (seeded N(0,1) values, scattered block placement"
+                + ("; E4M3 pool cast from them with seeded per-head scales)" if fp8 else ")"),
+        "config": {"workload": s.name + ("_fp8" if fp8 else ""), "batch": s.batch, "num_q_heads": s.num_q_heads,
                    "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size,
                    "layers_per_step": nl, "context_tokens": int(w.context_lens.sum()),
                    "num_blocks": w.num_blocks,
                    "partition": "persistent, equal blocks per warp" if splits == 0 else f"{splits} splits",
                    "l2": f"no flush: each call streams {attn_b / nl / 2**20:.0f} MiB of K/V, "
                          f"{attn_b / nl / L2_BYTES:.1f}x the 129 MiB L2",
-                   "step": "paged_decode_step: KV append + paged decode attention + merge"},
+                   "step": ("paged_decode_step_fp8: E4M3 quantise + append, attention over the E4M3 pool "
+                            "(fp16 mma, fp32 softmax), merge" if fp8 else
+                            "paged_decode_step: KV append + paged decode attention + merge"),
+                   "kv_cache": ("E4M3 codes + f32 per-KV-head K/V scales; q/out " + s.dtype) if fp8 else s.dtype},
         "steps_per_s": round(1e3 / ms_per_step, 2),
         "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "roofline": {"bound": "hbm",
-                     "kernel": ("paged_decode_step: decode_persistent_kernel (append fused) + merge_persistent_kernel"
+                     "kernel": ("paged_decode_step_fp8: decode_persistent_kernel<E4M3> (quantising append fused)"
+                                " + merge_persistent_kernel" if fp8 else
+                                "paged_decode_step: decode_persistent_kernel (append fused) + merge_persistent_kernel"
                                 if splits == 0 else "paged_decode_step: append_at_end_kernel + decode_split_kernel"
                                 + (" + merge_split_kernel" if splits > 1 else "")),
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic(s.name),
+                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic(s.name + ("_fp8" if fp8 else "")),
                      "bytes_per_launch": step_bytes // nl, "avg_launch_us": round(step_s * 1e6, 2),
                      "isolated_call_us": round(call_avg_s * 1e6, 2)},
         "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
@@ -416,9 +473,9 @@ def run_ours(args, rank, world, local):
         "clocks": clocks,
     }
     if s.shared_prefix:
-        result["config"]["unique_kv_bytes_per_call"] = unique_kv_bytes(w)
+        result["config"]["unique_kv_bytes_per_call"] = unique_kv_bytes(w, kv_elem)
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
+        result["cpu_baseline"] = cpu_baseline(w, args.cpu_budget, fp8=f8)
     if rank == 0:
         print(json.dumps(result), flush=True)
 
@@ -560,6 +617,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds of oracle work for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv", choices=["native", "fp8"], default="native",
+                    help="pool format: the configuration's fp16/bf16, or E4M3 codes with per-head scales")
     ap.add_argument("--loop", action="store_true", help="continuous-batching loop instead of the fixed batch")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -207,6 +207,57 @@ int paged_decode_attention_no_alloc(const void* q, const void* k_cache, const vo
                                     float scale, void* out, int32_t num_splits,
                                     const pkv_dims* dims, void* stream);
 
+/* ------------------------------------------------------------------------
+ * FP8 (E4M3) KV cache.  design.babushkai.com "GPU推論の内部構造", section
+ * "KVキャッシュの台帳", and the quantisation section of youngju.dev "LLM
+ * サービング最適化完全ガイド": storing K/V in FP8 halves the cache's bytes per
+ * token, so decode attention -- bound by reading the cache -- moves half the
+ * bytes.  The pages fix neither the FP8 format nor the scaling; this library
+ * takes E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ * infinities, S.1111.111 = NaN, largest finite 448) with one float32 scale per
+ * KV head for K and one for V:  value = E4M3(code) * scale.
+ *
+ * Layouts: k_cache, v_cache : uint8[num_blocks][num_kv_heads][block_size][head_dim]
+ *                             (E4M3 codes, same slot rule as above)
+ *          k_scale, v_scale : float32[num_kv_heads] (device), finite and > 0
+ *          q, out, k_new, v_new: T as above (pkv_dims.dtype is their type).
+ * Quantisation (append): code = E4M3(float32(x) / scale) -- IEEE float32
+ * division, round to nearest even, magnitudes past 448 saturate to 448.
+ * Attention: the plain attention of the dequantised cache, as
+ * paged_decode_attention computes it for fp16/bf16 caches.  The products run
+ * as fp16 tensor-core mma (E4M3 values are exact in fp16), so a bf16 query is
+ * converted to fp16: a query entry beyond +-65504 sets the error word
+ * (PKV_ERR_OUT_OF_RANGE from paged_kv_check_status).
+ * Limits: head_dim 128 for attention; at most 1024 sequences per call; only
+ * the automatic persistent path (its workspace is
+ * paged_decode_workspace_bytes(dims, 0) bytes, zero-filled once, as above).
+ * Bad shapes and pointers return PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED.
+ * ---------------------------------------------------------------------- */
+
+/* Slot-mapped append of num_tokens tokens into an E4M3 pool (device).  Same
+ * slot rule and error behaviour as paged_kv_append; caches 8-byte aligned,
+ * k_new / v_new 16-byte aligned. */
+int paged_kv_append_fp8(const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                        int32_t num_tokens, void* k_cache, void* v_cache, const float* k_scale,
+                        const float* v_scale, const pkv_dims* dims, void* stream);
+
+/* Decode attention over an E4M3 pool (device); arguments as
+ * paged_decode_attention with the automatic path. */
+int paged_decode_attention_fp8(const void* q, const void* k_cache, const void* v_cache,
+                               const float* k_scale, const float* v_scale,
+                               const int32_t* block_tables, const int32_t* context_lens,
+                               float scale, void* out, void* workspace, size_t workspace_bytes,
+                               const pkv_dims* dims, void* stream);
+
+/* One decode step over an E4M3 pool (device): quantise and append each
+ * sequence's token at position context_lens[b] - 1, then attend, in one fused
+ * launch; arguments as paged_decode_step with the automatic path. */
+int paged_decode_step_fp8(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                          void* v_cache, const float* k_scale, const float* v_scale,
+                          const int32_t* block_tables, const int32_t* context_lens, float scale,
+                          void* out, void* workspace, size_t workspace_bytes,
+                          const pkv_dims* dims, void* stream);
+
 /* Synchronises `stream`, then reads and clears this device's error word.
  * Returns PKV_OK, PKV_ERR_OUT_OF_RANGE, PKV_ERR_TIMEOUT or PKV_ERR_CUDA. */
 int paged_kv_check_status(void* stream);

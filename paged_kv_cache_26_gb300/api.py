@@ -205,6 +205,122 @@ def paged_decode_step_from_host(host: dict, dev: dict, k_cache: torch.Tensor, v_
            "paged_decode_step_from_host")
 
 
+# ---------------------------------------------------------------- FP8 (E4M3) cache
+
+_FP8_CACHE_DTYPES = (torch.uint8, torch.float8_e4m3fn)
+
+
+def _need_fp8_cache(name: str, t: torch.Tensor):
+    _need_cuda(name, t)
+    if t.dtype not in _FP8_CACHE_DTYPES:
+        raise ValueError(f"{name} must hold E4M3 codes (uint8 or float8_e4m3fn), got {t.dtype}")
+
+
+def _need_scales(k_scale: torch.Tensor, v_scale: torch.Tensor, hkv: int):
+    for n, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        _need_cuda(n, t, torch.float32)
+        if t.shape != (hkv,):
+            raise ValueError(f"{n} must be float32[num_kv_heads]")
+
+
+def make_dims_fp8(q_or_new: torch.Tensor, k_cache: torch.Tensor, block_tables: Optional[torch.Tensor] = None,
+                  num_q_heads: Optional[int] = None) -> PkvDims:
+    """Dims of a call over an E4M3 pool: dtype is that of q / out / k_new / v_new."""
+    nb, hkv, bs, d = k_cache.shape
+    if q_or_new.dtype not in _DTYPE_CODE:
+        raise ValueError("q / k_new / v_new must be float16 or bfloat16")
+    return PkvDims(num_seqs=q_or_new.shape[0],
+                   num_q_heads=num_q_heads if num_q_heads is not None else q_or_new.shape[1],
+                   num_kv_heads=hkv, head_dim=d, block_size=bs, num_blocks=nb,
+                   max_blocks_per_seq=block_tables.shape[1] if block_tables is not None else 0,
+                   dtype=_DTYPE_CODE[q_or_new.dtype])
+
+
+def paged_kv_append_fp8(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                        k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: torch.Tensor,
+                        v_scale: torch.Tensor, stream=None) -> None:
+    """paged_kv_append into E4M3 caches: token i's K/V of KV head h are stored
+    as E4M3(x / k_scale[h]) and E4M3(x / v_scale[h])."""
+    _need_cuda("k_new", k_new)
+    _need_cuda("v_new", v_new, k_new.dtype)
+    _need_cuda("slot_mapping", slot_mapping, torch.int32)
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _need_fp8_cache(n, t)
+    _need_scales(k_scale, v_scale, k_cache.shape[1])
+    if k_new.shape != v_new.shape or k_new.shape[1:] != (k_cache.shape[1], k_cache.shape[3]):
+        raise ValueError("k_new / v_new must be [num_tokens][num_kv_heads][head_dim] matching the cache")
+    if k_cache.shape != v_cache.shape or slot_mapping.shape != (k_new.shape[0],):
+        raise ValueError("cache shapes differ or slot_mapping is not [num_tokens]")
+    dims = make_dims_fp8(k_new, k_cache, num_q_heads=k_cache.shape[1])
+    _check(lib().paged_kv_append_fp8(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), k_new.shape[0], _ptr(k_cache),
+                                     _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), ctypes.byref(dims),
+                                     _stream(stream)),
+           "paged_kv_append_fp8")
+
+
+def _fp8_call_checks(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, out):
+    _need_cuda("q", q)
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _need_fp8_cache(n, t)
+    _need_scales(k_scale, v_scale, k_cache.shape[1])
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    _need_cuda("out", out, q.dtype)
+    if out.shape != q.shape or q.dim() != 3 or q.shape[2] != k_cache.shape[3] or k_cache.shape != v_cache.shape:
+        raise ValueError("q / out must be [num_seqs][num_q_heads][head_dim] matching the caches")
+    if block_tables.dim() != 2 or block_tables.shape[0] != q.shape[0] or context_lens.shape != (q.shape[0],):
+        raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
+
+
+def _fp8_workspace(dims, q, workspace):
+    need = int(lib().paged_decode_workspace_bytes(ctypes.byref(dims), 0))
+    if need and workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return workspace, ws_bytes
+
+
+def paged_decode_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               k_scale: torch.Tensor, v_scale: torch.Tensor, block_tables: torch.Tensor,
+                               context_lens: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
+                               workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """paged_decode_attention over E4M3 caches with per-KV-head scales."""
+    if out is None:
+        out = torch.empty_like(q)
+    _fp8_call_checks(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, out)
+    dims = make_dims_fp8(q, k_cache, block_tables)
+    workspace, ws_bytes = _fp8_workspace(dims, q, workspace)
+    _check(lib().paged_decode_attention_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                            _ptr(block_tables), _ptr(context_lens), float(scale), _ptr(out),
+                                            _ptr(workspace), ws_bytes, ctypes.byref(dims), _stream(stream)),
+           "paged_decode_attention_fp8")
+    return out
+
+
+def paged_decode_step_fp8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                          v_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                          block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                          out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    """paged_decode_step over E4M3 caches: the new token is quantised with
+    the scales and appended, then attended, in one fused launch."""
+    if out is None:
+        out = torch.empty_like(q)
+    _fp8_call_checks(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, out)
+    _need_cuda("k_new", k_new, q.dtype)
+    _need_cuda("v_new", v_new, q.dtype)
+    if k_new.shape != (q.shape[0], k_cache.shape[1], k_cache.shape[3]) or v_new.shape != k_new.shape:
+        raise ValueError("k_new / v_new must be [num_seqs][num_kv_heads][head_dim]")
+    dims = make_dims_fp8(q, k_cache, block_tables)
+    workspace, ws_bytes = _fp8_workspace(dims, q, workspace)
+    _check(lib().paged_decode_step_fp8(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                       _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(context_lens),
+                                       float(scale), _ptr(out), _ptr(workspace), ws_bytes, ctypes.byref(dims),
+                                       _stream(stream)),
+           "paged_decode_step_fp8")
+    return out
+
+
 def paged_kv_check_status(stream=None) -> None:
     """Synchronise the stream and raise if a kernel flagged an error."""
     _check(lib().paged_kv_check_status(_stream(stream)), "paged_kv_check_status")

@@ -21,7 +21,6 @@ constexpr int kConsumerWarps = 4;   // split kernel
 constexpr int kStages = 8;          // split kernel ring depth
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kAutoSplitBlocks = 32;  // 512-token splits when the split path is chosen automatically
-constexpr int kMaxPersistentSeqs = 2048;  // prefix sums of the persistent kernel live in shared memory
 constexpr int kMaxDevices = 64;
 
 int device_sms() {
@@ -81,17 +80,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // The pool as a 2-D tensor: rows = num_blocks * Hkv * 16 of head_dim elements;
-// boxes of 16 rows x 64 elements (128 bytes) with the 128-byte swizzle.
-int make_cache_map(CUtensorMap* map, const void* cache, const pkv_dims* d) {
+// boxes of 16 rows x 128 bytes (64 fp16/bf16 elements or 128 E4M3 codes) with
+// the 128-byte swizzle.
+int make_cache_map(CUtensorMap* map, const void* cache, const pkv_dims* d, bool f8) {
   auto fn = encode_fn();
   if (!fn) return pkv_fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d->head_dim),
                               static_cast<cuuint64_t>(d->num_blocks) * d->num_kv_heads * pkv::kBlockSize};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d->head_dim) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(pkv::kBlockSize)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d->head_dim) * (f8 ? 1 : 2)};
+  const cuuint32_t box[2] = {f8 ? 128u : 64u, static_cast<cuuint32_t>(pkv::kBlockSize)};
   const cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapDataType dt =
-      d->dtype == PKV_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType dt = f8                           ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : d->dtype == PKV_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUresult r = fn(map, dt, 2, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -112,21 +113,22 @@ struct MapCache {
   int next = 0;
   std::mutex mu;
 
-  int get(const void* ptr, const pkv_dims* d, CUtensorMap* out) {
+  int get(const void* ptr, const pkv_dims* d, bool f8, CUtensorMap* out) {
+    const int32_t dt = f8 ? -2 : d->dtype;
     std::lock_guard<std::mutex> lock(mu);
     for (auto& x : e)
-      if (x.ptr == ptr && x.nb == d->num_blocks && x.hkv == d->num_kv_heads && x.hd == d->head_dim && x.dt == d->dtype) {
+      if (x.ptr == ptr && x.nb == d->num_blocks && x.hkv == d->num_kv_heads && x.hd == d->head_dim && x.dt == dt) {
         *out = x.map;
         return PKV_OK;
       }
     Entry& n = e[next];
-    int rc = make_cache_map(&n.map, ptr, d);
+    int rc = make_cache_map(&n.map, ptr, d, f8);
     if (rc != PKV_OK) return rc;
     n.ptr = ptr;
     n.nb = d->num_blocks;
     n.hkv = d->num_kv_heads;
     n.hd = d->head_dim;
-    n.dt = d->dtype;
+    n.dt = dt;
     next = (next + 1) % kEntries;
     *out = n.map;
     return PKV_OK;
@@ -142,8 +144,15 @@ struct SplitPlan {
   int32_t split_blocks;   // split kernel: blocks per split
 };
 
-bool persistent_eligible(const pkv_dims* d) {
-  return d->num_seqs <= kMaxPersistentSeqs &&
+// Largest batch of the persistent kernel: its prefix sums live in shared
+// memory beside the ring (2048 for fp16/bf16 pools, 1024 for E4M3 pools).
+int max_persistent_seqs(const pkv_dims* d, bool f8) {
+  if (f8) return pkv::persistent_max_seqs<128, true>() / 256 * 256;
+  return d->head_dim == 128 ? pkv::persistent_max_seqs<128>() : pkv::persistent_max_seqs<64>();
+}
+
+bool persistent_eligible(const pkv_dims* d, bool f8 = false) {
+  return d->num_seqs <= max_persistent_seqs(d, f8) &&
          static_cast<int64_t>(d->num_seqs) * d->num_kv_heads * d->max_blocks_per_seq < (int64_t(1) << 31);
 }
 
@@ -210,61 +219,64 @@ cudaError_t configure_smem(int bytes) {
   return e;
 }
 
+// Persistent decode + merge.  Both are programmatic dependent launches: each
+// may start while the kernel before it in the stream finishes, and waits
+// in-kernel (griddepcontrol.wait) before touching anything that kernel writes.
+template <typename T, int D, bool F8>
+int launch_persistent(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::DecodeArgs& args,
+                      const pkv_dims* d, int max_seqs, cudaStream_t stream) {
+  using PS = pkv::PersistentShape<D, F8>;
+  constexpr auto kern = pkv::decode_persistent_kernel<T, D, F8>;
+  cudaError_t e = configure_smem<kern>(static_cast<int>(pkv::persistent_smem_bytes<D, F8>(max_seqs)));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_persistent_kernel)");
+  const int64_t upper_blocks = static_cast<int64_t>(d->num_seqs) * d->num_kv_heads * d->max_blocks_per_seq;
+  int64_t grid = (upper_blocks + PS::kWarps - 1) / PS::kWarps;
+  if (grid > device_sms()) grid = device_sms();
+  if (grid < 1) grid = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(PS::kWarps * 32);
+  cfg.dynamicSmemBytes = pkv::persistent_smem_bytes<D, F8>(d->num_seqs);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, mk, mv, args);
+  if (e != cudaSuccess) return cuda_fail(e, "decode_persistent_kernel launch");
+  constexpr auto merge = pkv::merge_persistent_kernel<T, D>;
+  e = configure_smem<merge>(static_cast<int>((2 * static_cast<size_t>(max_persistent_seqs(d, false)) + 1) * 4));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_persistent_kernel)");
+  const int rows = d->num_seqs * d->num_q_heads;
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + pkv::kMergeWarps - 1) / pkv::kMergeWarps));
+  cfg.blockDim = dim3(pkv::kMergeWarps * 32);
+  cfg.dynamicSmemBytes = (2 * static_cast<size_t>(d->num_seqs) + 1) * 4;
+  e = cudaLaunchKernelEx(&cfg, merge, args, static_cast<int32_t>(grid) * PS::kWarps);
+  if (e != cudaSuccess) return cuda_fail(e, "merge_persistent_kernel launch");
+  return PKV_OK;
+}
+
 template <typename T, int D>
 int launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::DecodeArgs& args, const SplitPlan& plan,
                   const pkv_dims* d, cudaStream_t stream) {
   using Shape = pkv::TileShape<D>;
-  cudaError_t e;
-  if (plan.persistent) {
-    constexpr auto kern = pkv::decode_persistent_kernel<T, D>;
-    e = configure_smem<kern>(static_cast<int>(pkv::persistent_smem_bytes<D>(kMaxPersistentSeqs)));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_persistent_kernel)");
-    const int64_t upper_blocks = static_cast<int64_t>(d->num_seqs) * d->num_kv_heads * d->max_blocks_per_seq;
-    int64_t grid = (upper_blocks + pkv::PersistentShape<D>::kWarps - 1) / pkv::PersistentShape<D>::kWarps;
-    if (grid > device_sms()) grid = device_sms();
-    if (grid < 1) grid = 1;
-    // Both kernels are programmatic dependent launches: each may start while
-    // the kernel before it in the stream finishes, and waits in-kernel
-    // (griddepcontrol.wait) before touching anything that kernel writes.
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(pkv::PersistentShape<D>::kWarps * 32);
-    cfg.dynamicSmemBytes = pkv::persistent_smem_bytes<D>(d->num_seqs);
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, mk, mv, args);
-    if (e != cudaSuccess) return cuda_fail(e, "decode_persistent_kernel launch");
-    constexpr auto merge = pkv::merge_persistent_kernel<T, D>;
-    const int merge_smem = static_cast<int>((2 * static_cast<size_t>(kMaxPersistentSeqs) + 1) * 4);
-    e = configure_smem<merge>(merge_smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_persistent_kernel)");
+  if (plan.persistent) return launch_persistent<T, D, false>(mk, mv, args, d, max_persistent_seqs(d, false), stream);
+  constexpr int kSmem = kStages * Shape::kStageBytes + 1024;
+  constexpr auto kern = pkv::decode_split_kernel<T, D, kConsumerWarps, kStages>;
+  cudaError_t e = configure_smem<kern>(kSmem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_split_kernel)");
+  dim3 grid(plan.num_splits, d->num_kv_heads, d->num_seqs);
+  kern<<<grid, kThreads, kSmem, stream>>>(mk, mv, args);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "decode_split_kernel launch");
+  if (plan.num_splits > 1) {
     const int rows = d->num_seqs * d->num_q_heads;
-    cfg.gridDim = dim3(static_cast<unsigned>((rows + pkv::kMergeWarps - 1) / pkv::kMergeWarps));
-    cfg.blockDim = dim3(pkv::kMergeWarps * 32);
-    cfg.dynamicSmemBytes = (2 * static_cast<size_t>(d->num_seqs) + 1) * 4;
-    e = cudaLaunchKernelEx(&cfg, merge, args, static_cast<int32_t>(grid) * pkv::PersistentShape<D>::kWarps);
-    if (e != cudaSuccess) return cuda_fail(e, "merge_persistent_kernel launch");
-  } else {
-    constexpr int kSmem = kStages * Shape::kStageBytes + 1024;
-    constexpr auto kern = pkv::decode_split_kernel<T, D, kConsumerWarps, kStages>;
-    e = configure_smem<kern>(kSmem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_split_kernel)");
-    dim3 grid(plan.num_splits, d->num_kv_heads, d->num_seqs);
-    kern<<<grid, kThreads, kSmem, stream>>>(mk, mv, args);
+    pkv::merge_split_kernel<T, D><<<(rows + 3) / 4, 128, 0, stream>>>(
+        args.part_o, args.part_lse, args.context_lens, static_cast<T*>(args.out), d->num_seqs, d->num_q_heads,
+        plan.num_splits, plan.split_blocks, args.max_blocks);
     e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "decode_split_kernel launch");
-    if (plan.num_splits > 1) {
-      const int rows = d->num_seqs * d->num_q_heads;
-      pkv::merge_split_kernel<T, D><<<(rows + 3) / 4, 128, 0, stream>>>(
-          args.part_o, args.part_lse, args.context_lens, static_cast<T*>(args.out), d->num_seqs, d->num_q_heads,
-          plan.num_splits, plan.split_blocks, args.max_blocks);
-      e = cudaGetLastError();
-      if (e != cudaSuccess) return cuda_fail(e, "merge_split_kernel launch");
-    }
+    if (e != cudaSuccess) return cuda_fail(e, "merge_split_kernel launch");
   }
   return PKV_OK;
 }
@@ -276,12 +288,24 @@ int append_at_end_impl(const void* k_new, const void* v_new, const int32_t* bloc
 // Attention, optionally preceded by the append of each sequence's token at
 // position context_lens[b] - 1 (k_new / v_new non-null): fused into the
 // persistent kernel when that path runs, else a separate append launch.
+//
+// f8: the pool holds E4M3 codes with per-KV-head scales k_scale / v_scale
+// (head_dim 128, persistent path only).
 int decode_impl(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                 const int32_t* block_tables, const int32_t* context_lens, float scale, void* out,
                 int32_t num_splits, void* workspace, size_t workspace_bytes, const pkv_dims* d,
-                cudaStream_t stream) {
+                cudaStream_t stream, bool f8 = false, const float* k_scale = nullptr,
+                const float* v_scale = nullptr) {
   int rc = check_dims(d, true);
   if (rc != PKV_OK) return rc;
+  if (f8) {
+    if (d->head_dim != 128) return pkv_fail(PKV_ERR_UNSUPPORTED, "fp8 cache: head_dim must be 128");
+    if (!persistent_eligible(d, true))
+      return pkv_fail(PKV_ERR_UNSUPPORTED, "fp8 cache: at most " + std::to_string(max_persistent_seqs(d, true)) +
+                                               " sequences per call");
+    if (!k_scale || !v_scale || !aligned(k_scale, 4) || !aligned(v_scale, 4))
+      return pkv_fail(PKV_ERR_INVALID_ARG, "fp8 cache: k_scale / v_scale missing or misaligned");
+  }
   if (d->num_seqs == 0) return PKV_OK;
   // A zero-width table means every context is empty (contexts are clamped to
   // the table): the table pointer is then never read.
@@ -309,14 +333,16 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, void* k_cac
     if (rc != PKV_OK) return rc;
   }
   CUtensorMap mk, mv;
-  if ((rc = g_maps.get(k_cache, d, &mk)) != PKV_OK) return rc;
-  if ((rc = g_maps.get(v_cache, d, &mv)) != PKV_OK) return rc;
+  if ((rc = g_maps.get(k_cache, d, f8, &mk)) != PKV_OK) return rc;
+  if ((rc = g_maps.get(v_cache, d, f8, &mv)) != PKV_OK) return rc;
 
   pkv::DecodeArgs args;
   args.k_new = append && plan.persistent ? k_new : nullptr;
   args.v_new = append && plan.persistent ? v_new : nullptr;
   args.k_cache_w = k_cache;
   args.v_cache_w = v_cache;
+  args.k_scale = k_scale;
+  args.v_scale = v_scale;
   args.q = q;
   args.out = out;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -336,6 +362,11 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, void* k_cac
   args.split_blocks = plan.split_blocks;
 
   const bool bf16 = d->dtype == PKV_DTYPE_BF16;
+  if (f8) {
+    const int mx = max_persistent_seqs(d, true);
+    return bf16 ? launch_persistent<__nv_bfloat16, 128, true>(mk, mv, args, d, mx, stream)
+                : launch_persistent<__half, 128, true>(mk, mv, args, d, mx, stream);
+  }
   if (d->head_dim == 128)
     return bf16 ? launch_decode<__nv_bfloat16, 128>(mk, mv, args, plan, d, stream)
                 : launch_decode<__half, 128>(mk, mv, args, plan, d, stream);
@@ -386,9 +417,69 @@ int append_impl(const void* k_new, const void* v_new, const int32_t* slot_mappin
   return PKV_OK;
 }
 
+// Slot-mapped append into an E4M3 pool (head_dim 128 or 64: any multiple of 8
+// works for the copy; the attention side needs 128).
+int append_fp8_impl(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t num_tokens,
+                    void* k_cache, void* v_cache, const float* k_scale, const float* v_scale, const pkv_dims* d,
+                    cudaStream_t stream) {
+  int rc = check_dims(d, false);
+  if (rc != PKV_OK) return rc;
+  if (num_tokens < 0) return pkv_fail(PKV_ERR_INVALID_ARG, "append_fp8: num_tokens < 0");
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "append_fp8: NULL pointer");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 8) || !aligned(v_cache, 8) ||
+      !aligned(slot_mapping, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "append_fp8: misaligned pointer (values 16 bytes, caches 8)");
+  const int32_t groups = d->head_dim / 8;
+  const int64_t total = static_cast<int64_t>(num_tokens) * d->num_kv_heads * groups;
+  const int threads = 256;
+  const int64_t blocks64 = (total + threads - 1) / threads;
+  const int blocks = static_cast<int>(blocks64 < 65536 ? blocks64 : 65536);
+  const int64_t slots = static_cast<int64_t>(d->num_blocks) * pkv::kBlockSize;
+  auto kv = [&](auto kern) {
+    kern<<<blocks, threads, 0, stream>>>(static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+                                         slot_mapping, num_tokens, d->num_kv_heads, groups, slots,
+                                         static_cast<uint2*>(k_cache), static_cast<uint2*>(v_cache), k_scale,
+                                         v_scale);
+  };
+  if (d->dtype == PKV_DTYPE_BF16)
+    kv(pkv::append_fp8_kernel<__nv_bfloat16>);
+  else
+    kv(pkv::append_fp8_kernel<__half>);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "append_fp8_kernel launch");
+  return PKV_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+int paged_kv_append_fp8(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t num_tokens,
+                        void* k_cache, void* v_cache, const float* k_scale, const float* v_scale,
+                        const pkv_dims* dims, void* stream) {
+  return append_fp8_impl(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache, k_scale, v_scale, dims,
+                         static_cast<cudaStream_t>(stream));
+}
+
+int paged_decode_attention_fp8(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                               const float* v_scale, const int32_t* block_tables, const int32_t* context_lens,
+                               float scale, void* out, void* workspace, size_t workspace_bytes,
+                               const pkv_dims* dims, void* stream) {
+  return decode_impl(q, nullptr, nullptr, const_cast<void*>(k_cache), const_cast<void*>(v_cache), block_tables,
+                     context_lens, scale, out, 0, workspace, workspace_bytes, dims,
+                     static_cast<cudaStream_t>(stream), true, k_scale, v_scale);
+}
+
+int paged_decode_step_fp8(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                          const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                          const int32_t* context_lens, float scale, void* out, void* workspace,
+                          size_t workspace_bytes, const pkv_dims* dims, void* stream) {
+  if (!k_new || !v_new) return pkv_fail(PKV_ERR_INVALID_ARG, "decode_step_fp8: NULL k_new / v_new");
+  return decode_impl(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, out, 0, workspace,
+                     workspace_bytes, dims, static_cast<cudaStream_t>(stream), true, k_scale, v_scale);
+}
 
 int paged_kv_append(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t num_tokens,
                     void* k_cache, void* v_cache, const pkv_dims* dims, void* stream) {
@@ -481,6 +572,7 @@ int paged_kv_check_status(void* stream_v) {
   if (word & pkv::kErrSlot) msg += " append slot out of range;";
   if (word & pkv::kErrContext) msg += " context length out of range;";
   if (word & pkv::kErrTimeout) msg += " a bounded wait gave up;";
+  if (word & pkv::kErrQuery) msg += " a query value exceeds the fp16 range (fp8 cache path);";
   return pkv_fail((word & pkv::kErrTimeout) ? PKV_ERR_TIMEOUT : PKV_ERR_OUT_OF_RANGE, msg);
 }
 

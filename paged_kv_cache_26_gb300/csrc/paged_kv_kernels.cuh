@@ -29,7 +29,15 @@
 // rows = num_blocks * Hkv * 16 and D columns and loads a tile as D/64 boxes of
 // 16 rows x 64 elements (128 bytes) with the 128-byte swizzle, which makes the
 // fragment loads below free of shared-memory bank conflicts.
+//
+// FP8 cache: the same kernels over a pool of E4M3 codes, uint8[num_blocks][Hkv]
+// [16][D] with one float32 scale per KV head for K and one for V (value =
+// code * scale; design.babushkai.com "GPU推論の内部構造", section "KVキャッシュの
+// 台帳": an FP8 cache halves the bytes per token).  A tile row is then 128
+// bytes for D = 128 and a tile one 2 KB box.
 #pragma once
+
+#include <type_traits>
 
 #include "pkv_device.cuh"
 
@@ -101,6 +109,53 @@ __global__ void append_at_end_kernel(const uint4* __restrict__ k_new, const uint
         ((static_cast<int64_t>(blk) * num_kv_heads + head) * kBlockSize + pos % kBlockSize) * chunks_per_row + chunk;
     k_cache[dst] = k_new[idx];
     v_cache[dst] = v_new[idx];
+  }
+}
+
+// E4M3 codes of 8 fp16/bf16 values divided by `scale` (IEEE fp32 division,
+// then round to nearest even with saturation to +-448).
+template <typename T>
+__device__ __forceinline__ uint2 quantize8(const uint4& v, float scale) {
+  uint32_t out[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float2 a = unpack2<T>(word_of(v, 2 * h)), b = unpack2<T>(word_of(v, 2 * h + 1));
+    const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(a.x, scale), __fdiv_rn(a.y, scale));
+    const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(b.x, scale), __fdiv_rn(b.y, scale));
+    out[h] = lo | (hi << 16);
+  }
+  return make_uint2(out[0], out[1]);
+}
+
+// Slot-mapped append into an E4M3 pool: one thread quantises 8 consecutive
+// elements of one token's K row and of its V row for one KV head (C = D / 8
+// groups per row) with that head's scales.
+template <typename T>
+__global__ void append_fp8_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                                  const int32_t* __restrict__ slots, int32_t num_tokens, int32_t num_kv_heads,
+                                  int32_t groups_per_row, int64_t num_slots, uint2* __restrict__ k_cache,
+                                  uint2* __restrict__ v_cache, const float* __restrict__ k_scale,
+                                  const float* __restrict__ v_scale) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int64_t per_token = static_cast<int64_t>(num_kv_heads) * groups_per_row;
+  const int64_t total = per_token * num_tokens;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t token = idx / per_token;
+    const int64_t within = idx - token * per_token;  // head * C + group
+    const int32_t slot = slots[token];
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      flag_error(kErrSlot);
+      continue;
+    }
+    const int64_t blk = slot / kBlockSize;
+    const int64_t off = slot % kBlockSize;
+    const int64_t head = within / groups_per_row;
+    const int64_t grp = within - head * groups_per_row;
+    const int64_t dst = ((blk * num_kv_heads + head) * kBlockSize + off) * groups_per_row + grp;
+    k_cache[dst] = quantize8<T>(k_new[idx], __ldg(k_scale + head));
+    v_cache[dst] = quantize8<T>(v_new[idx], __ldg(v_scale + head));
   }
 }
 
@@ -259,6 +314,152 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
   return make_uint4(pack2<T>(v[0], v[1]), pack2<T>(v[2], v[3]), pack2<T>(v[4], v[5]), pack2<T>(v[6], v[7]));
 }
 
+// One warp's attention state for one unit whose K and V tiles hold E4M3
+// codes (D = 128: a tile row is 128 bytes, one TMA box with the 128-byte
+// swizzle).  Every E4M3 value is exactly an fp16 value, so the products run as
+// fp16 mma with fp32 accumulation, the query converted to fp16 at load and
+// the weights P rounded to fp16.  The per-KV-head scales stay outside the mma:
+// K's is folded into the logit scale, V's into the final normalisation.
+// Lane (gid = lane/4, c = lane%4):
+//  * S^T = K Q^T: k-step j (0..7) covers head_dim entries 32c + 4j .. 32c + 4j + 3
+//    (byte word j of chunks {2c, 2c+1} of K rows gid and gid + 8, and the same
+//    entries of q row gid);
+//  * O^T += V^T P^T: row m of m-tile mt is head_dim entry 16 gid + mt (m = gid)
+//    or 16 gid + 8 + mt (m = gid + 8), so the lane reads chunk gid of V rows
+//    2c, 2c+1, 2c+8, 2c+9 and ends up holding output entries
+//    [16 gid, 16 gid + 16) of heads 2c and 2c + 1.
+template <typename T>
+struct WarpAttnE4M3 {
+  static constexpr int D = 128;
+  uint32_t qf[16];  // q row gid as fp16 pairs; k-step j uses qf[2j], qf[2j + 1]
+  float acc[8][4];
+  float m0, m1, l0, l1;
+
+  __device__ __forceinline__ void reset() {
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  }
+
+  // Entries [32c, 32c + 32) of query row gid.  A bf16 query beyond the fp16
+  // range would become infinite: that is flagged (kErrQuery).
+  __device__ __forceinline__ void load_q(const T* q_group, int group, int lane) {
+    const int gid = lane >> 2, c = lane & 3;
+    bool big = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 raw =
+          gid < group ? __ldg(reinterpret_cast<const uint4*>(q_group + gid * D + 32 * c) + i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t x = word_of(raw, w);
+        if constexpr (MmaKind<T>::kBf16) {
+          const float2 f = unpack2<T>(x);
+          big |= fabsf(f.x) > 65504.f || fabsf(f.y) > 65504.f;
+          qf[4 * i + w] = pack2<__half>(f.x, f.y);
+        } else {
+          qf[4 * i + w] = x;
+        }
+      }
+    }
+    if (__any_sync(0xffffffffu, big) && lane == 0) flag_error(kErrQuery);
+  }
+
+  __device__ __forceinline__ void block(const uint8_t* ks, const uint8_t* vs, int valid, float scale_log2,
+                                        int lane) {
+    const int gid = lane >> 2, c = lane & 3;
+    const uint8_t* kr0 = ks + gid * 128;
+    const uint8_t* kr1 = ks + (gid + 8) * 128;  // same swizzle phase: (gid + 8) & 7 == gid
+    const uint4 ka0 = *reinterpret_cast<const uint4*>(kr0 + (((2 * c) ^ gid) << 4));
+    const uint4 ka1 = *reinterpret_cast<const uint4*>(kr0 + (((2 * c + 1) ^ gid) << 4));
+    const uint4 kb0 = *reinterpret_cast<const uint4*>(kr1 + (((2 * c) ^ gid) << 4));
+    const uint4 kb1 = *reinterpret_cast<const uint4*>(kr1 + (((2 * c + 1) ^ gid) << 4));
+    float s[4] = {0.f, 0.f, 0.f, 0.f}, t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t wa = word_of(j < 4 ? ka0 : ka1, j & 3);  // row gid: entries 32c + 4j .. + 3
+      const uint32_t wb = word_of(j < 4 ? kb0 : kb1, j & 3);  // row gid + 8
+      const uint32_t a0 = e4m3x2_to_f16x2(wa), a2 = e4m3x2_to_f16x2(wa >> 16);
+      const uint32_t a1 = e4m3x2_to_f16x2(wb), a3 = e4m3x2_to_f16x2(wb >> 16);
+      if (j & 1)
+        mma16816<__half>(t, a0, a1, a2, a3, qf[2 * j], qf[2 * j + 1]);
+      else
+        mma16816<__half>(s, a0, a1, a2, a3, qf[2 * j], qf[2 * j + 1]);
+    }
+    float x0 = (s[0] + t[0]) * scale_log2, x1 = (s[1] + t[1]) * scale_log2;  // token gid
+    float x2 = (s[2] + t[2]) * scale_log2, x3 = (s[3] + t[3]) * scale_log2;  // token gid + 8
+    if (valid < kBlockSize) {
+      if (gid >= valid) x0 = x1 = -INFINITY;
+      if (gid + 8 >= valid) x2 = x3 = -INFINITY;
+    }
+    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+    for (int o = 4; o <= 16; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    const uint32_t plo = pack2<__half>(exp2f(x0 - mn0), exp2f(x1 - mn1));
+    const uint32_t phi = pack2<__half>(exp2f(x2 - mn0), exp2f(x3 - mn1));
+    const float2 fl = unpack2<__half>(plo), fh = unpack2<__half>(phi);
+    l0 = l0 * al0 + (fl.x + fh.x);
+    l1 = l1 * al1 + (fl.y + fh.y);
+    const uint32_t b0 = movmatrix_trans(plo);
+    const uint32_t b1 = movmatrix_trans(phi);
+
+    uint4 vr[4];  // chunk gid of V rows 2c, 2c+1, 2c+8, 2c+9
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int row = 2 * c + (rr & 1) + 8 * (rr >> 1);
+      vr[rr] = *reinterpret_cast<const uint4*>(vs + row * 128 + ((gid ^ (row & 7)) << 4));
+      if (valid < kBlockSize && row >= valid) vr[rr] = make_uint4(0, 0, 0, 0);  // never 0 * NaN
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      acc[mt][0] *= al0;
+      acc[mt][1] *= al1;
+      acc[mt][2] *= al0;
+      acc[mt][3] *= al1;
+    }
+    // m-tiles 2p and 2p + 1 read bytes 2p, 2p + 1 (rows m = gid) and 8 + 2p,
+    // 9 + 2p (rows m = gid + 8) of the chunks; interleaving the byte pairs of
+    // two token rows puts each mma operand's two tokens side by side.
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const int w = p >> 1;
+      const uint32_t sel = (p & 1) ? 0x7362u : 0x5140u;
+      const uint32_t x0 = __byte_perm(word_of(vr[0], w), word_of(vr[1], w), sel);
+      const uint32_t x1 = __byte_perm(word_of(vr[0], w + 2), word_of(vr[1], w + 2), sel);
+      const uint32_t x2 = __byte_perm(word_of(vr[2], w), word_of(vr[3], w), sel);
+      const uint32_t x3 = __byte_perm(word_of(vr[2], w + 2), word_of(vr[3], w + 2), sel);
+      mma16816<__half>(acc[2 * p], e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x1), e4m3x2_to_f16x2(x2),
+                       e4m3x2_to_f16x2(x3), b0, b1);
+      mma16816<__half>(acc[2 * p + 1], e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x1 >> 16),
+                       e4m3x2_to_f16x2(x2 >> 16), e4m3x2_to_f16x2(x3 >> 16), b0, b1);
+    }
+  }
+
+  __device__ __forceinline__ void finish_sums() {
+#pragma unroll
+    for (int o = 4; o <= 16; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+  }
+
+  // Entries chunk_dim(lane, k) .. + 7 of head 2c + e, scaled by `mul`.
+  __device__ __forceinline__ void chunk_values(int e, int k, float mul, float (&v)[8]) const {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) v[mt] = acc[mt][2 * k + e] * mul;
+  }
+  __device__ __forceinline__ static int chunk_dim(int lane, int k) { return 16 * (lane >> 2) + 8 * k; }
+  static constexpr int kChunks = 2;
+};
+
 // ===================================================================== shared argument block
 
 struct DecodeArgs {
@@ -273,6 +474,8 @@ struct DecodeArgs {
   const void* v_new;
   void* k_cache_w;            // the pool, for the appended rows
   void* v_cache_w;
+  const float* k_scale;       // E4M3 pool only: f32[Hkv] scales of K and V codes
+  const float* v_scale;
   float scale_log2;           // scale * log2(e)
   int32_t num_seqs;
   int32_t num_q_heads;
@@ -305,41 +508,64 @@ __device__ __forceinline__ int tile_row(int phys, int kvh, const DecodeArgs& a) 
   return (phys * a.num_kv_heads + kvh) * kBlockSize;
 }
 
+// Byte geometry of one (block, KV head) K or V tile: 16 rows of D elements
+// (2 bytes for fp16 / bf16, 1 for E4M3), loaded as 128-byte-wide TMA boxes of
+// 16 rows (2 KB each) with the 128-byte swizzle.
+template <int D, bool F8>
+struct KvTile {
+  static constexpr int kRowBytes = F8 ? D : 2 * D;
+  static constexpr int kBoxes = kRowBytes / 128;
+  static constexpr int kBoxElems = F8 ? 128 : 64;
+  static constexpr int kTileBytes = kBlockSize * kRowBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+};
+
 // TMA loads of one block's K and V tiles into a stage, completing on `bar`
 // (whose transaction count the caller has set).
-template <int D>
+template <int D, bool F8 = false>
 __device__ __forceinline__ void issue_tiles(uint32_t stage, uint32_t bar, const CUtensorMap* mk,
                                             const CUtensorMap* mv, int row, uint64_t policy) {
-  using Shape = TileShape<D>;
+  using Tile = KvTile<D, F8>;
 #pragma unroll
-  for (int bx = 0; bx < Shape::kBoxes; ++bx) {
-    tma_load_2d(stage + bx * 2048, mk, bx * 64, row, bar, policy);
-    tma_load_2d(stage + Shape::kTileBytes + bx * 2048, mv, bx * 64, row, bar, policy);
+  for (int bx = 0; bx < Tile::kBoxes; ++bx) {
+    tma_load_2d(stage + bx * 2048, mk, bx * Tile::kBoxElems, row, bar, policy);
+    tma_load_2d(stage + Tile::kTileBytes + bx * 2048, mv, bx * Tile::kBoxElems, row, bar, policy);
   }
 }
 
-template <int D>
+template <int D, bool F8 = false>
 __device__ __forceinline__ void issue_block(uint32_t stage, uint32_t bar, const CUtensorMap* mk,
                                             const CUtensorMap* mv, int row, uint64_t policy) {
-  mbar_arrive_expect_tx(bar, TileShape<D>::kStageBytes);
-  issue_tiles<D>(stage, bar, mk, mv, row, policy);
+  mbar_arrive_expect_tx(bar, KvTile<D, F8>::kStageBytes);
+  issue_tiles<D, F8>(stage, bar, mk, mv, row, policy);
 }
 
 // ===================================================================== persistent kernel
 
-template <int D>
+// 24 KB of K/V in flight per warp: 3 stages of 8 KB (fp16/bf16, D = 128) or
+// 6 of 4 KB (D = 64, or E4M3 with D = 128).
+template <int D, bool F8 = false>
 struct PersistentShape {
   static constexpr int kWarps = 8;
-  static constexpr int kStages = D == 128 ? 3 : 6;  // per warp
-  static constexpr int kRingBytes = kWarps * kStages * TileShape<D>::kStageBytes;
+  static constexpr int kStages = 24576 / KvTile<D, F8>::kStageBytes;  // per warp
+  static constexpr int kRingBytes = kWarps * kStages * KvTile<D, F8>::kStageBytes;
 };
 
-// Dynamic shared memory: [ring][appended-token rows][prefix P[B+1]][context ctx[B]]
-// (+1 KB alignment slack).
-template <int D>
+// Dynamic shared memory: [ring][appended-token rows (fp16/bf16, K and V)]
+// [prefix P[B+1]][context ctx[B]] (+1 KB alignment slack).
+template <int D, bool F8 = false>
 constexpr size_t persistent_smem_bytes(int num_seqs) {
-  return PersistentShape<D>::kRingBytes + PersistentShape<D>::kWarps * PersistentShape<D>::kStages * 4 * D +
+  return PersistentShape<D, F8>::kRingBytes +
+         PersistentShape<D, F8>::kWarps * PersistentShape<D, F8>::kStages * 4 * D +
          (2 * static_cast<size_t>(num_seqs) + 1) * 4 + 1024;
+}
+
+// Largest batch whose prefix arrays fit beside the ring in 227 KB of shared
+// memory (1.5 KB kept for the static arrays, which take 1.2 KB), at most 2048.
+template <int D, bool F8 = false>
+constexpr int persistent_max_seqs() {
+  constexpr long long room = 232448LL - 1536 - static_cast<long long>(persistent_smem_bytes<D, F8>(0));
+  return room / 8 < 2048 ? static_cast<int>(room / 8) : 2048;
 }
 
 // Work partition of the persistent kernel.  The flattened block space
@@ -418,21 +644,25 @@ __device__ __forceinline__ void context_prefix(const DecodeArgs& a, int* s_P, in
   __syncthreads();
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
+// F8: the pool holds E4M3 codes (D = 128 only); the query, output and the
+// appended token's K/V stay fp16/bf16 and the append quantises in-kernel.
+template <typename T, int D, bool F8 = false>
+__global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
     decode_persistent_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                              const DecodeArgs a) {
-  using Shape = TileShape<D>;
-  constexpr int NW = PersistentShape<D>::kWarps;
-  constexpr int SW = PersistentShape<D>::kStages;
-  constexpr int kRowBytes = D * 2;  // one token's K (or V) row for one KV head
+  static_assert(!F8 || D == 128, "the E4M3 path is built for head_dim 128");
+  using Tile = KvTile<D, F8>;
+  using Attn = std::conditional_t<F8, WarpAttnE4M3<T>, WarpAttn<T, D>>;
+  constexpr int NW = PersistentShape<D, F8>::kWarps;
+  constexpr int SW = PersistentShape<D, F8>::kStages;
+  constexpr int kRowBytes = D * 2;  // one appended token's K (or V) row for one KV head (fp16/bf16)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[NW][SW];
   __shared__ int4 s_desc[NW][SW];  // per stage: unit, block j, segment id | flags << 28, pool row
   __shared__ int s_warp_sum[NW];
 
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* side = ring + PersistentShape<D>::kRingBytes;  // [NW][SW][K row, V row] of appended tokens
+  uint8_t* side = ring + PersistentShape<D, F8>::kRingBytes;  // [NW][SW][K row, V row] of appended tokens
   int* s_P = reinterpret_cast<int*>(side + NW * SW * 2 * kRowBytes);
   int* s_ctx = s_P + a.num_seqs + 1;
 
@@ -468,7 +698,7 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
     j = rem - kvh * nb;
   };
 
-  uint8_t* wring = ring + warp * SW * Shape::kStageBytes;
+  uint8_t* wring = ring + warp * SW * Tile::kStageBytes;
   uint8_t* wside = side + warp * SW * 2 * kRowBytes;
   const uint64_t policy = l2_evict_first_policy();
   if (lane == 0) {
@@ -538,7 +768,8 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- consume side
-  WarpAttn<T, D> at;
+  Attn at;
+  float unit_sl2 = a.scale_log2, unit_vs = 1.f;  // logit scale (log2 units) and output factor of the unit
   int unit_first_j = 0;
   bool seg_first_flush = true;
   int issued = 0, consumed = 0;
@@ -563,13 +794,13 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
         const uint32_t bar = smem_u32(&full_bar[warp][st]);
         if (fused_append && unit_last) {
           // The block that receives this step's token: fetch the token's K and V rows too.
-          mbar_arrive_expect_tx(bar, Shape::kStageBytes + 2 * kRowBytes);
+          mbar_arrive_expect_tx(bar, Tile::kStageBytes + 2 * kRowBytes);
           const uint32_t sd = smem_u32(wside + st * 2 * kRowBytes);
           bulk_load(sd, static_cast<const T*>(a.k_new) + static_cast<int64_t>(u) * D, kRowBytes, bar);
           bulk_load(sd + kRowBytes, static_cast<const T*>(a.v_new) + static_cast<int64_t>(u) * D, kRowBytes, bar);
-          issue_tiles<D>(smem_u32(wring + st * Shape::kStageBytes), bar, &tmap_k, &tmap_v, row, policy);
+          issue_tiles<D, F8>(smem_u32(wring + st * Tile::kStageBytes), bar, &tmap_k, &tmap_v, row, policy);
         } else {
-          issue_block<D>(smem_u32(wring + st * Shape::kStageBytes), bar, &tmap_k, &tmap_v, row, policy);
+          issue_block<D, F8>(smem_u32(wring + st * Tile::kStageBytes), bar, &tmap_k, &tmap_v, row, policy);
         }
       }
       ++issued;
@@ -589,16 +820,27 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
     const int b = u / Hkv, kvh = u - b * Hkv;
     const int ctx = s_ctx[b];
     const int nb = (ctx + kBlockSize - 1) / kBlockSize;
-    uint8_t* ks = wring + st * Shape::kStageBytes;
+    uint8_t* ks = wring + st * Tile::kStageBytes;
     if (fused_append && j == nb - 1) {
       // Append: the token at position ctx - 1 goes into this block's row r, in
       // the staged tile (for this step's attention) and in the pool.
       const int r = (ctx - 1) % kBlockSize;
       constexpr int kChunksPerRow = D / 8;
-      if (lane < 2 * kChunksPerRow) {
+      if constexpr (F8) {
+        // Lanes 0-15 quantise 8 entries each of the K row, lanes 16-31 of the V row.
+        const int v = lane >> 4, c8 = lane & 15;
+        const uint4 val = *reinterpret_cast<const uint4*>(wside + st * 2 * kRowBytes + v * kRowBytes + c8 * 16);
+        const uint2 code = quantize8<T>(val, __ldg((v ? a.v_scale : a.k_scale) + kvh));
+        uint8_t* tile = ks + v * Tile::kTileBytes;
+        *reinterpret_cast<uint2*>(tile + r * 128 + (((c8 >> 1) ^ (r & 7)) << 4) + 8 * (c8 & 1)) = code;
+        if (dsc.w >= 0) {
+          uint8_t* cache = static_cast<uint8_t*>(v ? a.v_cache_w : a.k_cache_w);
+          *reinterpret_cast<uint2*>(cache + (static_cast<int64_t>(dsc.w) + r) * D + 8 * c8) = code;
+        }
+      } else if (lane < 2 * kChunksPerRow) {
         const int v = lane / kChunksPerRow, c16 = lane % kChunksPerRow;
         const uint4 val = *reinterpret_cast<const uint4*>(wside + st * 2 * kRowBytes + v * kRowBytes + c16 * 16);
-        uint8_t* tile = ks + v * Shape::kTileBytes;
+        uint8_t* tile = ks + v * Tile::kTileBytes;
         *reinterpret_cast<uint4*>(tile + (c16 >> 3) * 2048 + r * 128 + (((c16 & 7) ^ (r & 7)) << 4)) = val;
         if (dsc.w >= 0) {
           T* cache = static_cast<T*>(v ? a.v_cache_w : a.k_cache_w);
@@ -612,8 +854,12 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
       unit_first_j = j;
       at.load_q(static_cast<const T*>(a.q) + (static_cast<int64_t>(b) * a.num_q_heads + kvh * g) * D, g, lane);
       at.reset();
+      if constexpr (F8) {
+        unit_sl2 = a.scale_log2 * __ldg(a.k_scale + kvh);
+        unit_vs = __ldg(a.v_scale + kvh);
+      }
     }
-    at.block(ks, ks + Shape::kTileBytes, min(kBlockSize, ctx - j * kBlockSize), a.scale_log2, lane);
+    at.block(ks, ks + Tile::kTileBytes, min(kBlockSize, ctx - j * kBlockSize), unit_sl2, lane);
     ++consumed;
 
     if (j == nb - 1 || last_of_seg) {
@@ -630,18 +876,18 @@ __global__ void __launch_bounds__(PersistentShape<D>::kWarps * 32, 1)
         if (complete) {
           T* orow = static_cast<T*>(a.out) + (static_cast<int64_t>(b) * a.num_q_heads + kvh * g + h) * D;
 #pragma unroll
-          for (int kk = 0; kk < WarpAttn<T, D>::kChunks; ++kk) {
+          for (int kk = 0; kk < Attn::kChunks; ++kk) {
             float v[8];
-            at.chunk_values(e, kk, 1.0f / l, v);
-            *reinterpret_cast<uint4*>(orow + WarpAttn<T, D>::chunk_dim(lane, kk)) = pack8<T>(v);
+            at.chunk_values(e, kk, unit_vs / l, v);
+            *reinterpret_cast<uint4*>(orow + Attn::chunk_dim(lane, kk)) = pack8<T>(v);
           }
         } else {
           float* prow = a.part_o + (pbase + h) * D;
 #pragma unroll
-          for (int kk = 0; kk < WarpAttn<T, D>::kChunks; ++kk) {
+          for (int kk = 0; kk < Attn::kChunks; ++kk) {
             float v[8];
-            at.chunk_values(e, kk, 1.0f / l, v);
-            float4* dst = reinterpret_cast<float4*>(prow + WarpAttn<T, D>::chunk_dim(lane, kk));
+            at.chunk_values(e, kk, unit_vs / l, v);
+            float4* dst = reinterpret_cast<float4*>(prow + Attn::chunk_dim(lane, kk));
             dst[0] = make_float4(v[0], v[1], v[2], v[3]);
             dst[1] = make_float4(v[4], v[5], v[6], v[7]);
           }

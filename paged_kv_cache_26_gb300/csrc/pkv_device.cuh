@@ -15,6 +15,7 @@ enum : unsigned {
   kErrSlot = 2u,      // an append slot outside the pool
   kErrContext = 4u,   // a context length < 0 or longer than its block table
   kErrTimeout = 8u,   // a bounded wait gave up
+  kErrQuery = 16u,    // E4M3 path: a query value beyond the fp16 range
 };
 
 // A wait that has not finished after this long is treated as lost.
@@ -168,6 +169,25 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
     __half2 h = *reinterpret_cast<__half2*>(&v);
     return __half22float2(h);
   }
+}
+
+// ------------------------------------------------------------------ E4M3
+
+// Two E4M3 codes (bits 0-7 and 8-15) to their exact fp16 values (bits 0-15
+// and 16-31 of the result).  Every E4M3 value is an fp16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t r;
+  const uint16_t v = static_cast<uint16_t>(two_codes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+
+// E4M3 codes of two fp32 values, round to nearest even, saturating to +-448:
+// lo in bits 0-7, hi in bits 8-15.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // Transpose an 8x8 matrix of 16-bit elements held in the mma fragment layout

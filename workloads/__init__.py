@@ -239,3 +239,38 @@ def _plant_spikes(spec, scale, q, k_new, kcache, tables, lens, spike_pos):
             else:
                 kcache[int(tables[b, p // bs]), h, p % bs] = key
 
+
+
+# ---------------------------------------------------------------- E4M3 pools
+
+@dataclass
+class Fp8Caches:
+    """E4M3 stand-ins of a workload's caches (before the append)."""
+
+    k_cache: List[torch.Tensor]   # per layer: uint8[NB][Hkv][BS][D], E4M3 codes
+    v_cache: List[torch.Tensor]
+    k_scale: List[torch.Tensor]   # per layer: float32[Hkv]
+    v_scale: List[torch.Tensor]
+
+
+def fp8_caches(w: Workload, seed: int = 0) -> Fp8Caches:
+    """Draw an E4M3 pool for workload ``w``: per layer and KV head a K scale and
+    a V scale drawn uniformly from [0.004, 0.02], and as codes the workload's own
+    N(0,1) cache values over those scales, cast by torch's float8_e4m3fn
+    conversion after clamping to +-448 (so values up to ~1.8-9 sigma are
+    represented and the rest sit at +-448).  Every non-token slot holds the NaN
+    code 0x7F.  The new token's K/V (``w.k_new`` / ``w.v_new``) stay fp16/bf16:
+    the append quantises them."""
+    rng = np.random.default_rng(seed + 7919)
+    Hk = w.spec.num_kv_heads
+    out = Fp8Caches([], [], [], [])
+    for layer in range(len(w.k_cache)):
+        for src, codes, scales in ((w.k_cache[layer], out.k_cache, out.k_scale),
+                                   (w.v_cache[layer], out.v_cache, out.v_scale)):
+            s = torch.from_numpy(rng.uniform(0.004, 0.02, Hk).astype(np.float32)).to(src.device)
+            x = src.float() / s.view(1, Hk, 1, 1)
+            c = x.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+            c[torch.isnan(x)] = 0x7F
+            codes.append(c)
+            scales.append(s)
+    return out
