@@ -228,7 +228,7 @@ int paged_decode_attention_no_alloc(const void* q, const void* k_cache, const vo
  * as fp16 tensor-core mma (E4M3 values are exact in fp16), so a bf16 query is
  * converted to fp16: a query entry beyond +-65504 sets the error word
  * (PKV_ERR_OUT_OF_RANGE from paged_kv_check_status).
- * Limits: head_dim 128 for attention; at most 1024 sequences per call; only
+ * Limits: head_dim 128 for attention; at most 2048 sequences per call; only
  * the automatic persistent path (its workspace is
  * paged_decode_workspace_bytes(dims, 0) bytes, zero-filled once, as above).
  * Bad shapes and pointers return PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED.

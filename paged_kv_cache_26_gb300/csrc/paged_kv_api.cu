@@ -145,7 +145,7 @@ struct SplitPlan {
 };
 
 // Largest batch of the persistent kernel: its prefix sums live in shared
-// memory beside the ring (2048 for fp16/bf16 pools, 1024 for E4M3 pools).
+// memory beside the ring (2048 sequences for every pool format built).
 int max_persistent_seqs(const pkv_dims* d, bool f8) {
   if (f8) return pkv::persistent_max_seqs<128, true>() / 256 * 256;
   return d->head_dim == 128 ? pkv::persistent_max_seqs<128>() : pkv::persistent_max_seqs<64>();

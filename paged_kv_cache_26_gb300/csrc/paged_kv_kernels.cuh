@@ -366,8 +366,10 @@ struct WarpAttnE4M3 {
     if (__any_sync(0xffffffffu, big) && lane == 0) flag_error(kErrQuery);
   }
 
-  __device__ __forceinline__ void block(const uint8_t* ks, const uint8_t* vs, int valid, float scale_log2,
-                                        int lane) {
+  // Scores of one 16-token K tile against the group: s[0..1] token gid and
+  // s[2..3] token gid + 8 (heads 2c, 2c+1), unscaled; two interleaved mma
+  // chains.
+  __device__ __forceinline__ void scores(const uint8_t* ks, int lane, float (&x)[4]) const {
     const int gid = lane >> 2, c = lane & 3;
     const uint8_t* kr0 = ks + gid * 128;
     const uint8_t* kr1 = ks + (gid + 8) * 128;  // same swizzle phase: (gid + 8) & 7 == gid
@@ -387,47 +389,27 @@ struct WarpAttnE4M3 {
       else
         mma16816<__half>(s, a0, a1, a2, a3, qf[2 * j], qf[2 * j + 1]);
     }
-    float x0 = (s[0] + t[0]) * scale_log2, x1 = (s[1] + t[1]) * scale_log2;  // token gid
-    float x2 = (s[2] + t[2]) * scale_log2, x3 = (s[3] + t[3]) * scale_log2;  // token gid + 8
-    if (valid < kBlockSize) {
-      if (gid >= valid) x0 = x1 = -INFINITY;
-      if (gid + 8 >= valid) x2 = x3 = -INFINITY;
-    }
-    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
-    for (int o = 4; o <= 16; o <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-    }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
-    const uint32_t plo = pack2<__half>(exp2f(x0 - mn0), exp2f(x1 - mn1));
-    const uint32_t phi = pack2<__half>(exp2f(x2 - mn0), exp2f(x3 - mn1));
-    const float2 fl = unpack2<__half>(plo), fh = unpack2<__half>(phi);
-    l0 = l0 * al0 + (fl.x + fh.x);
-    l1 = l1 * al1 + (fl.y + fh.y);
-    const uint32_t b0 = movmatrix_trans(plo);
-    const uint32_t b1 = movmatrix_trans(phi);
+    for (int i = 0; i < 4; ++i) x[i] = s[i] + t[i];
+  }
 
-    uint4 vr[4];  // chunk gid of V rows 2c, 2c+1, 2c+8, 2c+9
+  // Chunk gid of V rows 2c, 2c+1, 2c+8, 2c+9 of one tile; rows at or past
+  // `valid` read as zeros (never 0 * NaN).
+  __device__ __forceinline__ static void load_v(const uint8_t* vs, int valid, int lane, uint4 (&vr)[4]) {
+    const int gid = lane >> 2, c = lane & 3;
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
       const int row = 2 * c + (rr & 1) + 8 * (rr >> 1);
       vr[rr] = *reinterpret_cast<const uint4*>(vs + row * 128 + ((gid ^ (row & 7)) << 4));
-      if (valid < kBlockSize && row >= valid) vr[rr] = make_uint4(0, 0, 0, 0);  // never 0 * NaN
+      if (valid < kBlockSize && row >= valid) vr[rr] = make_uint4(0, 0, 0, 0);
     }
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      acc[mt][0] *= al0;
-      acc[mt][1] *= al1;
-      acc[mt][2] *= al0;
-      acc[mt][3] *= al1;
-    }
-    // m-tiles 2p and 2p + 1 read bytes 2p, 2p + 1 (rows m = gid) and 8 + 2p,
-    // 9 + 2p (rows m = gid + 8) of the chunks; interleaving the byte pairs of
-    // two token rows puts each mma operand's two tokens side by side.
+  }
+
+  // acc += V^T P^T for one tile.  m-tiles 2p and 2p + 1 read bytes 2p, 2p + 1
+  // (rows m = gid) and 8 + 2p, 9 + 2p (rows m = gid + 8) of the chunks;
+  // interleaving the byte pairs of two token rows puts each mma operand's two
+  // tokens side by side.
+  __device__ __forceinline__ void pv(const uint4 (&vr)[4], uint32_t b0, uint32_t b1) {
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
       const int w = p >> 1;
@@ -441,6 +423,99 @@ struct WarpAttnE4M3 {
       mma16816<__half>(acc[2 * p + 1], e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x1 >> 16),
                        e4m3x2_to_f16x2(x2 >> 16), e4m3x2_to_f16x2(x3 >> 16), b0, b1);
     }
+  }
+
+  __device__ __forceinline__ void rescale(float al0, float al1) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      acc[mt][0] *= al0;
+      acc[mt][1] *= al1;
+      acc[mt][2] *= al0;
+      acc[mt][3] *= al1;
+    }
+  }
+
+  // Scores of tokens at or past `valid` in one tile become -inf.
+  __device__ __forceinline__ static void mask(float (&x)[4], int valid, int lane) {
+    const int gid = lane >> 2;
+    if (valid < kBlockSize) {
+      if (gid >= valid) x[0] = x[1] = -INFINITY;
+      if (gid + 8 >= valid) x[2] = x[3] = -INFINITY;
+    }
+  }
+
+  // Accumulate one block whose K and V tiles sit (swizzled) at ks / vs; the
+  // first `valid` (1..16) of its 16 tokens belong to the context.
+  __device__ __forceinline__ void block(const uint8_t* ks, const uint8_t* vs, int valid, float scale_log2,
+                                        int lane) {
+    float x[4];
+    scores(ks, lane, x);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] *= scale_log2;
+    mask(x, valid, lane);
+    float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+    for (int o = 4; o <= 16; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);  // finite: token 0 is valid
+    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    const uint32_t plo = pack2<__half>(exp2f(x[0] - mn0), exp2f(x[1] - mn1));  // token gid
+    const uint32_t phi = pack2<__half>(exp2f(x[2] - mn0), exp2f(x[3] - mn1));  // token gid + 8
+    const float2 fl = unpack2<__half>(plo), fh = unpack2<__half>(phi);
+    l0 = l0 * al0 + (fl.x + fh.x);  // sums of the rounded weights the P V product uses
+    l1 = l1 * al1 + (fl.y + fh.y);
+    uint4 vr[4];
+    load_v(vs, valid, lane, vr);
+    rescale(al0, al1);
+    pv(vr, movmatrix_trans(plo), movmatrix_trans(phi));
+  }
+
+  // Two consecutive blocks of one unit (tiles kA/vA, then kB/vB) as one
+  // 32-token softmax step; `valid` (1..32) tokens belong to the context.
+  __device__ __forceinline__ void block2(const uint8_t* kA, const uint8_t* vA, const uint8_t* kB, const uint8_t* vB,
+                                         int valid, float scale_log2, int lane) {
+    if (valid <= kBlockSize) {  // the second block is not part of this stage
+      block(kA, vA, valid, scale_log2, lane);
+      return;
+    }
+    float xa[4], xb[4];
+    scores(kA, lane, xa);
+    scores(kB, lane, xb);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      xa[i] *= scale_log2;
+      xb[i] *= scale_log2;
+    }
+    mask(xb, valid - kBlockSize, lane);
+    float mx0 = fmaxf(fmaxf(xa[0], xa[2]), fmaxf(xb[0], xb[2]));
+    float mx1 = fmaxf(fmaxf(xa[1], xa[3]), fmaxf(xb[1], xb[3]));
+#pragma unroll
+    for (int o = 4; o <= 16; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    const uint32_t pal = pack2<__half>(exp2f(xa[0] - mn0), exp2f(xa[1] - mn1));
+    const uint32_t pah = pack2<__half>(exp2f(xa[2] - mn0), exp2f(xa[3] - mn1));
+    const uint32_t pbl = pack2<__half>(exp2f(xb[0] - mn0), exp2f(xb[1] - mn1));
+    const uint32_t pbh = pack2<__half>(exp2f(xb[2] - mn0), exp2f(xb[3] - mn1));
+    const float2 f0 = unpack2<__half>(pal), f1 = unpack2<__half>(pah);
+    const float2 f2 = unpack2<__half>(pbl), f3 = unpack2<__half>(pbh);
+    l0 = l0 * al0 + ((f0.x + f1.x) + (f2.x + f3.x));
+    l1 = l1 * al1 + ((f0.y + f1.y) + (f2.y + f3.y));
+    uint4 va[4], vb[4];
+    load_v(vA, kBlockSize, lane, va);
+    load_v(vB, valid - kBlockSize, lane, vb);
+    rescale(al0, al1);
+    pv(va, movmatrix_trans(pal), movmatrix_trans(pah));
+    pv(vb, movmatrix_trans(pbl), movmatrix_trans(pbh));
   }
 
   __device__ __forceinline__ void finish_sums() {
@@ -542,13 +617,18 @@ __device__ __forceinline__ void issue_block(uint32_t stage, uint32_t bar, const 
 
 // ===================================================================== persistent kernel
 
-// 24 KB of K/V in flight per warp: 3 stages of 8 KB (fp16/bf16, D = 128) or
-// 6 of 4 KB (D = 64, or E4M3 with D = 128).
+// 24 KB of K/V in flight per warp.  A stage holds one block (fp16/bf16: 3
+// stages of 8 KB for D = 128, 6 of 4 KB for D = 64) or, for E4M3, two
+// consecutive blocks of one unit (3 stages of 2 x 4 KB): 32 tokens per softmax
+// step halve the per-block bookkeeping and give each warp two independent
+// score chains.
 template <int D, bool F8 = false>
 struct PersistentShape {
   static constexpr int kWarps = 8;
-  static constexpr int kStages = 24576 / KvTile<D, F8>::kStageBytes;  // per warp
-  static constexpr int kRingBytes = kWarps * kStages * KvTile<D, F8>::kStageBytes;
+  static constexpr int kBlocksPerStage = F8 ? 2 : 1;
+  static constexpr int kStageBytes = kBlocksPerStage * KvTile<D, F8>::kStageBytes;
+  static constexpr int kStages = 24576 / kStageBytes;  // per warp
+  static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
 };
 
 // Dynamic shared memory: [ring][appended-token rows (fp16/bf16, K and V)]
@@ -652,17 +732,20 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
                              const DecodeArgs a) {
   static_assert(!F8 || D == 128, "the E4M3 path is built for head_dim 128");
   using Tile = KvTile<D, F8>;
+  using Shape = PersistentShape<D, F8>;
   using Attn = std::conditional_t<F8, WarpAttnE4M3<T>, WarpAttn<T, D>>;
-  constexpr int NW = PersistentShape<D, F8>::kWarps;
-  constexpr int SW = PersistentShape<D, F8>::kStages;
+  constexpr int NW = Shape::kWarps;
+  constexpr int SW = Shape::kStages;
+  constexpr int NPS = Shape::kBlocksPerStage;
   constexpr int kRowBytes = D * 2;  // one appended token's K (or V) row for one KV head (fp16/bf16)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[NW][SW];
-  __shared__ int4 s_desc[NW][SW];  // per stage: unit, block j, segment id | flags << 28, pool row
+  __shared__ int4 s_desc[NW][SW];  // per stage: sequence, KV head, first block j, segment id | flags << 28
+  __shared__ int s_prow[NW][SW];   // per stage: pool row of its last block (the fused append's target)
   __shared__ int s_warp_sum[NW];
 
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* side = ring + PersistentShape<D, F8>::kRingBytes;  // [NW][SW][K row, V row] of appended tokens
+  uint8_t* side = ring + Shape::kRingBytes;  // [NW][SW][K row, V row] of appended tokens
   int* s_P = reinterpret_cast<int*>(side + NW * SW * 2 * kRowBytes);
   int* s_ctx = s_P + a.num_seqs + 1;
 
@@ -683,8 +766,8 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
   const Partition part(Hkv * s_P[B], gridDim.x * NW);
   const int gw = blockIdx.x * NW + warp;
 
-  // Unit (b, kvh) and block j of flattened block f: units are ordered
-  // (b, kvh) and unit (b, kvh) holds blocks [Hkv*P[b] + kvh*nb, +nb).
+  // Sequence b, KV head kvh and block j of flattened block f: units are
+  // ordered (b, kvh) and unit (b, kvh) holds blocks [Hkv*P[b] + kvh*nb, +nb).
   auto locate = [&](int f, int& b, int& kvh, int& j) {
     int lo = 0, hi = B - 1;
     while (lo < hi) {
@@ -698,7 +781,7 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
     j = rem - kvh * nb;
   };
 
-  uint8_t* wring = ring + warp * SW * Tile::kStageBytes;
+  uint8_t* wring = ring + warp * SW * Shape::kStageBytes;
   uint8_t* wside = side + warp * SW * 2 * kRowBytes;
   const uint64_t policy = l2_evict_first_policy();
   if (lane == 0) {
@@ -707,25 +790,26 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
   }
 
   // ---- issue side: current segment [seg_s, seg_e) and a 32-block window of it,
-  // lane i describing block win_s + i (unit, block j, pool row).
+  // lane i describing block win_s + i (sequence, KV head, block j, pool row).
   int seg, seg_s, seg_e;
   part.head(gw, seg_s, seg_e);
   seg = gw;
   int win_s = seg_s, win_e = seg_s, ip = seg_s;
-  int wu = -1, wj = 0, wrow = -kBlockSize;
+  int wb = -1, wkvh = -1, wj = 0, wrow = -kBlockSize;
   bool more = true;
   auto fill_window = [&]() {
     win_s = ip;
     win_e = min(seg_e, ip + 32);
-    wu = -1; wj = 0; wrow = -kBlockSize;
+    wb = -1; wkvh = -1; wj = 0; wrow = -kBlockSize;
     if (win_s + lane < win_e) {
       int b, kvh, j;
       locate(win_s + lane, b, kvh, j);
-      wu = b * Hkv + kvh;
+      wb = b;
+      wkvh = kvh;
       wj = j;
       wrow = tile_row(__ldg(a.block_tables + static_cast<int64_t>(b) * a.max_blocks + j), kvh, a);
       if (j == 0 || lane == 0)  // a unit starts here: bring its query rows into L2
-        prefetch_l2_bulk(static_cast<const T*>(a.q) + static_cast<int64_t>(wu) * g * D,
+        prefetch_l2_bulk(static_cast<const T*>(a.q) + (static_cast<int64_t>(b) * Hkv + kvh) * g * D,
                          static_cast<uint32_t>(g * D * sizeof(T)));
     }
   };
@@ -773,6 +857,8 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
   int unit_first_j = 0;
   bool seg_first_flush = true;
   int issued = 0, consumed = 0;
+  int st_i = 0;                  // stage the next issue fills
+  int st_c = 0, ph_c = 0;        // stage the next consume reads, and its phase parity
   bool ok = true;
   while (true) {
     while (more && issued - consumed < SW) {
@@ -781,70 +867,91 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
         if (!more) break;
       }
       const int src = ip - win_s;
-      const int u = __shfl_sync(0xffffffffu, wu, src);
+      const int b = __shfl_sync(0xffffffffu, wb, src);
+      const int kvh = __shfl_sync(0xffffffffu, wkvh, src);
       const int j = __shfl_sync(0xffffffffu, wj, src);
       const int row = __shfl_sync(0xffffffffu, wrow, src);
-      const int st = issued % SW;
-      if (lane == 0) {
-        const int b = u / Hkv;
-        const bool unit_last = j == (s_ctx[b] + kBlockSize - 1) / kBlockSize - 1;
-        const int flags = (ip == seg_s ? 1 : 0) | (ip == seg_e - 1 ? 2 : 0);
-        s_desc[warp][st] = make_int4(u, j, seg | (flags << 28), row);
-        fence_proxy_async_smem();  // earlier generic accesses of this stage come before the refill
-        const uint32_t bar = smem_u32(&full_bar[warp][st]);
-        if (fused_append && unit_last) {
-          // The block that receives this step's token: fetch the token's K and V rows too.
-          mbar_arrive_expect_tx(bar, Tile::kStageBytes + 2 * kRowBytes);
-          const uint32_t sd = smem_u32(wside + st * 2 * kRowBytes);
-          bulk_load(sd, static_cast<const T*>(a.k_new) + static_cast<int64_t>(u) * D, kRowBytes, bar);
-          bulk_load(sd + kRowBytes, static_cast<const T*>(a.v_new) + static_cast<int64_t>(u) * D, kRowBytes, bar);
-          issue_tiles<D, F8>(smem_u32(wring + st * Tile::kStageBytes), bar, &tmap_k, &tmap_v, row, policy);
-        } else {
-          issue_block<D, F8>(smem_u32(wring + st * Tile::kStageBytes), bar, &tmap_k, &tmap_v, row, policy);
+      int n = 1, row2 = row;
+      if constexpr (NPS == 2) {
+        // Take the next block too when it is in this window (so in this
+        // segment) and belongs to the same unit.
+        const int src2 = src + 1 < 32 ? src + 1 : src;
+        const int b2 = __shfl_sync(0xffffffffu, wb, src2);
+        const int kvh2 = __shfl_sync(0xffffffffu, wkvh, src2);
+        const int r2 = __shfl_sync(0xffffffffu, wrow, src2);
+        if (ip + 1 < win_e && b2 == b && kvh2 == kvh) {
+          n = 2;
+          row2 = r2;
         }
       }
+      if (lane == 0) {
+        const bool unit_last = j + n == (s_ctx[b] + kBlockSize - 1) / kBlockSize;
+        const int flags = (ip == seg_s ? 1 : 0) | (ip + n == seg_e ? 2 : 0) | ((n - 1) << 2);
+        s_desc[warp][st_i] = make_int4(b, kvh, j, seg | (flags << 28));
+        s_prow[warp][st_i] = row2;
+        fence_proxy_async_smem();  // earlier generic accesses of this stage come before the refill
+        const uint32_t bar = smem_u32(&full_bar[warp][st_i]);
+        const uint32_t stage = smem_u32(wring + st_i * Shape::kStageBytes);
+        const int64_t unit = static_cast<int64_t>(b) * Hkv + kvh;
+        if (fused_append && unit_last) {
+          // The block that receives this step's token: fetch the token's K and V rows too.
+          mbar_arrive_expect_tx(bar, n * Tile::kStageBytes + 2 * kRowBytes);
+          const uint32_t sd = smem_u32(wside + st_i * 2 * kRowBytes);
+          bulk_load(sd, static_cast<const T*>(a.k_new) + unit * D, kRowBytes, bar);
+          bulk_load(sd + kRowBytes, static_cast<const T*>(a.v_new) + unit * D, kRowBytes, bar);
+        } else {
+          mbar_arrive_expect_tx(bar, n * Tile::kStageBytes);
+        }
+        issue_tiles<D, F8>(stage, bar, &tmap_k, &tmap_v, row, policy);
+        if (NPS == 2 && n == 2) issue_tiles<D, F8>(stage + Tile::kStageBytes, bar, &tmap_k, &tmap_v, row2, policy);
+      }
       ++issued;
-      ++ip;
+      ip += n;
+      st_i = st_i + 1 == SW ? 0 : st_i + 1;
     }
     __syncwarp();  // the descriptors written by lane 0 are visible to the warp
     if (consumed == issued) break;
 
-    const int st = consumed % SW;
-    if (!mbar_wait(smem_u32(&full_bar[warp][st]), (consumed / SW) & 1)) {  // timed out: flagged
+    if (!mbar_wait(smem_u32(&full_bar[warp][st_c]), ph_c)) {  // timed out: flagged
       ok = false;
       break;
     }
-    const int4 dsc = s_desc[warp][st];
-    const int u = dsc.x, j = dsc.y, sid = dsc.z & 0x0FFFFFFF;
-    const bool first_of_seg = (dsc.z >> 28) & 1, last_of_seg = (dsc.z >> 28) & 2;
-    const int b = u / Hkv, kvh = u - b * Hkv;
+    const int4 dsc = s_desc[warp][st_c];
+    const int b = dsc.x, kvh = dsc.y, j = dsc.z, sid = dsc.w & 0x0FFFFFFF;
+    const int flags = dsc.w >> 28;
+    const bool first_of_seg = flags & 1, last_of_seg = flags & 2;
+    const int n = 1 + ((flags >> 2) & 1);
     const int ctx = s_ctx[b];
     const int nb = (ctx + kBlockSize - 1) / kBlockSize;
-    uint8_t* ks = wring + st * Tile::kStageBytes;
-    if (fused_append && j == nb - 1) {
-      // Append: the token at position ctx - 1 goes into this block's row r, in
+    const int jl = j + n - 1;  // the stage's last block
+    uint8_t* ks = wring + st_c * Shape::kStageBytes;
+    if (fused_append && jl == nb - 1) {
+      // Append: the token at position ctx - 1 goes into row r of block jl, in
       // the staged tile (for this step's attention) and in the pool.
       const int r = (ctx - 1) % kBlockSize;
+      const int prow = s_prow[warp][st_c];
+      uint8_t* lt = ks + (n - 1) * Tile::kStageBytes;  // K tile of block jl; its V tile follows
+      const uint8_t* sd = wside + st_c * 2 * kRowBytes;
       constexpr int kChunksPerRow = D / 8;
       if constexpr (F8) {
         // Lanes 0-15 quantise 8 entries each of the K row, lanes 16-31 of the V row.
         const int v = lane >> 4, c8 = lane & 15;
-        const uint4 val = *reinterpret_cast<const uint4*>(wside + st * 2 * kRowBytes + v * kRowBytes + c8 * 16);
+        const uint4 val = *reinterpret_cast<const uint4*>(sd + v * kRowBytes + c8 * 16);
         const uint2 code = quantize8<T>(val, __ldg((v ? a.v_scale : a.k_scale) + kvh));
-        uint8_t* tile = ks + v * Tile::kTileBytes;
+        uint8_t* tile = lt + v * Tile::kTileBytes;
         *reinterpret_cast<uint2*>(tile + r * 128 + (((c8 >> 1) ^ (r & 7)) << 4) + 8 * (c8 & 1)) = code;
-        if (dsc.w >= 0) {
+        if (prow >= 0) {
           uint8_t* cache = static_cast<uint8_t*>(v ? a.v_cache_w : a.k_cache_w);
-          *reinterpret_cast<uint2*>(cache + (static_cast<int64_t>(dsc.w) + r) * D + 8 * c8) = code;
+          *reinterpret_cast<uint2*>(cache + (static_cast<int64_t>(prow) + r) * D + 8 * c8) = code;
         }
       } else if (lane < 2 * kChunksPerRow) {
         const int v = lane / kChunksPerRow, c16 = lane % kChunksPerRow;
-        const uint4 val = *reinterpret_cast<const uint4*>(wside + st * 2 * kRowBytes + v * kRowBytes + c16 * 16);
-        uint8_t* tile = ks + v * Tile::kTileBytes;
+        const uint4 val = *reinterpret_cast<const uint4*>(sd + v * kRowBytes + c16 * 16);
+        uint8_t* tile = lt + v * Tile::kTileBytes;
         *reinterpret_cast<uint4*>(tile + (c16 >> 3) * 2048 + r * 128 + (((c16 & 7) ^ (r & 7)) << 4)) = val;
-        if (dsc.w >= 0) {
+        if (prow >= 0) {
           T* cache = static_cast<T*>(v ? a.v_cache_w : a.k_cache_w);
-          *reinterpret_cast<uint4*>(cache + (static_cast<int64_t>(dsc.w) + r) * D + c16 * 8) = val;
+          *reinterpret_cast<uint4*>(cache + (static_cast<int64_t>(prow) + r) * D + c16 * 8) = val;
         }
       }
       __syncwarp();
@@ -859,14 +966,23 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
         unit_vs = __ldg(a.v_scale + kvh);
       }
     }
-    at.block(ks, ks + Tile::kTileBytes, min(kBlockSize, ctx - j * kBlockSize), unit_sl2, lane);
+    const int valid = min(n * kBlockSize, ctx - j * kBlockSize);
+    if constexpr (NPS == 2)
+      at.block2(ks, ks + Tile::kTileBytes, ks + Tile::kStageBytes, ks + Tile::kStageBytes + Tile::kTileBytes, valid,
+                unit_sl2, lane);
+    else
+      at.block(ks, ks + Tile::kTileBytes, valid, unit_sl2, lane);
     ++consumed;
+    if (++st_c == SW) {
+      st_c = 0;
+      ph_c ^= 1;
+    }
 
-    if (j == nb - 1 || last_of_seg) {
+    if (jl == nb - 1 || last_of_seg) {
       // ---- the unit ends here or the segment does: write it out, or leave a piece for the merge
       at.finish_sums();
       const int gid = lane >> 2, c = lane & 3;
-      const bool complete = unit_first_j == 0 && j == nb - 1;
+      const bool complete = unit_first_j == 0 && jl == nb - 1;
       const int64_t pbase = (static_cast<int64_t>(sid) * 2 + (seg_first_flush ? 0 : 1)) * kMaxGroup;
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
@@ -899,7 +1015,13 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
   }
   if (!ok && lane == 0) {
     // A wait gave up: let this warp's copies in flight land before the CTA exits.
-    for (int i = consumed; i < issued; ++i) mbar_wait(smem_u32(&full_bar[warp][i % SW]), (i / SW) & 1);
+    for (int i = consumed; i < issued; ++i) {
+      mbar_wait(smem_u32(&full_bar[warp][st_c]), ph_c);
+      if (++st_c == SW) {
+        st_c = 0;
+        ph_c ^= 1;
+      }
+    }
   }
 }
 

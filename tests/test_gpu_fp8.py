@@ -113,7 +113,7 @@ def test_fp8_edge_lengths(lens):
 
 
 def test_fp8_maximum_batch():
-    spec = wl.LLAMA3_8B.replace(name="b1024", batch=1024, lengths=("uniform", 1, 40), num_q_heads=8,
+    spec = wl.LLAMA3_8B.replace(name="b2048", batch=2048, lengths=("uniform", 1, 40), num_q_heads=8,
                                 num_kv_heads=2)
     w = wl.generate(spec, seed=4, device=DEV)
     check_fp8(w, wl.fp8_caches(w, seed=4), rows=sample_rows(w, 64))
@@ -180,10 +180,10 @@ def test_fp8_invalid_arguments_are_rejected():
     with pytest.raises(pkv.PagedKVError) as e:          # head_dim 64 is not built for E4M3
         pkv.paged_decode_attention_fp8(q, kc, kc, s, s, bt, cl, 0.1)
     assert e.value.code == -2
-    q = torch.zeros(1025, 8, 128, dtype=torch.bfloat16, device=dev)
+    q = torch.zeros(2049, 8, 128, dtype=torch.bfloat16, device=dev)
     kc = torch.zeros(4, 2, 16, 128, dtype=torch.uint8, device=dev)
-    bt = torch.zeros(1025, 1, dtype=torch.int32, device=dev)
-    cl = torch.ones(1025, dtype=torch.int32, device=dev)
+    bt = torch.zeros(2049, 1, dtype=torch.int32, device=dev)
+    cl = torch.ones(2049, dtype=torch.int32, device=dev)
     with pytest.raises(pkv.PagedKVError) as e:          # more sequences than the shared-memory prefix holds
         pkv.paged_decode_attention_fp8(q, kc, kc, s, s, bt, cl, 0.1)
     assert e.value.code == -2
