@@ -624,12 +624,13 @@ __device__ __forceinline__ void issue_block(uint32_t stage, uint32_t bar, const 
 // score chains.
 template <int D, bool F8 = false>
 struct PersistentShape {
-  static constexpr int kWarps = 8;
+  static constexpr int kWarps = F8 ? 12 : 8;
   static constexpr int kBlocksPerStage = F8 ? 2 : 1;
   static constexpr int kStageBytes = kBlocksPerStage * KvTile<D, F8>::kStageBytes;
-  static constexpr int kStages = 24576 / kStageBytes;  // per warp
+  static constexpr int kStages = (F8 ? 16384 : 24576) / kStageBytes;  // per warp
   static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
 };
+constexpr int kMaxPersistentWarps = 12;  // sizes the workspace
 
 // Dynamic shared memory: [ring][appended-token rows (fp16/bf16, K and V)]
 // [prefix P[B+1]][context ctx[B]] (+1 KB alignment slack).
