@@ -245,14 +245,26 @@ int launch_persistent(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::D
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, kern, mk, mv, args);
   if (e != cudaSuccess) return cuda_fail(e, "decode_persistent_kernel launch");
-  constexpr auto merge = pkv::merge_persistent_kernel<T, D>;
-  e = configure_smem<merge>(static_cast<int>((2 * static_cast<size_t>(max_persistent_seqs(d, false)) + 1) * 4));
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_persistent_kernel)");
+  // Long units cut into many pieces (on average 6 or more warp shares per
+  // unit): a CTA per row, its warps splitting the row's pieces; otherwise a
+  // warp per row.
+  const int32_t nwarps = static_cast<int32_t>(grid) * PS::kWarps;
+  const bool coop = nwarps >= 6 * static_cast<int64_t>(d->num_seqs) * d->num_kv_heads;
+  const int merge_smem = static_cast<int>((2 * static_cast<size_t>(max_persistent_seqs(d, false)) + 1) * 4);
   const int rows = d->num_seqs * d->num_q_heads;
-  cfg.gridDim = dim3(static_cast<unsigned>((rows + pkv::kMergeWarps - 1) / pkv::kMergeWarps));
+  const int rows_per_cta = coop ? 1 : pkv::kMergeWarps;
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + rows_per_cta - 1) / rows_per_cta));
   cfg.blockDim = dim3(pkv::kMergeWarps * 32);
   cfg.dynamicSmemBytes = (2 * static_cast<size_t>(d->num_seqs) + 1) * 4;
-  e = cudaLaunchKernelEx(&cfg, merge, args, static_cast<int32_t>(grid) * PS::kWarps);
+  if (coop) {
+    constexpr auto merge = pkv::merge_persistent_kernel<T, D, true>;
+    e = configure_smem<merge>(merge_smem);
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, merge, args, nwarps);
+  } else {
+    constexpr auto merge = pkv::merge_persistent_kernel<T, D, false>;
+    e = configure_smem<merge>(merge_smem);
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, merge, args, nwarps);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "merge_persistent_kernel launch");
   return PKV_OK;
 }

@@ -1026,21 +1026,24 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
   }
 }
 
-// Merge of the pieces the persistent kernel left: one warp per (sequence,
-// query head) row (warps stride over rows if the grid is smaller).  Units
-// wholly inside one segment were written by the decode kernel; an empty
-// context gives a zero row.  Everything that depends only on the inputs (the block prefix of the
-// contexts) is computed before griddepcontrol.wait, while the decode grid is
-// still running; after it, only the partials are read.  The unit's blocks
-// [U, U+nb) overlap shares w0..w1 of 5 segments each; lanes test those
-// candidates in parallel, the overlapping ones are compacted into a list, and
-// their rows are accumulated with independent loads.
-// Small CTAs (4 warps at <= 64 registers, 8 K registers): one fits beside a
-// decode CTA, and the grid covers every row at once.
+// Merge of the pieces the persistent kernel left.  A CTA of kMergeWarps warps
+// takes kMergeWarps (sequence, query head) rows at a time, one warp per row;
+// or, COOP, one row at a time, its warps splitting the row's pieces between
+// them and combining their partial results through shared memory (for long
+// units cut into many pieces, which one warp would fold in a long serial
+// chain).
+// Units wholly inside one segment were written by the decode kernel; an empty
+// context gives a zero row.  Everything that depends only on the inputs (the
+// block prefix of the contexts) is computed before griddepcontrol.wait, while
+// the decode grid is still running; after it, only the partials are read.  The
+// unit's blocks [U, U+nb) overlap shares w0..w1 of 5 segments each; lanes test
+// those candidates in parallel, the overlapping ones are compacted into a
+// list, and their rows are accumulated with independent loads.  Small CTAs
+// (4 warps at <= 64 registers, 80 for COOP): they fit beside a decode CTA.
 constexpr int kMergeWarps = 4;
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kMergeWarps * 32, 8)
+template <typename T, int D, bool COOP>
+__global__ void __launch_bounds__(kMergeWarps * 32, COOP ? 6 : 8)
     merge_persistent_kernel(const DecodeArgs a, int32_t nwarps) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int kPer = D / 32;
@@ -1049,101 +1052,151 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 8)
   __shared__ int s_warp_sum[kMergeWarps];
   __shared__ int64_t s_row[kMergeWarps][32];
   __shared__ float s_w[kMergeWarps][32];
+  __shared__ float s_ml[COOP ? kMergeWarps : 1][2];
+  __shared__ __align__(16) float s_o[COOP ? kMergeWarps : 1][COOP ? D : 4];
   int* s_P = merge_smem;
   int* s_ctx = s_P + a.num_seqs + 1;
   context_prefix(a, s_P, s_ctx, s_warp_sum, kMergeWarps * 32, false);
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int rows_per_cta = COOP ? 1 : kMergeWarps;
+  constexpr int wpr = kMergeWarps / rows_per_cta;  // warps per row
+  const int sub = warp % wpr;                      // this warp's part of its row
   const int Hkv = a.num_kv_heads;
   const Partition part(Hkv * s_P[a.num_seqs], nwarps);
   const int rows = a.num_seqs * a.num_q_heads;
-  for (int row = blockIdx.x * kMergeWarps + warp; row < rows; row += gridDim.x * kMergeWarps) {
-    const int b = row / a.num_q_heads, hq = row - b * a.num_q_heads;
-    const int kvh = hq / a.group, h = hq - kvh * a.group;
-    const int nb = (s_ctx[b] + kBlockSize - 1) / kBlockSize;
-    T* dst = static_cast<T*>(a.out) + static_cast<int64_t>(row) * D + lane * kPer;
-    if (nb == 0) {
-#pragma unroll
-      for (int k = 0; k < kPer; k += 2) *reinterpret_cast<uint32_t*>(dst + k) = 0u;
-      continue;
+  // Every warp of the CTA runs the same number of iterations (barriers inside).
+  for (int base_row = blockIdx.x * rows_per_cta; base_row < rows; base_row += gridDim.x * rows_per_cta) {
+    const int row = base_row + warp / wpr;
+    bool work = row < rows;
+    int b = 0, kvh = 0, h = 0, nb = 0, U = 0, Uend = 0;
+    if (work) {
+      b = row / a.num_q_heads;
+      const int hq = row - b * a.num_q_heads;
+      kvh = hq / a.group;
+      h = hq - kvh * a.group;
+      nb = (s_ctx[b] + kBlockSize - 1) / kBlockSize;
     }
-    const int U = Hkv * s_P[b] + kvh * nb, Uend = U + nb;
-    {
+    T* dst = static_cast<T*>(a.out) + static_cast<int64_t>(row) * D + lane * kPer;
+    if (work && nb == 0) {
+      if (sub == 0) {
+#pragma unroll
+        for (int k = 0; k < kPer; k += 2) *reinterpret_cast<uint32_t*>(dst + k) = 0u;
+      }
+      work = false;
+    }
+    if (work) {
+      U = Hkv * s_P[b] + kvh * nb;
+      Uend = U + nb;
       int s, e;
       part.segment_of(U, s, e);
-      if (e >= Uend) continue;  // one segment: the decode kernel wrote it
+      if (e >= Uend) work = false;  // one segment: the decode kernel wrote it
     }
-    const int w0 = U / part.R, ncand = ((Uend - 1) / part.R - w0 + 1) * kSegPerShare;
-    auto piece = [&](int c) -> int64_t {
-      const int w = w0 + c / kSegPerShare, k = c % kSegPerShare;
-      int s, e, sid;
-      if (k == 0) {
-        part.head(w, s, e);
-        sid = w;
-      } else {
-        part.chunk(k - 1, w, s, e);
-        sid = part.nwarps + (k - 1) * part.nwarps + w;
-      }
-      if (e <= s || e <= U || s >= Uend) return -1;
-      return (static_cast<int64_t>(sid) * 2 + (U > s ? 1 : 0)) * kMaxGroup + h;
-    };
-
-    // Pieces are folded in with a running log-sum-exp, in batches of up to 32
-    // candidates; within a batch the log-sum-exps and the partial rows are
-    // loaded together (one round trip), at most kBatch rows in flight.
-    constexpr int kBatch = 8;
     float m = -INFINITY, L = 0.f, o[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) o[k] = 0.f;
-    for (int base = 0; base < ncand; base += 32) {
-      const int64_t pr = base + lane < ncand ? piece(base + lane) : -1;
-      const unsigned valid = __ballot_sync(0xffffffffu, pr >= 0);
-      const int rank = __popc(valid & ((1u << lane) - 1));
-      if (pr >= 0) s_row[warp][rank] = pr;
-      const float lse = pr >= 0 ? __ldcg(a.part_lse + pr) : -INFINITY;
-      __syncwarp();
-      const int cnt = __popc(valid);
-      for (int i0 = 0; i0 < cnt; i0 += kBatch) {
-        float v[kBatch][kPer];
+    if (work) {
+      const int w0 = U / part.R, ncand = ((Uend - 1) / part.R - w0 + 1) * kSegPerShare;
+      auto piece = [&](int c) -> int64_t {
+        const int w = w0 + c / kSegPerShare, k = c % kSegPerShare;
+        int s, e, sid;
+        if (k == 0) {
+          part.head(w, s, e);
+          sid = w;
+        } else {
+          part.chunk(k - 1, w, s, e);
+          sid = part.nwarps + (k - 1) * part.nwarps + w;
+        }
+        if (e <= s || e <= U || s >= Uend) return -1;
+        return (static_cast<int64_t>(sid) * 2 + (U > s ? 1 : 0)) * kMaxGroup + h;
+      };
+
+      // Pieces are folded in with a running log-sum-exp, in batches of up to
+      // 32 candidates (this warp's share of them); within a batch the
+      // log-sum-exps and the partial rows are loaded together (one round
+      // trip), at most kBatch rows in flight.
+      constexpr int kBatch = 8;
+      for (int base = 32 * sub; base < ncand; base += 32 * wpr) {
+        const int64_t pr = base + lane < ncand ? piece(base + lane) : -1;
+        const unsigned valid = __ballot_sync(0xffffffffu, pr >= 0);
+        const int rank = __popc(valid & ((1u << lane) - 1));
+        if (pr >= 0) s_row[warp][rank] = pr;
+        const float lse = pr >= 0 ? __ldcg(a.part_lse + pr) : -INFINITY;
+        __syncwarp();
+        const int cnt = __popc(valid);
+        for (int i0 = 0; i0 < cnt; i0 += kBatch) {
+          float v[kBatch][kPer];
 #pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-          if (i0 + i < cnt) {
-            const float* src = a.part_o + s_row[warp][i0 + i] * D + lane * kPer;
+          for (int i = 0; i < kBatch; ++i) {
+            if (i0 + i < cnt) {
+              const float* src = a.part_o + s_row[warp][i0 + i] * D + lane * kPer;
 #pragma unroll
-            for (int k = 0; k < kPer; k += 2) {
-              const float2 x = __ldcg(reinterpret_cast<const float2*>(src + k));
-              v[i][k] = x.x;
-              v[i][k + 1] = x.y;
+              for (int k = 0; k < kPer; k += 2) {
+                const float2 x = __ldcg(reinterpret_cast<const float2*>(src + k));
+                v[i][k] = x.x;
+                v[i][k + 1] = x.y;
+              }
             }
           }
-        }
-        if (i0 == 0 && pr >= 0) s_w[warp][rank] = lse;  // the batch's log-sum-exps, by rank
-        __syncwarp();
-        float mb = m;
+          if (i0 == 0 && pr >= 0) s_w[warp][rank] = lse;  // the batch's log-sum-exps, by rank
+          __syncwarp();
+          float mb = m;
 #pragma unroll
-        for (int i = 0; i < kBatch; ++i)
-          if (i0 + i < cnt) mb = fmaxf(mb, s_w[warp][i0 + i]);
-        const float sc = exp2f(m - mb);
-        L *= sc;
+          for (int i = 0; i < kBatch; ++i)
+            if (i0 + i < cnt) mb = fmaxf(mb, s_w[warp][i0 + i]);
+          const float sc = exp2f(m - mb);  // m == mb == -inf cannot happen: a batch has a piece
+          L *= sc;
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) o[k] *= sc;
+          for (int k = 0; k < kPer; ++k) o[k] *= sc;
 #pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-          if (i0 + i < cnt) {
-            const float w = exp2f(s_w[warp][i0 + i] - mb);
-            L += w;
+          for (int i = 0; i < kBatch; ++i) {
+            if (i0 + i < cnt) {
+              const float w = exp2f(s_w[warp][i0 + i] - mb);
+              L += w;
 #pragma unroll
-            for (int k = 0; k < kPer; ++k) o[k] += w * v[i][k];
+              for (int k = 0; k < kPer; ++k) o[k] += w * v[i][k];
+            }
           }
+          m = mb;
         }
-        m = mb;
+        __syncwarp();
       }
-      __syncwarp();
     }
-    const float inv = 1.0f / L;
+    if constexpr (COOP) {
+      // Combine the row's warps: (m, L, o) of each through shared memory.
+      if (lane == 0) {
+        s_ml[warp][0] = m;
+        s_ml[warp][1] = L;
+      }
 #pragma unroll
-    for (int k = 0; k < kPer; k += 2) *reinterpret_cast<uint32_t*>(dst + k) = pack2<T>(o[k] * inv, o[k + 1] * inv);
+      for (int k = 0; k < kPer; ++k) s_o[warp][lane * kPer + k] = o[k];
+      __syncthreads();
+      if (work && sub == 0) {
+        float mt = m;
+        for (int w = 1; w < wpr; ++w) mt = fmaxf(mt, s_ml[warp + w][0]);
+        float Lt = 0.f, ot[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) ot[k] = 0.f;
+        for (int w = 0; w < wpr; ++w) {
+          const float mw = s_ml[warp + w][0];
+          if (mw == -INFINITY) continue;  // that warp had no pieces
+          const float sc = exp2f(mw - mt);
+          Lt += sc * s_ml[warp + w][1];
+#pragma unroll
+          for (int k = 0; k < kPer; ++k) ot[k] += sc * s_o[warp + w][lane * kPer + k];
+        }
+        const float inv = 1.0f / Lt;
+#pragma unroll
+        for (int k = 0; k < kPer; k += 2)
+          *reinterpret_cast<uint32_t*>(dst + k) = pack2<T>(ot[k] * inv, ot[k + 1] * inv);
+      }
+      __syncthreads();
+    } else if (work) {
+      const float inv = 1.0f / L;
+#pragma unroll
+      for (int k = 0; k < kPer; k += 2) *reinterpret_cast<uint32_t*>(dst + k) = pack2<T>(o[k] * inv, o[k + 1] * inv);
+    }
   }
 }
 
