@@ -46,7 +46,8 @@ import numpy as np
 
 __all__ = [
     "widen", "e4m3_decode", "e4m3_encode", "quantize_e4m3", "dequantize_e4m3", "kv_append_fp8", "kv_head_of", "slot_of_position", "slot_mapping", "kv_append",
-    "gather_kv", "attend_one", "decode_attention", "decode_attention_rows",
+    "gather_kv", "attend_one", "decode_attention", "decode_attention_rows", "decode_attention_multi",
+    "slot_mapping_multi",
     "split_partials", "lse_merge", "kv_bytes_per_token", "blocks_needed",
     "allocated_bytes", "wasted_bytes", "kv_cache_bytes", "decode_step_tokens_per_s",
     "attention_call_bytes",
@@ -248,6 +249,58 @@ def decode_attention(q_bits, k_cache_bits, v_cache_bits, block_tables, context_l
     rows = [(b, h) for b in range(B) for h in range(Hq)]
     return decode_attention_rows(q_bits, k_cache_bits, v_cache_bits, block_tables, context_lens,
                                  scale, dtype, block_size, rows).reshape(B, Hq, D)
+
+
+# ---------------------------------------------------------------- several new tokens per sequence
+
+def decode_attention_multi(q_bits, k_cache_bits, v_cache_bits, block_tables, context_lens, q_len: int,
+                           scale: float, dtype: str, block_size: int, kv_scales=None,
+                           rows: Optional[Iterable[Tuple[int, int, int]]] = None) -> np.ndarray:
+    """Decode attention for q_len new tokens per sequence (speculative
+    verification, chunked decode: youngju.dev "LLM サービング最適化完全ガイド",
+    speculative decoding section -- the target model checks several draft
+    tokens in one pass -- and design.babushkai.com "GPU推論の内部構造", section
+    "KVキャッシュの台帳", chunked prefill).
+
+    q_bits: [B][q_len][Hq][D].  context_lens[b] = L counts the q_len new tokens,
+    which sit at positions L - q_len .. L - 1; new token i attends to positions
+    [0, L - q_len + i] (causal among the new tokens).  A token whose position
+    is negative (L < q_len) attends to nothing and gets a zero row.
+
+    Returns float64 [B][q_len][Hq][D], or, for ``rows`` = [(b, i, h), ...],
+    float64 [len(rows)][D]."""
+    q_bits = np.asarray(q_bits)
+    B, n, Hq, D = q_bits.shape
+    Hkv = k_cache_bits.shape[1]
+    g = Hq // Hkv
+    want = rows if rows is not None else [(b, i, h) for b in range(B) for i in range(n) for h in range(Hq)]
+    out = np.zeros((len(want), D))
+    for r, (b, i, h) in enumerate(want):
+        pos = int(context_lens[b]) - n + i
+        if pos < 0:
+            continue
+        kv = kv_head_of(h, g)
+        Kc = gather_kv(k_cache_bits, block_tables[b], pos + 1, kv, block_size)
+        Vc = gather_kv(v_cache_bits, block_tables[b], pos + 1, kv, block_size)
+        if kv_scales is None:
+            K, V = widen(Kc, dtype), widen(Vc, dtype)
+        else:
+            K, V = dequantize_e4m3(Kc, kv_scales[0][kv]), dequantize_e4m3(Vc, kv_scales[1][kv])
+        out[r] = attend_one(widen(q_bits[b, i, h], dtype), K, V, scale)[0]
+    return out if rows is not None else out.reshape(B, n, Hq, D)
+
+
+def slot_mapping_multi(block_tables, context_lens, q_len: int, block_size: int) -> np.ndarray:
+    """Slots of each sequence's q_len newest tokens (positions L - q_len .. L - 1),
+    int32 [B][q_len]; -1 for a position below 0."""
+    B = len(context_lens)
+    out = np.full((B, q_len), -1, dtype=np.int32)
+    for b in range(B):
+        for i in range(q_len):
+            pos = int(context_lens[b]) - q_len + i
+            if pos >= 0:
+                out[b, i] = slot_of_position(block_tables[b], pos, block_size)
+    return out
 
 
 # ---------------------------------------------------------------- split + merge

@@ -496,3 +496,91 @@ def test_planted_fp8_mistake_is_caught(monkeypatch, name):
     attr, bad = FP8_MUTATIONS[name]
     monkeypatch.setattr(oracle, attr, bad)
     assert not _fp8_pins_pass()
+
+
+# ------------------------------------------------------------------ several new tokens per sequence
+
+def _causal_bruteforce(q_bits, K_bits, V_bits, lens, q_len, scale, dtype):
+    """Contiguous causal attention with Python loops: new token i of sequence
+    b (position L - q_len + i) against keys 0 .. L - q_len + i."""
+    B, n, Hq, D = q_bits.shape
+    g = Hq // K_bits.shape[1]
+    q, K, V = (oracle.widen(x, dtype) for x in (q_bits, K_bits, V_bits))
+    out = np.zeros((B, n, Hq, D))
+    for b in range(B):
+        for i in range(n):
+            pos = lens[b] - n + i
+            if pos < 0:
+                continue
+            for h in range(Hq):
+                s = [scale * math.fsum(q[b, i, h, d] * K[b, h // g, t, d] for d in range(D)) for t in range(pos + 1)]
+                e = [math.exp(x) for x in s]
+                z = math.fsum(e)
+                for d in range(D):
+                    out[b, i, h, d] = math.fsum(e[t] * V[b, h // g, t, d] for t in range(pos + 1)) / z
+    return out
+
+
+def _multi_case(seed, lens, n, Hq=4, Hkv=2, D=8, bs=4):
+    q1, K, V, kc, vc, tables = paged_case(seed, lens=lens, Hq=Hq, Hkv=Hkv, D=D, bs=bs)
+    g = torch.Generator().manual_seed(seed + 100)
+    q = bits_of(torch.randn(len(lens), n, Hq, D, generator=g).to(torch.float16))
+    return q, K, V, kc, vc, tables
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5])
+def test_multi_query_equals_causal_bruteforce(n):
+    lens = (7, 2, 13, 0)
+    q, K, V, kc, vc, tables = _multi_case(4, lens, n)
+    ours = oracle.decode_attention_multi(q, kc, vc, tables, np.array(lens), n, 0.4, "fp16", 4)
+    ref = _causal_bruteforce(q, K, V, lens, n, 0.4, "fp16")
+    assert np.abs(ours - ref).max() < 1e-13
+    # a sequence shorter than q_len: its first tokens have no keys and give zero rows
+    assert np.all(ours[1, :max(0, n - 2)] == 0)
+
+
+def test_multi_query_rows_are_single_token_decodes_of_the_prefix():
+    """New token i is exactly a one-token decode with context L - q_len + i + 1."""
+    lens, n = (9, 16, 17), 4
+    q, K, V, kc, vc, tables = _multi_case(6, lens, n)
+    ours = oracle.decode_attention_multi(q, kc, vc, tables, np.array(lens), n, 0.3, "fp16", 4)
+    for i in range(n):
+        ctx = np.array([L - n + i + 1 for L in lens])
+        one = oracle.decode_attention(q[:, i], kc, vc, tables, ctx, 0.3, "fp16", 4)
+        assert np.array_equal(ours[:, i], one)
+    # q_len = 1 is the one-token decode itself
+    q1 = q[:, :1]
+    assert np.array_equal(oracle.decode_attention_multi(q1, kc, vc, tables, np.array(lens), 1, 0.3, "fp16", 4)[:, 0],
+                          oracle.decode_attention(q1[:, 0], kc, vc, tables, np.array(lens), 0.3, "fp16", 4))
+
+
+def test_slot_mapping_multi_on_page_block_tables(golden_dir):
+    gold = json.load(open(os.path.join(golden_dir, "block_tables.json")))
+    bs = gold["block_size"]
+    A = gold["kasblo"]
+    table = np.array([A["tables"]["A"]], np.int32)
+    printed = dict(zip(A["positions"]["A"], A["slots"]["A"]))
+    # L = 33 with 3 new tokens: positions 30, 31, 32 (31 and 32 printed on the page: 31, 144)
+    slots = oracle.slot_mapping_multi(table, np.array([33]), 3, bs)[0]
+    assert slots[1] == printed[31] and slots[2] == printed[32] and slots[0] == printed[31] - 1
+    # L = 17 with 2 new tokens: positions 15, 16 -> 127, 16
+    assert list(oracle.slot_mapping_multi(table, np.array([17]), 2, bs)[0]) == [printed[15], printed[16]]
+    # fewer tokens than new tokens: the missing positions are -1
+    assert list(oracle.slot_mapping_multi(table, np.array([1]), 3, bs)[0]) == [-1, -1, printed[0]]
+
+
+def _bad_multi(q_bits, kc, vc, tables, lens, n, scale, dtype, bs, kv_scales=None, rows=None,
+               f=oracle.decode_attention_multi):
+    """Off by one in the causal limit: token i also sees token i + 1."""
+    return f(q_bits, kc, vc, tables, np.asarray(lens) + 1, n, scale, dtype, bs, kv_scales, rows)
+
+
+def test_planted_causal_off_by_one_is_caught(monkeypatch):
+    lens, n = (7, 13), 3
+    q, K, V, kc, vc, tables = _multi_case(2, lens, n)
+    ref = _causal_bruteforce(q, K, V, lens, n, 0.4, "fp16")
+    good = oracle.decode_attention_multi(q, kc, vc, tables, np.array(lens), n, 0.4, "fp16", 4)
+    assert np.abs(good - ref).max() < 1e-13
+    monkeypatch.setattr(oracle, "decode_attention_multi", _bad_multi)
+    bad = oracle.decode_attention_multi(q, kc, vc, tables, np.array(lens), n, 0.4, "fp16", 4)
+    assert not np.abs(bad - ref).max() < 1e-13
