@@ -480,6 +480,150 @@ def run_ours(args, rank, world, local):
         print(json.dumps(result), flush=True)
 
 
+# ----------------------------------------------------------------------------- several new tokens per sequence
+
+def run_multi(args, rank, world, local):
+    """One step = the q_len-token append + multi-token paged decode attention
+    (+ split merge) for the whole batch.  Bytes: the one-token formula with q
+    and out q_len times larger; the append moves q_len rows per sequence."""
+    import oracle
+    import paged_kv_cache_26_gb300 as pkv
+    from paged_kv_cache_26_gb300 import build as pkv_build
+    from paged_kv_cache_26_gb300._native import PkvDims, lib
+
+    pkv_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    n = args.q_len
+    spec = wl.CONFIGS[args.config]
+    if args.batch:
+        spec = spec.replace(name=f"{spec.name}_b{args.batch}", batch=args.batch)
+    w, m = wl.generate_multi(spec, n, seed=args.seed + rank, device=dev, layers=1)
+    s = w.spec
+    L = lib()
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    out = torch.empty_like(m.q[0])
+    dims = PkvDims(num_seqs=s.batch, num_q_heads=s.num_q_heads, num_kv_heads=s.num_kv_heads, head_dim=s.head_dim,
+                   block_size=s.block_size, num_blocks=w.num_blocks, max_blocks_per_seq=w.max_blocks,
+                   dtype=0 if s.dtype == "fp16" else 1)
+    splits = int(L.paged_decode_multi_resolve_splits(ctypes.byref(dims), n, args.splits))
+    ws_bytes = int(L.paged_decode_multi_workspace_bytes(ctypes.byref(dims), n, args.splits))
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    P = ctypes.c_void_p
+    step_args = (P(m.q[0].data_ptr()), P(m.k_new[0].data_ptr()), P(m.v_new[0].data_ptr()),
+                 P(w.k_cache[0].data_ptr()), P(w.v_cache[0].data_ptr()), P(bt.data_ptr()), P(cl.data_ptr()), n,
+                 ctypes.c_float(w.scale), P(out.data_ptr()), args.splits, P(ws.data_ptr()), ws_bytes,
+                 ctypes.byref(dims), sp)
+    f_step = L.paged_decode_step_multi
+
+    def step():
+        if f_step(*step_args):
+            raise RuntimeError(L.paged_kv_last_error().decode())
+
+    K, W = args.steps, args.warmup
+    sampler = ClockSampler(local) if rank == 0 else None
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    pkv.paged_kv_check_status(stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(stream)
+    for _ in range(K):
+        f_step(*step_args)
+    end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop(t_wall0, time.time()) if sampler else None
+    barrier(world)
+    pkv.paged_kv_check_status(stream)
+    ms_per_step = max_over_ranks(start.elapsed_time(end), world, dev) / K
+
+    elem = 2
+    kv_b = attention_bytes(w.context_lens, s.batch, s.num_q_heads, s.num_kv_heads, s.head_dim, elem)
+    kv_b += 2 * s.batch * (n - 1) * s.num_q_heads * s.head_dim * elem          # q and out of the extra tokens
+    app_b = append_bytes(s.batch * n, s.num_kv_heads, s.head_dim, elem)
+    step_bytes = kv_b + app_b
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = load_peaks()
+
+    # ---- end to end: pinned host inputs copied in, the output copied back, on the stream
+    h = {"q": m.q[0].cpu(), "k_new": m.k_new[0].cpu(), "v_new": m.v_new[0].cpu(),
+         "block_tables": torch.from_numpy(w.block_tables), "context_lens": torch.from_numpy(w.context_lens),
+         "out": torch.empty_like(out, device="cpu")}
+    h = {k: v.contiguous().pin_memory() for k, v in h.items()}
+    d = {"q": m.q[0], "k_new": m.k_new[0], "v_new": m.v_new[0], "block_tables": bt, "context_lens": cl}
+
+    def e2e_once():
+        for k, t in d.items():
+            t.copy_(h[k], non_blocking=True)
+        step()
+        h["out"].copy_(out, non_blocking=True)
+
+    for _ in range(min(W, 10)):
+        e2e_once()
+    torch.cuda.synchronize()
+    barrier(world)
+    start.record(stream)
+    for _ in range(K):
+        e2e_once()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(start.elapsed_time(end), world, dev) / K
+    h2d = sum(h[k].numel() * h[k].element_size() for k in d)
+    d2h = h["out"].numel() * h["out"].element_size()
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": s.dtype, "data": "synthetic (seeded N(0,1) values, scattered block placement)",
+        "config": {"workload": f"{s.name}_q{n}", "batch": s.batch, "q_len": n, "num_q_heads": s.num_q_heads,
+                   "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size,
+                   "context_tokens": int(w.context_lens.sum()), "num_blocks": w.num_blocks,
+                   "partition": f"{splits} splits per sequence",
+                   "l2": f"no flush: each call streams {kv_b / 2**20:.0f} MiB, {kv_b / L2_BYTES:.1f}x the 129 MiB L2",
+                   "step": "paged_decode_step_multi: q_len-token KV append + causal multi-token paged attention"
+                           + (" + merge" if splits > 1 else "")},
+        "steps_per_s": round(1e3 / ms_per_step, 2),
+        "query_tokens_per_s": round(world * s.batch * n * 1e3 / ms_per_step, 1),
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_step_multi: append_multi_kernel + "
+                     "decode_multi_query_kernel" + (" + merge_split_kernel" if splits > 1 else ""),
+                     "achieved": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / peak, 4), "traffic": None,
+                     "bytes_per_launch": step_bytes, "avg_launch_us": round(ms_per_step * 1e3, 2)},
+        "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": K * (3 if splits > 1 else 2),
+        "clocks": clocks,
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        # the oracle over the batch's sequences in order (all tokens and heads) for about cpu_budget seconds
+        qb = m.q[0].cpu().view(torch.int16).numpy().view(np.uint16)
+        spent, done, nseq = 0.0, 0.0, 0
+        while spent < args.cpu_budget:
+            b = nseq % s.batch
+            sample = host_sample(w, [b])
+            rows = [(0, i, hh) for i in range(n) for hh in range(s.num_q_heads)]
+            t0 = time.perf_counter()
+            oracle.decode_attention_multi(qb[[b]], sample[1], sample[2], sample[3], sample[4], n, w.scale, s.dtype,
+                                          s.block_size, rows=rows)
+            spent += time.perf_counter() - t0
+            done += row_bytes(w, [w.context_lens[b]] * s.num_q_heads) + 2 * (n - 1) * s.num_q_heads * s.head_dim * 2
+            nseq += 1
+        result["cpu_baseline"] = {"value": done / spent / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                  "sample": f"{nseq} sequences in order, all {n} tokens x {s.num_q_heads} heads; "
+                                            f"{spent:.1f} s of numpy fp64 on one host thread (the cache as left "
+                                            f"by the timed steps)"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
 # ----------------------------------------------------------------------------- continuous batching
 
 def run_loop(args, rank, world, local):
@@ -620,6 +764,7 @@ def main():
     ap.add_argument("--kv", choices=["native", "fp8"], default="native",
                     help="pool format: the configuration's fp16/bf16, or E4M3 codes with per-head scales")
     ap.add_argument("--loop", action="store_true", help="continuous-batching loop instead of the fixed batch")
+    ap.add_argument("--q-len", type=int, default=1, help="new tokens per sequence (>1: multi-token decode)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -628,6 +773,8 @@ def main():
         run_reference(args, rank, world)
     elif args.loop:
         run_loop(args, rank, world, local)
+    elif args.q_len > 1:
+        run_multi(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:

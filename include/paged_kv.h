@@ -258,6 +258,52 @@ int paged_decode_step_fp8(const void* q, const void* k_new, const void* v_new, v
                           void* out, void* workspace, size_t workspace_bytes,
                           const pkv_dims* dims, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Several new tokens per sequence (speculative verification, chunked decode):
+ * youngju.dev "LLM サービング最適化完全ガイド", speculative decoding section (the
+ * target model checks several draft tokens in one pass) and
+ * design.babushkai.com "GPU推論の内部構造", section "KVキャッシュの台帳" (chunked
+ * prefill).  The pages give no kernel; the masking is the causal rule of
+ * decoding itself.
+ *
+ * q, out       : T[num_seqs][q_len][num_q_heads][head_dim], 1 <= q_len <= 8
+ * k_new, v_new : T[num_seqs][q_len][num_kv_heads][head_dim] (step only)
+ * context_lens[b] = L counts the q_len new tokens, which sit at positions
+ * L - q_len .. L - 1; new token i attends to positions [0, L - q_len + i]
+ * (the cache before it and the new tokens up to itself).  A token whose
+ * position would be negative (L < q_len) gets a zero row.  num_splits: 0 =
+ * automatic (512-token splits, more when the batch alone would not fill the
+ * GPU), n >= 1 = n splits.  Workspace: paged_decode_multi_workspace_bytes
+ * bytes (0 for one split), 256-byte aligned; its contents need no
+ * initialisation.  Errors as paged_decode_attention; q_len outside 1..8 gives
+ * PKV_ERR_UNSUPPORTED.
+ * ---------------------------------------------------------------------- */
+int paged_decode_attention_multi(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_tables, const int32_t* context_lens,
+                                 int32_t q_len, float scale, void* out, int32_t num_splits,
+                                 void* workspace, size_t workspace_bytes, const pkv_dims* dims,
+                                 void* stream);
+
+/* Append the q_len new tokens' K/V of every sequence (at positions
+ * L - q_len .. L - 1 through its table; nothing for negative positions), then
+ * paged_decode_attention_multi (device). */
+int paged_decode_step_multi(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                            void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+                            int32_t q_len, float scale, void* out, int32_t num_splits, void* workspace,
+                            size_t workspace_bytes, const pkv_dims* dims, void* stream);
+
+/* Workspace bytes, and the number of splits, a multi-token call with these
+ * arguments uses (0 bytes / a negative error code for invalid arguments). */
+size_t paged_decode_multi_workspace_bytes(const pkv_dims* dims, int32_t q_len, int32_t num_splits);
+int32_t paged_decode_multi_resolve_splits(const pkv_dims* dims, int32_t q_len, int32_t num_splits);
+
+/* Host helper: slots of each sequence's q_len newest tokens, slot_mapping[b][i]
+ * for position L - q_len + i (-1 when negative).  Host pointers;
+ * slot_mapping holds num_seqs * q_len entries. */
+int paged_kv_slot_mapping_multi(const int32_t* block_tables, const int32_t* context_lens,
+                                int32_t num_seqs, int32_t max_blocks, int32_t block_size,
+                                int32_t q_len, int32_t* slot_mapping);
+
 /* Synchronises `stream`, then reads and clears this device's error word.
  * Returns PKV_OK, PKV_ERR_OUT_OF_RANGE, PKV_ERR_TIMEOUT or PKV_ERR_CUDA. */
 int paged_kv_check_status(void* stream);

@@ -205,6 +205,99 @@ def paged_decode_step_from_host(host: dict, dev: dict, k_cache: torch.Tensor, v_
            "paged_decode_step_from_host")
 
 
+# ---------------------------------------------------------------- several new tokens per sequence
+
+def _multi_checks(q, k_cache, v_cache, block_tables, context_lens, out):
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need_cuda(n, t, k_cache.dtype)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    _need_cuda("out", out, q.dtype)
+    if q.dim() != 4 or out.shape != q.shape or q.shape[3] != k_cache.shape[3] or k_cache.shape != v_cache.shape:
+        raise ValueError("q / out must be [num_seqs][q_len][num_q_heads][head_dim] matching the caches")
+    if block_tables.dim() != 2 or block_tables.shape[0] != q.shape[0] or context_lens.shape != (q.shape[0],):
+        raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
+
+
+def _multi_dims(q, k_cache, block_tables):
+    return make_dims(q, k_cache, block_tables, num_q_heads=q.shape[2])
+
+
+def paged_decode_multi_workspace_bytes(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
+                                       num_splits: int = 0) -> int:
+    dims = _multi_dims(q, k_cache, block_tables)
+    return int(lib().paged_decode_multi_workspace_bytes(ctypes.byref(dims), q.shape[1], num_splits))
+
+
+def paged_decode_multi_resolve_splits(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
+                                      num_splits: int = 0) -> int:
+    dims = _multi_dims(q, k_cache, block_tables)
+    return _check(lib().paged_decode_multi_resolve_splits(ctypes.byref(dims), q.shape[1], num_splits),
+                  "paged_decode_multi_resolve_splits")
+
+
+def _multi_workspace(q, k_cache, block_tables, num_splits, workspace):
+    need = paged_decode_multi_workspace_bytes(q, k_cache, block_tables, num_splits)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    return workspace, (workspace.numel() * workspace.element_size() if workspace is not None else 0)
+
+
+def paged_decode_attention_multi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                 block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                                 out: Optional[torch.Tensor] = None, num_splits: int = 0,
+                                 workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode attention for q.shape[1] new tokens per sequence (q:
+    [B][q_len][Hq][D]): new token i of sequence b, at position
+    context_lens[b] - q_len + i, attends to positions 0 .. itself."""
+    if out is None:
+        out = torch.empty_like(q)
+    _multi_checks(q, k_cache, v_cache, block_tables, context_lens, out)
+    dims = _multi_dims(q, k_cache, block_tables)
+    workspace, ws_bytes = _multi_workspace(q, k_cache, block_tables, num_splits, workspace)
+    _check(lib().paged_decode_attention_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                              _ptr(context_lens), q.shape[1], float(scale), _ptr(out), num_splits,
+                                              _ptr(workspace), ws_bytes, ctypes.byref(dims), _stream(stream)),
+           "paged_decode_attention_multi")
+    return out
+
+
+def paged_decode_step_multi(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                            v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                            scale: float, out: Optional[torch.Tensor] = None, num_splits: int = 0,
+                            workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Append the q_len new tokens' K/V (k_new, v_new: [B][q_len][Hkv][D]) at
+    positions context_lens[b] - q_len .. context_lens[b] - 1, then
+    paged_decode_attention_multi."""
+    if out is None:
+        out = torch.empty_like(q)
+    _multi_checks(q, k_cache, v_cache, block_tables, context_lens, out)
+    for n, t in (("k_new", k_new), ("v_new", v_new)):
+        _need_cuda(n, t, k_cache.dtype)
+    if k_new.shape != (q.shape[0], q.shape[1], k_cache.shape[1], k_cache.shape[3]) or v_new.shape != k_new.shape:
+        raise ValueError("k_new / v_new must be [num_seqs][q_len][num_kv_heads][head_dim]")
+    dims = _multi_dims(q, k_cache, block_tables)
+    workspace, ws_bytes = _multi_workspace(q, k_cache, block_tables, num_splits, workspace)
+    _check(lib().paged_decode_step_multi(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                         _ptr(block_tables), _ptr(context_lens), q.shape[1], float(scale), _ptr(out),
+                                         num_splits, _ptr(workspace), ws_bytes, ctypes.byref(dims), _stream(stream)),
+           "paged_decode_step_multi")
+    return out
+
+
+def paged_kv_slot_mapping_multi(block_tables: np.ndarray, context_lens: np.ndarray, q_len: int,
+                                block_size: int = 16) -> np.ndarray:
+    """Host: slots [B][q_len] of each sequence's q_len newest tokens (-1 below position 0)."""
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    out = np.empty((cl.shape[0], q_len), dtype=np.int32)
+    _check(lib().paged_kv_slot_mapping_multi(bt.ctypes.data_as(c_int32_p), cl.ctypes.data_as(c_int32_p),
+                                             cl.shape[0], bt.shape[1] if bt.ndim == 2 else 0, block_size, q_len,
+                                             out.ctypes.data_as(c_int32_p)),
+           "paged_kv_slot_mapping_multi")
+    return out
+
+
 # ---------------------------------------------------------------- FP8 (E4M3) cache
 
 _FP8_CACHE_DTYPES = (torch.uint8, torch.float8_e4m3fn)

@@ -282,4 +282,28 @@ int paged_kv_slot_mapping(const int32_t* block_tables, const int32_t* context_le
   return PKV_OK;
 }
 
+int paged_kv_slot_mapping_multi(const int32_t* block_tables, const int32_t* context_lens, int32_t num_seqs,
+                                int32_t max_blocks, int32_t block_size, int32_t q_len, int32_t* slot_mapping) {
+  if (num_seqs < 0 || max_blocks < 0 || block_size <= 0 || q_len < 1 ||
+      (num_seqs > 0 && (!block_tables || !context_lens || !slot_mapping)))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "slot_mapping_multi: bad argument");
+  for (int32_t b = 0; b < num_seqs; ++b) {
+    const int32_t L = context_lens[b];
+    for (int32_t i = 0; i < q_len; ++i) {
+      const int32_t pos = L - q_len + i;
+      int32_t& out = slot_mapping[static_cast<int64_t>(b) * q_len + i];
+      if (pos < 0) {
+        out = -1;
+        continue;
+      }
+      const int32_t j = pos / block_size;
+      if (j >= max_blocks) return pkv_fail(PKV_ERR_INVALID_ARG, "slot_mapping_multi: context longer than its table");
+      const int32_t blk = block_tables[static_cast<int64_t>(b) * max_blocks + j];
+      if (blk < 0) return pkv_fail(PKV_ERR_INVALID_ARG, "slot_mapping_multi: table entry is -1");
+      out = blk * block_size + pos % block_size;
+    }
+  }
+  return PKV_OK;
+}
+
 }  // extern "C"

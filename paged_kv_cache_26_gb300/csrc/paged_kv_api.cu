@@ -12,6 +12,7 @@
 #include <string>
 
 #include "paged_kv.h"
+#include "multi_query.cuh"
 #include "paged_kv_kernels.cuh"
 #include "pkv_errors.h"
 
@@ -464,9 +465,180 @@ int append_fp8_impl(const void* k_new, const void* v_new, const int32_t* slot_ma
   return PKV_OK;
 }
 
+// ------------------------------------------------------------------ several new tokens per sequence
+
+// Splits of the multi-token kernel: 512-token splits, more when the
+// (sequence, KV head) units alone would not give two CTAs per SM.
+void multi_plan(const pkv_dims* d, int32_t requested, int32_t* splits, int32_t* split_blocks) {
+  const int32_t mb = d->max_blocks_per_seq;
+  if (mb <= 1) {
+    *splits = 1;
+    *split_blocks = mb > 0 ? mb : 1;
+    return;
+  }
+  int64_t n = requested;
+  if (n == 0) {
+    const int64_t units = static_cast<int64_t>(d->num_seqs) * d->num_kv_heads;
+    n = (mb + kAutoSplitBlocks - 1) / kAutoSplitBlocks;
+    const int64_t fill = (2 * static_cast<int64_t>(device_sms()) + units - 1) / units;
+    if (fill > n) n = fill;
+  }
+  if (n > mb) n = mb;
+  if (n < 1) n = 1;
+  const int32_t per = static_cast<int32_t>((mb + n - 1) / n);
+  *split_blocks = per;
+  *splits = (mb + per - 1) / per;
+}
+
+size_t multi_workspace(const pkv_dims* d, int32_t q_len, int32_t splits) {
+  if (splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(d->num_seqs) * q_len * d->num_q_heads * splits;
+  return align256(rows * d->head_dim * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+int check_multi(const pkv_dims* d, int32_t q_len, int32_t num_splits) {
+  int rc = check_dims(d, true);
+  if (rc != PKV_OK) return rc;
+  if (q_len < 1 || q_len > pkv::kMaxQueryLen)
+    return pkv_fail(PKV_ERR_UNSUPPORTED, "multi-token decode: q_len must be 1.." + std::to_string(pkv::kMaxQueryLen));
+  if (num_splits < 0) return pkv_fail(PKV_ERR_INVALID_ARG, "num_splits must be >= 0");
+  if (static_cast<int64_t>(d->num_seqs) * q_len * d->num_q_heads >= (int64_t(1) << 31))
+    return pkv_fail(PKV_ERR_UNSUPPORTED, "multi-token decode: too many query rows");
+  return PKV_OK;
+}
+
+// Attention for q_len new tokens per sequence, optionally preceded by the
+// append of their K/V (k_new / v_new non-null) at positions L - q_len .. L - 1.
+int decode_multi_impl(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                      const int32_t* block_tables, const int32_t* context_lens, int32_t q_len, float scale,
+                      void* out, int32_t num_splits, void* workspace, size_t workspace_bytes, const pkv_dims* d,
+                      cudaStream_t stream) {
+  int rc = check_multi(d, q_len, num_splits);
+  if (rc != PKV_OK) return rc;
+  if (d->num_seqs == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || (!block_tables && d->max_blocks_per_seq > 0) || !context_lens || !out)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "decode_attention_multi: NULL pointer");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "decode_attention_multi: misaligned pointer (q/out/caches need 16 bytes)");
+  if (!std::isfinite(scale)) return pkv_fail(PKV_ERR_INVALID_ARG, "decode_attention_multi: scale is not finite");
+  const bool append = k_new != nullptr;
+  if (append != (v_new != nullptr))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "decode_step_multi: k_new and v_new must both be given");
+  if (append && (!aligned(k_new, 16) || !aligned(v_new, 16)))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "decode_step_multi: k_new / v_new must be 16-byte aligned");
+  int32_t splits, split_blocks;
+  multi_plan(d, num_splits, &splits, &split_blocks);
+  const size_t need = multi_workspace(d, q_len, splits);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "decode_attention_multi: workspace missing, too small (" +
+                                             std::to_string(need) + " bytes needed) or not 256-byte aligned");
+  const bool bf16 = d->dtype == PKV_DTYPE_BF16;
+  cudaError_t e;
+  if (append && d->max_blocks_per_seq > 0) {
+    const int32_t chunks = d->head_dim * 2 / 16;
+    const int64_t total = static_cast<int64_t>(d->num_seqs) * q_len * d->num_kv_heads * chunks;
+    const int64_t blocks64 = (total + 255) / 256;
+    pkv::append_multi_kernel<<<static_cast<int>(blocks64 < 65536 ? blocks64 : 65536), 256, 0, stream>>>(
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), block_tables, context_lens,
+        d->num_seqs, q_len, d->max_blocks_per_seq, d->num_kv_heads, chunks, d->num_blocks,
+        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "append_multi_kernel launch");
+  }
+  CUtensorMap mk, mv;
+  if ((rc = g_maps.get(k_cache, d, false, &mk)) != PKV_OK) return rc;
+  if ((rc = g_maps.get(v_cache, d, false, &mv)) != PKV_OK) return rc;
+  pkv::DecodeArgs args = {};
+  args.q = q;
+  args.out = out;
+  args.block_tables = block_tables;
+  args.context_lens = context_lens;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t rows = static_cast<size_t>(d->num_seqs) * q_len * d->num_q_heads;
+  args.part_o = need ? reinterpret_cast<float*>(ws) : nullptr;
+  args.part_lse = need ? reinterpret_cast<float*>(ws + align256(rows * splits * d->head_dim * sizeof(float)))
+                       : nullptr;
+  args.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  args.num_seqs = d->num_seqs;
+  args.num_q_heads = d->num_q_heads;
+  args.num_kv_heads = d->num_kv_heads;
+  args.group = d->num_q_heads / d->num_kv_heads;
+  args.max_blocks = d->max_blocks_per_seq;
+  args.num_blocks = d->num_blocks;
+  args.num_splits = splits;
+  args.split_blocks = split_blocks;
+  const int nq = (args.group * q_len + 7) / 8;
+  const dim3 grid(splits, d->num_kv_heads, d->num_seqs);
+  auto launch = [&](auto kern, auto merge, int stage_bytes, auto typed_out) -> int {
+    const int smem = pkv::kMultiStages * stage_bytes + 1024;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute(decode_multi_query_kernel)");
+    kern<<<grid, (nq + 1) * 32, smem, stream>>>(mk, mv, args, q_len);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return cuda_fail(err, "decode_multi_query_kernel launch");
+    if (splits > 1) {
+      merge<<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(
+          args.part_o, args.part_lse, context_lens, static_cast<decltype(typed_out)>(out), d->num_seqs,
+          q_len * d->num_q_heads, splits,
+          split_blocks, d->max_blocks_per_seq);
+      err = cudaGetLastError();
+      if (err != cudaSuccess) return cuda_fail(err, "merge_split_kernel launch");
+    }
+    return PKV_OK;
+  };
+  if (d->head_dim == 128) {
+    if (bf16)
+      return launch(pkv::decode_multi_query_kernel<__nv_bfloat16, 128, pkv::kMultiStages>,
+                    pkv::merge_split_kernel<__nv_bfloat16, 128>, pkv::TileShape<128>::kStageBytes,
+                    static_cast<__nv_bfloat16*>(nullptr));
+    return launch(pkv::decode_multi_query_kernel<__half, 128, pkv::kMultiStages>, pkv::merge_split_kernel<__half, 128>,
+                  pkv::TileShape<128>::kStageBytes, static_cast<__half*>(nullptr));
+  }
+  if (bf16)
+    return launch(pkv::decode_multi_query_kernel<__nv_bfloat16, 64, pkv::kMultiStages>,
+                  pkv::merge_split_kernel<__nv_bfloat16, 64>, pkv::TileShape<64>::kStageBytes,
+                  static_cast<__nv_bfloat16*>(nullptr));
+  return launch(pkv::decode_multi_query_kernel<__half, 64, pkv::kMultiStages>, pkv::merge_split_kernel<__half, 64>,
+                pkv::TileShape<64>::kStageBytes, static_cast<__half*>(nullptr));
+}
+
 }  // namespace
 
 extern "C" {
+
+int paged_decode_attention_multi(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_tables, const int32_t* context_lens, int32_t q_len,
+                                 float scale, void* out, int32_t num_splits, void* workspace,
+                                 size_t workspace_bytes, const pkv_dims* dims, void* stream) {
+  return decode_multi_impl(q, nullptr, nullptr, const_cast<void*>(k_cache), const_cast<void*>(v_cache), block_tables,
+                           context_lens, q_len, scale, out, num_splits, workspace, workspace_bytes, dims,
+                           static_cast<cudaStream_t>(stream));
+}
+
+int paged_decode_step_multi(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens, int32_t q_len, float scale,
+                            void* out, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                            const pkv_dims* dims, void* stream) {
+  if (!k_new || !v_new) return pkv_fail(PKV_ERR_INVALID_ARG, "decode_step_multi: NULL k_new / v_new");
+  return decode_multi_impl(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, q_len, scale, out,
+                           num_splits, workspace, workspace_bytes, dims, static_cast<cudaStream_t>(stream));
+}
+
+size_t paged_decode_multi_workspace_bytes(const pkv_dims* dims, int32_t q_len, int32_t num_splits) {
+  if (check_multi(dims, q_len, num_splits) != PKV_OK) return 0;
+  int32_t splits, split_blocks;
+  multi_plan(dims, num_splits, &splits, &split_blocks);
+  return multi_workspace(dims, q_len, splits);
+}
+
+int32_t paged_decode_multi_resolve_splits(const pkv_dims* dims, int32_t q_len, int32_t num_splits) {
+  int rc = check_multi(dims, q_len, num_splits);
+  if (rc != PKV_OK) return rc;
+  int32_t splits, split_blocks;
+  multi_plan(dims, num_splits, &splits, &split_blocks);
+  return splits;
+}
 
 int paged_kv_append_fp8(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t num_tokens,
                         void* k_cache, void* v_cache, const float* k_scale, const float* v_scale,

@@ -236,14 +236,8 @@ struct WarpAttn {
     const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
     m0 = mn0;
     m1 = mn1;
-    const uint32_t plo = pack2<T>(exp2f(x0 - mn0), exp2f(x1 - mn1));  // token gid, heads 2c, 2c+1
-    const uint32_t phi = pack2<T>(exp2f(x2 - mn0), exp2f(x3 - mn1));  // token gid + 8
-    const float2 fl = unpack2<T>(plo), fh = unpack2<T>(phi);
-    l0 = l0 * al0 + (fl.x + fh.x);  // sums of the rounded weights the P V product uses
-    l1 = l1 * al1 + (fl.y + fh.y);
-    // P^T as the B operand: tokens 2c, 2c+1 (and 2c+8, 2c+9) of head gid.
-    const uint32_t b0 = movmatrix_trans(plo);
-    const uint32_t b1 = movmatrix_trans(phi);
+    uint32_t b0, b1, c0 = 0, c1 = 0;
+    weights(exp2f(x0 - mn0), exp2f(x1 - mn1), exp2f(x2 - mn0), exp2f(x3 - mn1), al0, al1, b0, b1, c0, c1);
 
     uint4 vr[4][Shape::kBoxes];  // V rows 2c, 2c+1, 2c+8, 2c+9; chunk gid of each box
 #pragma unroll
@@ -277,6 +271,34 @@ struct WarpAttn {
       const uint32_t a2 = __byte_perm(word_of(vr[2][0], w0), word_of(vr[3][0], w0), sel);
       const uint32_t a3 = __byte_perm(word_of(vr[2][bx1], w1), word_of(vr[3][bx1], w1), sel);
       mma16816<T>(acc[mt], a0, a1, a2, a3, b0, b1);
+      if constexpr (MmaKind<T>::kBf16) mma16816<T>(acc[mt], a0, a1, a2, a3, c0, c1);
+    }
+  }
+
+  // Softmax weights of tokens gid (e0: head 2c, e1: head 2c+1) and gid + 8
+  // (e2, e3) as the B operand of O^T += V^T P^T (b0 / b1: tokens 2c, 2c+1 and
+  // 2c+8, 2c+9 of head gid, via movmatrix), and the running sums.  fp16 keeps
+  // 11 bits of each weight, enough for the output bound; bf16 keeps 8, which
+  // short contexts with cancelling values would feel (about 2^-9 of |V|), so
+  // for bf16 the weights go in as two bf16 terms, p = hi + lo (c0 / c1 = lo),
+  // good to about 2^-17.  l sums the weights as fp32 (what the product uses,
+  // to that precision).
+  __device__ __forceinline__ void weights(float e0, float e1, float e2, float e3, float al0, float al1, uint32_t& b0,
+                                          uint32_t& b1, uint32_t& c0, uint32_t& c1) {
+    const uint32_t plo = pack2<T>(e0, e1);
+    const uint32_t phi = pack2<T>(e2, e3);
+    b0 = movmatrix_trans(plo);
+    b1 = movmatrix_trans(phi);
+    if constexpr (MmaKind<T>::kBf16) {
+      const float2 fl = unpack2<T>(plo), fh = unpack2<T>(phi);
+      c0 = movmatrix_trans(pack2<T>(e0 - fl.x, e1 - fl.y));
+      c1 = movmatrix_trans(pack2<T>(e2 - fh.x, e3 - fh.y));
+      l0 = l0 * al0 + (e0 + e2);
+      l1 = l1 * al1 + (e1 + e3);
+    } else {
+      const float2 fl = unpack2<T>(plo), fh = unpack2<T>(phi);
+      l0 = l0 * al0 + (fl.x + fh.x);  // sums of the rounded weights the P V product uses
+      l1 = l1 * al1 + (fl.y + fh.y);
     }
   }
 
@@ -1373,7 +1395,9 @@ __global__ void __launch_bounds__((NC + 1) * 32)
 }
 
 // One warp per (sequence, query head): out = sum_s w_s o_s / sum_s w_s with
-// w_s = 2^(lse_s - max lse), over the splits that hold at least one token.
+// w_s = 2^(lse_s - max lse), over the splits that hold at least one token.  A
+// row no split saw (lse = -inf everywhere: a new token before position 0 of
+// a multi-token call) is zero.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) merge_split_kernel(const float* __restrict__ o_part,
                                                           const float* __restrict__ lse_part,
@@ -1393,10 +1417,10 @@ __global__ void __launch_bounds__(128) merge_split_kernel(const float* __restric
   float o[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) o[k] = 0.f;
-  if (nvalid > 0) {
-    const float* lse = lse_part + static_cast<int64_t>(row) * num_splits;
-    float M = -INFINITY;
-    for (int s = 0; s < nvalid; ++s) M = fmaxf(M, lse[s]);
+  const float* lse = lse_part + static_cast<int64_t>(row) * num_splits;
+  float M = -INFINITY;
+  for (int s = 0; s < nvalid; ++s) M = fmaxf(M, lse[s]);
+  if (M > -INFINITY) {
     float L = 0.f;
     for (int s = 0; s < nvalid; ++s) {
       const float w = exp2f(lse[s] - M);

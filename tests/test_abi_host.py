@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 
 import oracle
+import paged_kv_cache_26_gb300 as pkv
 from paged_kv_cache_26_gb300 import BlockAllocator, PagedKVError, paged_kv_slot_mapping
 from paged_kv_cache_26_gb300 import build as pkv_build
 from paged_kv_cache_26_gb300._native import EXPORTED
@@ -144,3 +145,14 @@ def test_allocator_waste_below_one_block():
         n = int((row >= 0).sum())
         assert n == oracle.blocks_needed(int(L), 16)
         assert 0 <= n * 16 - L < 16
+
+
+def test_slot_mapping_multi_matches_oracle():
+    rng = np.random.default_rng(5)
+    B, MB, n = 7, 6, 4
+    tables = np.stack([rng.permutation(40)[:MB] for _ in range(B)]).astype(np.int32)
+    lens = np.array([0, 1, 3, 4, 16, 17, 96], np.int32)
+    got = pkv.paged_kv_slot_mapping_multi(tables, lens, n)
+    assert np.array_equal(got, oracle.slot_mapping_multi(tables, lens, n, 16))
+    with pytest.raises(pkv.PagedKVError):
+        pkv.paged_kv_slot_mapping_multi(tables, np.array([97] * B, np.int32), n)   # past the table

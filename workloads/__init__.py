@@ -274,3 +274,46 @@ def fp8_caches(w: Workload, seed: int = 0) -> Fp8Caches:
             codes.append(c)
             scales.append(s)
     return out
+
+
+# ---------------------------------------------------------------- several new tokens per sequence
+
+@dataclass
+class MultiTokens:
+    """q_len new tokens per sequence: their queries and K/V rows."""
+
+    q_len: int
+    q: List[torch.Tensor]        # per layer: T[B][q_len][Hq][D]
+    k_new: List[torch.Tensor]    # per layer: T[B][q_len][Hkv][D]
+    v_new: List[torch.Tensor]
+
+
+def generate_multi(spec: WorkloadSpec, q_len: int, seed: int = 0, device="cpu",
+                   layers: Optional[int] = None) -> Tuple[Workload, MultiTokens]:
+    """A workload whose sequences each receive q_len new tokens this step: the
+    cache holds the first L - q_len tokens of each sequence and NaN in every
+    other slot (the q_len slots the append fills included); the new tokens'
+    queries and K/V are N(0,1) like the rest."""
+    w = generate(spec, seed=seed, device=device, layers=layers)
+    bs = spec.block_size
+    blk, off = [], []
+    for b in range(spec.batch):
+        L = int(w.context_lens[b])
+        for pos in range(max(0, L - q_len), L - 1):      # position L - 1 is already NaN
+            blk.append(int(w.block_tables[b, pos // bs]))
+            off.append(pos % bs)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed + 104729)
+    dt = DTYPES[spec.dtype]
+    B, H, Hk, D = spec.batch, spec.num_q_heads, spec.num_kv_heads, spec.head_dim
+    m = MultiTokens(q_len, [], [], [])
+    for layer in range(len(w.k_cache)):
+        if blk:
+            bi = torch.tensor(blk, device=device)
+            oi = torch.tensor(off, device=device)
+            w.k_cache[layer][bi, :, oi, :] = float("nan")
+            w.v_cache[layer][bi, :, oi, :] = float("nan")
+        m.q.append(torch.randn((B, q_len, H, D), generator=gen, device=device, dtype=torch.float32).to(dt))
+        m.k_new.append(torch.randn((B, q_len, Hk, D), generator=gen, device=device, dtype=torch.float32).to(dt))
+        m.v_new.append(torch.randn((B, q_len, Hk, D), generator=gen, device=device, dtype=torch.float32).to(dt))
+    return w, m
