@@ -47,7 +47,7 @@ import numpy as np
 __all__ = [
     "widen", "e4m3_decode", "e4m3_encode", "quantize_e4m3", "dequantize_e4m3", "kv_append_fp8", "kv_head_of", "slot_of_position", "slot_mapping", "kv_append",
     "gather_kv", "attend_one", "decode_attention", "decode_attention_rows", "decode_attention_multi",
-    "slot_mapping_multi",
+    "slot_mapping_multi", "copy_blocks",
     "split_partials", "lse_merge", "kv_bytes_per_token", "blocks_needed",
     "allocated_bytes", "wasted_bytes", "kv_cache_bytes", "decode_step_tokens_per_s",
     "attention_call_bytes",
@@ -249,6 +249,22 @@ def decode_attention(q_bits, k_cache_bits, v_cache_bits, block_tables, context_l
     rows = [(b, h) for b in range(B) for h in range(Hq)]
     return decode_attention_rows(q_bits, k_cache_bits, v_cache_bits, block_tables, context_lens,
                                  scale, dtype, block_size, rows).reshape(B, Hq, D)
+
+
+# ---------------------------------------------------------------- copy-on-write
+
+def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, pairs) -> Tuple[np.ndarray, np.ndarray]:
+    """Copy-on-write of shared blocks (kasblo.com "vLLMとは？", section
+    "block共有とAutomatic Prefix Caching": a block shared by several sequences is
+    duplicated only when one of them must write into it).  For each (src, dst)
+    pair, physical block dst becomes a copy of block src (every KV head, every
+    slot, K and V).  Destinations are distinct and are not sources."""
+    k = k_cache.copy()
+    v = v_cache.copy()
+    for src, dst in pairs:
+        k[dst] = k_cache[src]
+        v[dst] = v_cache[src]
+    return k, v
 
 
 # ---------------------------------------------------------------- several new tokens per sequence

@@ -584,3 +584,51 @@ def test_planted_causal_off_by_one_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "decode_attention_multi", _bad_multi)
     bad = oracle.decode_attention_multi(q, kc, vc, tables, np.array(lens), n, 0.4, "fp16", 4)
     assert not np.abs(bad - ref).max() < 1e-13
+
+
+# ------------------------------------------------------------------ copy-on-write
+
+def test_copy_blocks_is_a_block_permutation_of_bytes():
+    rng = np.random.default_rng(3)
+    kc = rng.integers(0, 2 ** 16, size=(9, 2, 4, 8), dtype=np.uint16)
+    vc = rng.integers(0, 2 ** 16, size=(9, 2, 4, 8), dtype=np.uint16)
+    pairs = [(1, 5), (3, 7), (1, 8)]
+    k, v = oracle.copy_blocks(kc, vc, pairs)
+    for src, dst in pairs:
+        assert np.array_equal(k[dst], kc[src]) and np.array_equal(v[dst], vc[src])
+    untouched = [b for b in range(9) if b not in (5, 7, 8)]
+    assert np.array_equal(k[untouched], kc[untouched]) and np.array_equal(v[untouched], vc[untouched])
+    assert np.array_equal(oracle.copy_blocks(kc, vc, [])[0], kc)
+
+
+def test_forked_sequences_see_the_prefix_and_their_own_tokens_after_copy_on_write():
+    """Two sequences share a 6-token prefix (block size 4: one full and one
+    partial block).  Each then writes its own tokens: the copy of the partial
+    block before the first write keeps the prefix for both, and neither sees
+    the other's tokens."""
+    bs, D = 4, 8
+    kc = np.full((6, 1, bs, D), 0x7E00, np.uint16)
+    vc = kc.copy()
+    rng = np.random.default_rng(0)
+    prefix = rng.integers(0, 0x3C00, size=(6, D), dtype=np.uint16)
+    table_a = [2, 4]                       # the prefix: block 2 full, block 4 holds tokens 4, 5
+    for t in range(6):
+        kc[table_a[t // bs], 0, t % bs] = prefix[t]
+        vc[table_a[t // bs], 0, t % bs] = prefix[t] ^ 1
+    table_b = list(table_a)                # the fork shares both blocks
+    kc, vc = oracle.copy_blocks(kc, vc, [(4, 1)])   # b writes position 6 into shared block 4: copy it first
+    table_b[1] = 1
+    own_a = rng.integers(0, 0x3C00, size=(3, D), dtype=np.uint16)
+    own_b = rng.integers(0, 0x3C00, size=(3, D), dtype=np.uint16)
+    table_a.append(0)
+    table_b.append(3)
+    for i in range(3):
+        pos = 6 + i
+        kc, vc = oracle.kv_append(kc, vc, own_a[i:i + 1, None], own_a[i:i + 1, None] ^ 1,
+                                  np.array([table_a[pos // bs] * bs + pos % bs]), bs)
+        kc, vc = oracle.kv_append(kc, vc, own_b[i:i + 1, None], own_b[i:i + 1, None] ^ 1,
+                                  np.array([table_b[pos // bs] * bs + pos % bs]), bs)
+    ka = oracle.gather_kv(kc, np.array(table_a), 9, 0, bs)
+    kb = oracle.gather_kv(kc, np.array(table_b), 9, 0, bs)
+    assert np.array_equal(ka, np.concatenate([prefix, own_a])) and np.array_equal(kb, np.concatenate([prefix, own_b]))
+    assert np.array_equal(oracle.gather_kv(vc, np.array(table_b), 9, 0, bs), np.concatenate([prefix, own_b]) ^ 1)
