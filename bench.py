@@ -624,6 +624,104 @@ def run_multi(args, rank, world, local):
         print(json.dumps(result), flush=True)
 
 
+# ----------------------------------------------------------------------------- copy-on-write
+
+def run_cow(args, rank, world, local):
+    """Copy-on-write block copies at this configuration's block shape: one
+    step = paged_kv_copy_blocks of `--cow-pairs` random (src, dst) block pairs
+    of the K and V pools.  Bytes: each pair reads and writes one block of K and
+    one of V."""
+    import oracle
+    import paged_kv_cache_26_gb300 as pkv
+    from paged_kv_cache_26_gb300 import build as pkv_build
+
+    pkv_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    spec = wl.CONFIGS[args.config]
+    n = args.cow_pairs
+    nb = max(4 * n, 1024)
+    dt = wl.DTYPES[spec.dtype]
+    g = torch.Generator(device=dev)
+    g.manual_seed(args.seed + rank)
+    kc = torch.randn((nb, spec.num_kv_heads, spec.block_size, spec.head_dim), generator=g, device=dev).to(dt)
+    vc = torch.randn_like(kc)
+    perm = np.random.default_rng(args.seed + rank).permutation(nb)
+    pairs_np = np.stack([perm[:n], perm[n:2 * n]], 1).astype(np.int32)
+    pairs = torch.from_numpy(pairs_np).to(dev)
+    block_bytes = spec.num_kv_heads * spec.block_size * spec.head_dim * kc.element_size()
+    step_bytes = 2 * 2 * block_bytes * n
+    stream = torch.cuda.current_stream(dev)
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        pkv.paged_kv_copy_blocks(kc, vc, pairs)
+    torch.cuda.synchronize()
+    pkv.paged_kv_check_status(stream)
+    sampler = ClockSampler(local) if rank == 0 else None
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(stream)
+    for _ in range(K):
+        pkv.paged_kv_copy_blocks(kc, vc, pairs)
+    end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop(t_wall0, time.time()) if sampler else None
+    barrier(world)
+    pkv.paged_kv_check_status(stream)
+    ms = max_over_ranks(start.elapsed_time(end), world, dev) / K
+    peak, peak_kind = load_peaks()
+    achieved = step_bytes / (ms * 1e-3) / 1e9
+    # end to end: the pair list copied in from pinned host memory each step, a word read back
+    hp = torch.from_numpy(pairs_np).pin_memory()
+    flag = torch.empty(1, dtype=torch.int32).pin_memory()
+    barrier(world)
+    start.record(stream)
+    for _ in range(K):
+        pairs.copy_(hp, non_blocking=True)
+        pkv.paged_kv_copy_blocks(kc, vc, pairs)
+        flag.copy_(pairs[0, :1], non_blocking=True)
+    end.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(start.elapsed_time(end), world, dev) / K
+    result = {
+        "metric": METRIC, "value": round(world * achieved, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic (seeded N(0,1) blocks, seeded pairs)",
+        "config": {"workload": f"{spec.name}_cow{n}", "pairs": n, "num_blocks": nb,
+                   "block_bytes_per_cache": block_bytes,
+                   "l2": f"no flush: each call moves {step_bytes / 2**20:.0f} MiB over a "
+                         f"{2 * nb * block_bytes / 2**20:.0f} MiB pool",
+                   "step": "paged_kv_copy_blocks: copy-on-write of n shared blocks (K and V)"},
+        "roofline": {"bound": "hbm", "kernel": "copy_blocks_kernel", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "bytes_per_launch": step_bytes, "avg_launch_us": round(ms * 1e3, 2)},
+        "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(pairs_np.nbytes), "d2h_bytes_per_step": 4},
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        # the oracle works on a host copy of the touched blocks
+        idx = torch.from_numpy(np.unique(pairs_np)).to(dev)
+        remap = {int(b): i for i, b in enumerate(np.unique(pairs_np))}
+        hk = kc.index_select(0, idx).cpu().view(torch.int16).numpy()
+        hv = vc.index_select(0, idx).cpu().view(torch.int16).numpy()
+        local_pairs = [(remap[int(a)], remap[int(b)]) for a, b in pairs_np]
+        spent, calls = 0.0, 0
+        while spent < args.cpu_budget:
+            t0 = time.perf_counter()
+            oracle.copy_blocks(hk, hv, local_pairs)
+            spent += time.perf_counter() - t0
+            calls += 1
+        result["cpu_baseline"] = {"value": calls * step_bytes / spent / 1e9, "unit": UNIT, "cores": 1,
+                                  "kind": "oracle", "sample": f"{calls} full calls ({n} pairs each) on a host copy "
+                                                              f"of the touched blocks, {spent:.1f} s, one thread"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
 # ----------------------------------------------------------------------------- continuous batching
 
 def run_loop(args, rank, world, local):
@@ -765,6 +863,8 @@ def main():
                     help="pool format: the configuration's fp16/bf16, or E4M3 codes with per-head scales")
     ap.add_argument("--loop", action="store_true", help="continuous-batching loop instead of the fixed batch")
     ap.add_argument("--q-len", type=int, default=1, help="new tokens per sequence (>1: multi-token decode)")
+    ap.add_argument("--cow", action="store_true", help="copy-on-write block copies instead of the decode step")
+    ap.add_argument("--cow-pairs", type=int, default=2048, help="block pairs per copy-on-write call")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -775,6 +875,8 @@ def main():
         run_loop(args, rank, world, local)
     elif args.q_len > 1:
         run_multi(args, rank, world, local)
+    elif args.cow:
+        run_cow(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:

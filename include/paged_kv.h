@@ -304,6 +304,24 @@ int paged_kv_slot_mapping_multi(const int32_t* block_tables, const int32_t* cont
                                 int32_t num_seqs, int32_t max_blocks, int32_t block_size,
                                 int32_t q_len, int32_t* slot_mapping);
 
+/* ------------------------------------------------------------------------
+ * Copy-on-write of shared blocks: kasblo.com "vLLMとは？", section
+ * "block共有とAutomatic Prefix Caching" (a block carries a reference count, is
+ * shared by several sequences, and is duplicated only when one of them must
+ * write into it: parallel sampling, a shared prefix that ends inside a block).
+ * The allocator (block_allocator_fork / _append_slot_cow / _step_batch_cow
+ * below) decides the copies; this call performs them (device): for each pair
+ * block_pairs[i] = {src, dst} (int32[num_pairs][2], device), physical block
+ * dst of k_cache and of v_cache becomes a copy of block src.  Destinations
+ * must be distinct and not among the sources (the allocator's are fresh
+ * blocks).  cache_elem_bytes: 2 for fp16/bf16 pools, 1 for E4M3 pools
+ * (dims.dtype is not used).  Enqueue it before the append that writes into the
+ * copies.  A pair outside [0, num_blocks) is skipped and flagged
+ * (PKV_ERR_OUT_OF_RANGE from paged_kv_check_status).
+ * ---------------------------------------------------------------------- */
+int paged_kv_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs, int32_t num_pairs,
+                         const pkv_dims* dims, int32_t cache_elem_bytes, void* stream);
+
 /* Synchronises `stream`, then reads and clears this device's error word.
  * Returns PKV_OK, PKV_ERR_OUT_OF_RANGE, PKV_ERR_TIMEOUT or PKV_ERR_CUDA. */
 int paged_kv_check_status(void* stream);
@@ -340,6 +358,34 @@ int block_allocator_add_seq(pkv_block_allocator* a, int32_t num_tokens, int32_t*
  * must be a multiple of block_size and <= the length of src_seq. */
 int block_allocator_fork_prefix(pkv_block_allocator* a, int32_t src_seq, int32_t prefix_tokens,
                                 int32_t num_tokens, int32_t* seq_id);
+
+/* A new sequence holding the first prefix_tokens tokens of src_seq (any
+ * count 0..length): it shares the ceil(prefix_tokens / block_size) blocks that
+ * hold them (their reference counts rise), the last possibly partly filled.
+ * Parallel sampling forks the whole prompt; a request reusing part of
+ * another's context forks that part.  Its writes go through the _cow calls
+ * below, which copy a shared block before writing into it. */
+int block_allocator_fork(pkv_block_allocator* a, int32_t src_seq, int32_t prefix_tokens, int32_t* seq_id);
+
+/* append_slot with copy-on-write: if the block that receives the token is
+ * shared, the sequence gets a fresh block in its place (the old block loses a
+ * reference) and *num_copies = 1 with copy_pair = {old, fresh}: the caller
+ * copies the block (paged_kv_copy_blocks) before writing the token.  Else
+ * *num_copies = 0.  PKV_ERR_NO_BLOCKS (nothing changed) if a block is needed
+ * and the pool is empty. */
+int block_allocator_append_slot_cow(pkv_block_allocator* a, int32_t seq_id, int32_t* slot,
+                                    int32_t* copy_pair, int32_t* num_copies);
+
+/* step_batch with copy-on-write: as block_allocator_step_batch, but a
+ * sequence whose next token lands in a shared block gets a private copy
+ * instead of an error.  copy_pairs (int32[n][2], host) receives the
+ * *num_copies {src, dst} block copies to perform before this step's append;
+ * when several sequences of the batch write into the same shared block, the
+ * last of them keeps the original.  All or nothing: on an error nothing
+ * changes. */
+int block_allocator_step_batch_cow(pkv_block_allocator* a, const int32_t* slot_seq_ids, int32_t n,
+                                   int32_t max_blocks, int32_t* tables, int32_t* context_lens,
+                                   int32_t* copy_pairs, int32_t* num_copies);
 
 /* Grow seq_id by one token and return its slot (block * block_size + offset).
  * Takes a new block when the last one is full.  PKV_ERR_SHARED_BLOCK if the

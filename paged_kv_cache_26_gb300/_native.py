@@ -80,6 +80,13 @@ _SIGNATURES = {
     "block_allocator_step_batch": (ctypes.c_int, [ctypes.c_void_p, c_int32_p, ctypes.c_int32, ctypes.c_int32,
                                                   c_int32_p, c_int32_p]),
     "block_allocator_free_seq": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
+    "block_allocator_fork": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, c_int32_p]),
+    "block_allocator_append_slot_cow": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, c_int32_p, c_int32_p,
+                                                       c_int32_p]),
+    "block_allocator_step_batch_cow": (ctypes.c_int, [ctypes.c_void_p, c_int32_p, ctypes.c_int32, ctypes.c_int32,
+                                                      c_int32_p, c_int32_p, c_int32_p, c_int32_p]),
+    "paged_kv_copy_blocks": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                            ctypes.POINTER(PkvDims), ctypes.c_int32, ctypes.c_void_p]),
     "block_allocator_block_tables": (ctypes.c_int, [ctypes.c_void_p, c_int32_p, ctypes.c_int32, ctypes.c_int32,
                                                     c_int32_p, c_int32_p]),
     "block_allocator_num_free": (ctypes.c_int32, [ctypes.c_void_p]),

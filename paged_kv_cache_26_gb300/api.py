@@ -414,6 +414,26 @@ def paged_decode_step_fp8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Ten
     return out
 
 
+def paged_kv_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, block_pairs: torch.Tensor,
+                         stream=None) -> None:
+    """Copy-on-write: for each row (src, dst) of block_pairs (int32 [n][2] on
+    the device), physical block dst of both caches becomes a copy of block src.
+    Caches: fp16/bf16 [NB][Hkv][16][D] or E4M3 codes (uint8 / float8_e4m3fn)."""
+    _need_cuda("k_cache", k_cache)
+    _need_cuda("v_cache", v_cache, k_cache.dtype)
+    _need_cuda("block_pairs", block_pairs, torch.int32)
+    if block_pairs.dim() != 2 or block_pairs.shape[1] != 2:
+        raise ValueError("block_pairs must be int32 [n][2]")
+    if k_cache.shape != v_cache.shape or k_cache.dim() != 4:
+        raise ValueError("caches must both be [num_blocks][num_kv_heads][16][head_dim]")
+    nb, hkv, bs, d = k_cache.shape
+    dims = PkvDims(num_seqs=0, num_q_heads=hkv, num_kv_heads=hkv, head_dim=d, block_size=bs, num_blocks=nb,
+                   max_blocks_per_seq=0, dtype=_DTYPE_CODE.get(k_cache.dtype, 0))
+    _check(lib().paged_kv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_pairs), block_pairs.shape[0],
+                                      ctypes.byref(dims), k_cache.element_size(), _stream(stream)),
+           "paged_kv_copy_blocks")
+
+
 def paged_kv_check_status(stream=None) -> None:
     """Synchronise the stream and raise if a kernel flagged an error."""
     _check(lib().paged_kv_check_status(_stream(stream)), "paged_kv_check_status")
@@ -484,6 +504,34 @@ class BlockAllocator:
         _check(lib().block_allocator_step_batch(self._h, ids.ctypes.data_as(c_int32_p), ids.shape[0], max_blocks,
                                                 tables.ctypes.data_as(c_int32_p), lens.ctypes.data_as(c_int32_p)),
                "step_batch")
+
+    def fork(self, src_seq: int, prefix_tokens: int) -> int:
+        """A new sequence sharing the blocks of src_seq's first prefix_tokens
+        tokens (any count; the last shared block may be partly filled)."""
+        sid = ctypes.c_int32()
+        _check(lib().block_allocator_fork(self._h, src_seq, prefix_tokens, ctypes.byref(sid)), "fork")
+        return sid.value
+
+    def append_slot_cow(self, seq_id: int):
+        """Grow seq_id by one token, copying a shared block first: returns
+        (slot, copy) with copy = (src, dst) or None."""
+        slot, n = ctypes.c_int32(), ctypes.c_int32()
+        pair = (ctypes.c_int32 * 2)()
+        _check(lib().block_allocator_append_slot_cow(self._h, seq_id, ctypes.byref(slot), pair, ctypes.byref(n)),
+               "append_slot_cow")
+        return slot.value, ((pair[0], pair[1]) if n.value else None)
+
+    def step_batch_cow(self, slot_seq_ids: np.ndarray, max_blocks: int, tables: np.ndarray, lens: np.ndarray,
+                       copy_pairs: np.ndarray) -> int:
+        """step_batch with copy-on-write; copy_pairs (int32 [n][2], filled in
+        place) receives the block copies to perform first.  Returns their count."""
+        ids = np.ascontiguousarray(slot_seq_ids, dtype=np.int32)
+        n = ctypes.c_int32()
+        _check(lib().block_allocator_step_batch_cow(self._h, ids.ctypes.data_as(c_int32_p), ids.shape[0], max_blocks,
+                                                    tables.ctypes.data_as(c_int32_p), lens.ctypes.data_as(c_int32_p),
+                                                    copy_pairs.ctypes.data_as(c_int32_p), ctypes.byref(n)),
+               "step_batch_cow")
+        return n.value
 
     def free_seq(self, seq_id: int) -> None:
         _check(lib().block_allocator_free_seq(self._h, seq_id), "free_seq")

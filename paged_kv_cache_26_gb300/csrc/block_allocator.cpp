@@ -11,6 +11,7 @@
 //
 // The random draw uses splitmix64 so that a seed gives the same placement on
 // every host architecture.
+#include <algorithm>
 #include <cstdint>
 #include <vector>
 
@@ -126,6 +127,114 @@ int block_allocator_fork_prefix(pkv_block_allocator* a, int32_t src_seq, int32_t
   s.len = num_tokens;
   s.live = true;
   *seq_id = id;
+  return PKV_OK;
+}
+
+int block_allocator_fork(pkv_block_allocator* a, int32_t src_seq, int32_t prefix_tokens, int32_t* seq_id) {
+  if (!a || !seq_id || !a->live(src_seq)) return pkv_fail(PKV_ERR_INVALID_ARG, "fork: bad allocator or source");
+  if (prefix_tokens < 0 || prefix_tokens > a->seqs[src_seq].len)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "fork: prefix must be 0..length of the source");
+  const int32_t id = a->new_seq_id();  // may grow seqs: take references after this
+  auto& src = a->seqs[src_seq];
+  auto& s = a->seqs[id];
+  s.blocks.assign(src.blocks.begin(), src.blocks.begin() + a->blocks_for(prefix_tokens));
+  for (int32_t blk : s.blocks) ++a->refcount[blk];
+  s.len = prefix_tokens;
+  s.live = true;
+  *seq_id = id;
+  return PKV_OK;
+}
+
+namespace {
+// Block j of sequence s is about to be written: if another sequence holds it
+// too, give s a private copy (a fresh block) and report the copy.
+void copy_on_write(pkv_block_allocator* a, pkv_block_allocator::Seq& s, int32_t j, int32_t* pair, int32_t* copies) {
+  const int32_t old = s.blocks[j];
+  if (a->refcount[old] <= 1) return;
+  const int32_t fresh = a->pop_block();
+  --a->refcount[old];
+  s.blocks[j] = fresh;
+  pair[0] = old;
+  pair[1] = fresh;
+  ++*copies;
+}
+}  // namespace
+
+int block_allocator_append_slot_cow(pkv_block_allocator* a, int32_t seq_id, int32_t* slot, int32_t* copy_pair,
+                                    int32_t* num_copies) {
+  if (!a || !slot || !copy_pair || !num_copies || !a->live(seq_id))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "append_slot_cow: bad argument");
+  auto& s = a->seqs[seq_id];
+  const int32_t pos = s.len;
+  const int32_t j = pos / a->block_size;
+  *num_copies = 0;
+  if (a->free_list.empty() && (j == static_cast<int32_t>(s.blocks.size()) || a->refcount[s.blocks[j]] > 1))
+    return pkv_fail(PKV_ERR_NO_BLOCKS, "append_slot_cow: pool is empty");
+  if (j == static_cast<int32_t>(s.blocks.size()))
+    s.blocks.push_back(a->pop_block());
+  else
+    copy_on_write(a, s, j, copy_pair, num_copies);
+  *slot = s.blocks[j] * a->block_size + pos % a->block_size;
+  s.len = pos + 1;
+  return PKV_OK;
+}
+
+int block_allocator_step_batch_cow(pkv_block_allocator* a, const int32_t* slot_seq_ids, int32_t n,
+                                   int32_t max_blocks, int32_t* tables, int32_t* context_lens, int32_t* copy_pairs,
+                                   int32_t* num_copies) {
+  if (!a || n < 0 || max_blocks < 0 || !num_copies ||
+      (n > 0 && (!slot_seq_ids || !tables || !context_lens || !copy_pairs)))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "step_batch_cow: bad argument");
+  *num_copies = 0;
+  // Check first, so that a failure changes nothing.  A block shared only
+  // within this batch is copied for all but the last of its holders to write
+  // into it, so count the writers per shared block.
+  int32_t need = 0;
+  const uint64_t stamp = ++a->batch_calls;
+  std::vector<int32_t> writers;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t id = slot_seq_ids[i];
+    if (id < 0) continue;
+    if (!a->live(id)) return pkv_fail(PKV_ERR_INVALID_ARG, "step_batch_cow: sequence not live");
+    auto& s = a->seqs[id];
+    if (s.stamp == stamp) return pkv_fail(PKV_ERR_INVALID_ARG, "step_batch_cow: sequence listed twice");
+    s.stamp = stamp;
+    if (a->blocks_for(s.len + 1) > max_blocks)
+      return pkv_fail(PKV_ERR_INVALID_ARG, "step_batch_cow: a sequence would outgrow max_blocks");
+    const int32_t j = s.len / a->block_size;
+    if (j == static_cast<int32_t>(s.blocks.size()))
+      ++need;
+    else if (a->refcount[s.blocks[j]] > 1)
+      writers.push_back(s.blocks[j]);
+  }
+  // Each shared block written by w sequences of the batch needs
+  // min(w, refcount - 1) copies: the last holder keeps the original.
+  std::sort(writers.begin(), writers.end());
+  for (size_t i = 0; i < writers.size();) {
+    size_t k = i;
+    while (k < writers.size() && writers[k] == writers[i]) ++k;
+    const int32_t w = static_cast<int32_t>(k - i), rc = a->refcount[writers[i]];
+    need += w < rc - 1 ? w : rc - 1;
+    i = k;
+  }
+  if (need > static_cast<int32_t>(a->free_list.size()))
+    return pkv_fail(PKV_ERR_NO_BLOCKS, "step_batch_cow: pool has too few free blocks for this step");
+  for (int32_t i = 0; i < n; ++i) {
+    int32_t* row = tables + static_cast<int64_t>(i) * max_blocks;
+    const int32_t id = slot_seq_ids[i];
+    int32_t k = 0;
+    if (id >= 0) {
+      int32_t slot, c = 0;
+      block_allocator_append_slot_cow(a, id, &slot, copy_pairs + 2 * static_cast<int64_t>(*num_copies), &c);
+      *num_copies += c;
+      const auto& s = a->seqs[id];
+      for (; k < static_cast<int32_t>(s.blocks.size()); ++k) row[k] = s.blocks[k];
+      context_lens[i] = s.len;
+    } else {
+      context_lens[i] = 0;
+    }
+    for (; k < max_blocks; ++k) row[k] = -1;
+  }
   return PKV_OK;
 }
 

@@ -12,6 +12,7 @@
 #include <string>
 
 #include "paged_kv.h"
+#include "block_copy.cuh"
 #include "multi_query.cuh"
 #include "paged_kv_kernels.cuh"
 #include "pkv_errors.h"
@@ -638,6 +639,32 @@ int32_t paged_decode_multi_resolve_splits(const pkv_dims* dims, int32_t q_len, i
   int32_t splits, split_blocks;
   multi_plan(dims, num_splits, &splits, &split_blocks);
   return splits;
+}
+
+int paged_kv_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs, int32_t num_pairs,
+                         const pkv_dims* d, int32_t cache_elem_bytes, void* stream_v) {
+  if (!d) return pkv_fail(PKV_ERR_INVALID_ARG, "copy_blocks: dims is NULL");
+  if (num_pairs < 0) return pkv_fail(PKV_ERR_INVALID_ARG, "copy_blocks: num_pairs < 0");
+  if (num_pairs == 0) return PKV_OK;
+  if (cache_elem_bytes != 1 && cache_elem_bytes != 2)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "copy_blocks: cache_elem_bytes must be 1 (E4M3) or 2 (fp16/bf16)");
+  if (d->num_kv_heads <= 0 || d->num_blocks <= 0 || d->head_dim <= 0 || d->head_dim % 16 != 0 ||
+      d->block_size != pkv::kBlockSize)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "copy_blocks: bad dims");
+  if (!k_cache || !v_cache || !block_pairs) return pkv_fail(PKV_ERR_INVALID_ARG, "copy_blocks: NULL pointer");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_pairs, 4))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "copy_blocks: misaligned pointer (caches need 16 bytes)");
+  const int64_t chunks = static_cast<int64_t>(d->num_kv_heads) * pkv::kBlockSize * d->head_dim * cache_elem_bytes / 16;
+  const int64_t total = chunks * num_pairs;
+  const int64_t blocks64 = (total + 255) / 256;
+  const int cap = 8 * device_sms();
+  pkv::copy_blocks_kernel<<<static_cast<int>(blocks64 < cap ? blocks64 : cap), 256, 0,
+                            static_cast<cudaStream_t>(stream_v)>>>(block_pairs, num_pairs, chunks, d->num_blocks,
+                                                                   static_cast<uint4*>(k_cache),
+                                                                   static_cast<uint4*>(v_cache));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "copy_blocks_kernel launch");
+  return PKV_OK;
 }
 
 int paged_kv_append_fp8(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t num_tokens,
