@@ -452,14 +452,25 @@ int decode_engine_admit(pkv_decode_engine* e, int32_t prompt_tokens, int32_t gen
                         const void* prompt_v, void* k_cache, void* v_cache, int32_t* slot_staging_dev,
                         const pkv_dims* dims, void* stream, int32_t* batch_slot);
 
+/* Parallel sampling: a new sequence in a free batch slot that shares every
+ * block of the sequence in src_slot (its whole context so far; reference
+ * counts rise, nothing is copied now) and runs gen_tokens steps.  The shared
+ * block that a step writes into is copied first (copy-on-write, see
+ * decode_engine_step).  PKV_ERR_NO_BLOCKS if no batch slot is free. */
+int decode_engine_fork(pkv_decode_engine* e, int32_t src_slot, int32_t gen_tokens, int32_t* batch_slot);
+
 /* One decode step for every active slot: tables_dev (int32[max_batch][max_blocks_per_seq])
- * and lens_dev (int32[max_batch]) receive the step's tables, then
- * paged_decode_step runs with q / k_new / v_new / out covering all max_batch
- * slots (empty slots: context 0, zero output, nothing appended) and
- * num_splits 0.  dims->num_seqs must be max_batch. */
-int decode_engine_step(pkv_decode_engine* e, int32_t* tables_dev, int32_t* lens_dev, const void* q,
-                       const void* k_new, const void* v_new, void* k_cache, void* v_cache, float scale, void* out,
-                       void* workspace, size_t workspace_bytes, const pkv_dims* dims, void* stream);
+ * and lens_dev (int32[max_batch]) receive the step's tables; blocks shared by
+ * forked sequences that this step writes into are first copied
+ * (copy_pairs_dev, int32[max_batch][2] device scratch, receives the pairs; it
+ * may be NULL when no sequence was forked); then paged_decode_step runs with
+ * q / k_new / v_new / out covering all max_batch slots (empty slots: context
+ * 0, zero output, nothing appended) and num_splits 0.  dims->num_seqs must be
+ * max_batch; the pools are fp16/bf16. */
+int decode_engine_step(pkv_decode_engine* e, int32_t* tables_dev, int32_t* lens_dev, int32_t* copy_pairs_dev,
+                       const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                       float scale, void* out, void* workspace, size_t workspace_bytes, const pkv_dims* dims,
+                       void* stream);
 
 /* Count the step against every active sequence; those that spent their
  * budget free their blocks.  freed_slots (host, max_batch entries) receives

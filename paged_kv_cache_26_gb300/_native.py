@@ -97,8 +97,9 @@ _SIGNATURES = {
                                            ctypes.POINTER(PkvDims), ctypes.c_void_p, c_int32_p]),
     "decode_engine_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                                          ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
-                                          ctypes.POINTER(PkvDims), ctypes.c_void_p]),
+                                          ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_size_t, ctypes.POINTER(PkvDims), ctypes.c_void_p]),
+    "decode_engine_fork": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, c_int32_p]),
     "decode_engine_finish": (ctypes.c_int, [ctypes.c_void_p, c_int32_p, c_int32_p]),
     "decode_engine_state": (ctypes.c_int, [ctypes.c_void_p, c_int32_p, c_int32_p]),
     "block_allocator_refcount": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_int32]),

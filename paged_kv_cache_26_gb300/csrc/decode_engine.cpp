@@ -7,10 +7,15 @@
 // and magi "Inference Batching", continuous batching (finished sequences leave
 // and waiting ones enter at every iteration).
 //
-// The engine owns only host memory: pinned staging for the block tables and
-// the prompts' slot mappings (two table buffers, a ring of four slot buffers),
-// each reused only after an event shows that the copy reading it finished.
-// Device buffers are the caller's.
+// The engine owns only host memory: pinned staging for the block tables, the
+// copy-on-write block pairs and the prompts' slot mappings (two table / pair
+// buffers, a ring of four slot buffers), each reused only after an event shows
+// that the copy reading it finished.  Device buffers are the caller's.
+//
+// Parallel sampling (kasblo.com "vLLMとは？", section "block共有とAutomatic
+// Prefix Caching"): decode_engine_fork starts a sequence that shares all of
+// another's blocks; each step grows the batch with copy-on-write and copies
+// the shared blocks that are about to be written before the step's append.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -32,6 +37,7 @@ struct pkv_decode_engine {
   std::vector<int64_t> remaining;        // tokens still to generate
   int32_t* tables_h[2] = {nullptr, nullptr};
   int32_t* lens_h[2] = {nullptr, nullptr};
+  int32_t* pairs_h[2] = {nullptr, nullptr};
   cudaEvent_t copied[2] = {nullptr, nullptr};
   bool pending[2] = {false, false};
   int parity = 0;
@@ -47,6 +53,7 @@ struct pkv_decode_engine {
       if (copied[i]) cudaEventSynchronize(copied[i]), cudaEventDestroy(copied[i]);
       if (tables_h[i]) cudaFreeHost(tables_h[i]);
       if (lens_h[i]) cudaFreeHost(lens_h[i]);
+      if (pairs_h[i]) cudaFreeHost(pairs_h[i]);
     }
     for (int i = 0; i < kSlotRing; ++i) {
       if (adm_ev[i]) cudaEventSynchronize(adm_ev[i]), cudaEventDestroy(adm_ev[i]);
@@ -81,6 +88,8 @@ pkv_decode_engine* decode_engine_create(pkv_block_allocator* alloc, int32_t max_
   for (int i = 0; i < 2 && ok; ++i) {
     ok = cudaHostAlloc(reinterpret_cast<void**>(&e->tables_h[i]), tbl, cudaHostAllocDefault) == cudaSuccess &&
          cudaHostAlloc(reinterpret_cast<void**>(&e->lens_h[i]), max_batch * sizeof(int32_t),
+                       cudaHostAllocDefault) == cudaSuccess &&
+         cudaHostAlloc(reinterpret_cast<void**>(&e->pairs_h[i]), 2 * max_batch * sizeof(int32_t),
                        cudaHostAllocDefault) == cudaSuccess &&
          cudaEventCreateWithFlags(&e->copied[i], cudaEventDisableTiming) == cudaSuccess;
   }
@@ -145,27 +154,60 @@ int decode_engine_admit(pkv_decode_engine* e, int32_t prompt_tokens, int32_t gen
   return PKV_OK;
 }
 
-int decode_engine_step(pkv_decode_engine* e, int32_t* tables_dev, int32_t* lens_dev, const void* q,
-                       const void* k_new, const void* v_new, void* k_cache, void* v_cache, float scale, void* out,
-                       void* workspace, size_t workspace_bytes, const pkv_dims* dims, void* stream) {
+int decode_engine_fork(pkv_decode_engine* e, int32_t src_slot, int32_t gen_tokens, int32_t* batch_slot) {
+  if (!e || !batch_slot || gen_tokens < 1 || src_slot < 0 || src_slot >= e->max_batch || e->seq[src_slot] < 0)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "decode_engine_fork: bad argument");
+  *batch_slot = -1;
+  const int32_t src = e->seq[src_slot];
+  const int32_t len = block_allocator_seq_len(e->alloc, src);
+  if (static_cast<int64_t>(len) + gen_tokens > static_cast<int64_t>(e->max_blocks) * kBlockSize)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "decode_engine_fork: length + generation exceed max_blocks_per_seq");
+  int32_t slot = -1;
+  for (int32_t i = 0; i < e->max_batch; ++i)
+    if (e->seq[i] < 0) {
+      slot = i;
+      break;
+    }
+  if (slot < 0) return pkv_fail(PKV_ERR_NO_BLOCKS, "decode_engine_fork: no free batch slot");
+  int32_t sid;
+  const int rc = block_allocator_fork(e->alloc, src, len, &sid);
+  if (rc != PKV_OK) return rc;
+  e->seq[slot] = sid;
+  e->remaining[slot] = gen_tokens;
+  *batch_slot = slot;
+  return PKV_OK;
+}
+
+int decode_engine_step(pkv_decode_engine* e, int32_t* tables_dev, int32_t* lens_dev, int32_t* copy_pairs_dev,
+                       const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache, float scale,
+                       void* out, void* workspace, size_t workspace_bytes, const pkv_dims* dims, void* stream) {
   if (!e || !tables_dev || !lens_dev || !dims) return pkv_fail(PKV_ERR_INVALID_ARG, "decode_engine_step: bad argument");
   if (dims->num_seqs != e->max_batch || dims->max_blocks_per_seq != e->max_blocks)
     return pkv_fail(PKV_ERR_INVALID_ARG, "decode_engine_step: dims must match the engine's batch and table width");
   const int i = e->parity;
-  if (e->pending[i]) cudaEventSynchronize(e->copied[i]);  // the copy that last read this buffer is done
-  int rc = block_allocator_step_batch(e->alloc, e->seq.data(), e->max_batch, e->max_blocks, e->tables_h[i],
-                                      e->lens_h[i]);
+  if (e->pending[i]) cudaEventSynchronize(e->copied[i]);  // the copies that last read these buffers are done
+  int32_t ncopy = 0;
+  int rc = block_allocator_step_batch_cow(e->alloc, e->seq.data(), e->max_batch, e->max_blocks, e->tables_h[i],
+                                          e->lens_h[i], e->pairs_h[i], &ncopy);
   if (rc != PKV_OK) return rc;
+  if (ncopy > 0 && !copy_pairs_dev)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "decode_engine_step: shared blocks need copying but copy_pairs_dev is NULL");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t tbl = static_cast<size_t>(e->max_batch) * e->max_blocks * sizeof(int32_t);
   cudaError_t ce = cudaMemcpyAsync(tables_dev, e->tables_h[i], tbl, cudaMemcpyHostToDevice, s);
   if (ce == cudaSuccess)
     ce = cudaMemcpyAsync(lens_dev, e->lens_h[i], e->max_batch * sizeof(int32_t), cudaMemcpyHostToDevice, s);
+  if (ce == cudaSuccess && ncopy > 0)
+    ce = cudaMemcpyAsync(copy_pairs_dev, e->pairs_h[i], 2 * ncopy * sizeof(int32_t), cudaMemcpyHostToDevice, s);
   if (ce == cudaSuccess) ce = cudaEventRecord(e->copied[i], s);
   if (ce != cudaSuccess) return cuda_err(ce, "decode_engine_step: table copy");
   e->pending[i] = true;
   e->last = i;
   e->parity ^= 1;
+  if (ncopy > 0) {
+    rc = paged_kv_copy_blocks(k_cache, v_cache, copy_pairs_dev, ncopy, dims, 2, stream);
+    if (rc != PKV_OK) return rc;
+  }
   return paged_decode_step(q, k_new, v_new, k_cache, v_cache, tables_dev, lens_dev, scale, out, 0, workspace,
                            workspace_bytes, dims, stream);
 }

@@ -14,6 +14,9 @@ waiting ones enter at every iteration):
 * step(): every active sequence gets one token: the engine grows each
   sequence (a new block at a block boundary), ships the block tables and runs
   one paged_decode_step (append + attention) -- one native call per step;
+* fork(): parallel sampling -- a new sequence sharing all of an active one's
+  blocks; the shared block a step writes into is copied first (copy-on-write,
+  kasblo.com "vLLMとは？", section "block共有とAutomatic Prefix Caching");
 * finish_step(): sequences whose generation budget is spent free their blocks.
 
 Empty batch slots have context length 0 (zero output, nothing appended).
@@ -50,6 +53,7 @@ class DecodeLoop:
         self.tables = torch.full((max_batch, self.max_blocks), -1, dtype=torch.int32, device=self.device)
         self.lens = torch.zeros(max_batch, dtype=torch.int32, device=self.device)
         self.slot_staging = torch.empty(4 * self.max_blocks * BLOCK_SIZE, dtype=torch.int32, device=self.device)
+        self.copy_pairs = torch.empty(max_batch, 2, dtype=torch.int32, device=self.device)
         self.out = torch.empty(max_batch, num_q_heads, head_dim, dtype=dtype, device=self.device)
         probe_q = torch.empty(max_batch, num_q_heads, head_dim, dtype=dtype, device=self.device)
         self.workspace = api.make_workspace(probe_q, self.k_cache, self.tables, 0)
@@ -107,6 +111,16 @@ class DecodeLoop:
         api._check(rc, "decode_engine_admit")
         return int(self._slot.value)
 
+    def fork(self, src_slot: int, gen_len: int) -> Optional[int]:
+        """Parallel sampling: a new sequence sharing every block of the one in
+        src_slot, running gen_len steps.  Returns its batch slot, or None when
+        no slot is free."""
+        rc = lib().decode_engine_fork(self._eng, int(src_slot), int(gen_len), ctypes.byref(self._slot))
+        if rc == -5:
+            return None
+        api._check(rc, "decode_engine_fork")
+        return int(self._slot.value)
+
     # ------------------------------------------------------------------ one step
 
     def step(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor) -> torch.Tensor:
@@ -122,7 +136,8 @@ class DecodeLoop:
                 raise ValueError("q / k_new / v_new must cover every batch slot")
             P = ctypes.c_void_p
             ws = self.workspace
-            self._step_args = (self._eng, P(self.tables.data_ptr()), P(self.lens.data_ptr()), P(q.data_ptr()),
+            self._step_args = (self._eng, P(self.tables.data_ptr()), P(self.lens.data_ptr()),
+                               P(self.copy_pairs.data_ptr()), P(q.data_ptr()),
                                P(k_new.data_ptr()), P(v_new.data_ptr()), P(self.k_cache.data_ptr()),
                                P(self.v_cache.data_ptr()), ctypes.c_float(1.0 / math.sqrt(self.D)),
                                P(self.out.data_ptr()), P(ws.data_ptr() if ws is not None else 0),

@@ -136,3 +136,74 @@ def test_decode_loop_end_to_end_against_the_oracle():
     # every block is either free or held by exactly the live sequences' tables
     live_blocks = set(int(x) for s in range(B) if loop.seq[s] >= 0 for x in tables[s, :math.ceil(lens[s] / 16)])
     assert loop.alloc.num_free + len(live_blocks) == 40
+
+
+@pytest.mark.gpu
+def test_decode_loop_with_parallel_sampling_against_the_oracle():
+    """Forks (parallel samples) of live sequences share their blocks; the loop
+    copies a shared block before a step writes into it.  Every sequence must
+    read back exactly its own history and the output match the oracle."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_26_gb300.loop import DecodeLoop
+
+    dev = torch.device("cuda")
+    Hq, Hk, D, B = 8, 2, 128, 8
+    rng = np.random.default_rng(1)
+    g = torch.Generator(device=dev).manual_seed(1)
+    loop = DecodeLoop(num_blocks=80, num_q_heads=Hq, num_kv_heads=Hk, head_dim=D, max_batch=B,
+                      max_context=160, dtype=torch.bfloat16, device=dev, seed=5)
+    history = {}
+
+    def bits(t):
+        return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+    forks = 0
+    q = out = None
+    for step in range(50):
+        while loop.free_slots().size:
+            active = loop.active_slots()
+            if active.size and rng.random() < 0.6:
+                src = int(rng.choice(active))
+                slot = loop.fork(src, int(rng.integers(3, 25)))
+                if slot is None:
+                    break
+                history[int(loop.seq[slot])] = list(history[int(loop.seq[src])])
+                forks += 1
+            else:
+                P = int(rng.integers(1, 40))
+                pk = torch.randn(P, Hk, D, generator=g, device=dev).bfloat16()
+                pv = torch.randn(P, Hk, D, generator=g, device=dev).bfloat16()
+                slot = loop.admit(pk, pv, int(rng.integers(3, 25)))
+                if slot is None:
+                    break
+                history[int(loop.seq[slot])] = [(r[0], r[1]) for r in zip(bits(pk), bits(pv))]
+        q = torch.randn(B, Hq, D, generator=g, device=dev).bfloat16()
+        kn = torch.randn(B, Hk, D, generator=g, device=dev).bfloat16()
+        vn = torch.randn(B, Hk, D, generator=g, device=dev).bfloat16()
+        out = loop.step(q, kn, vn)
+        for slot in loop.active_slots():
+            history[int(loop.seq[slot])].append((bits(kn[slot]), bits(vn[slot])))
+        if step < 49:
+            loop.finish_step()
+    torch.cuda.synchronize()
+    assert forks > B
+    kc, vc = bits(loop.k_cache), bits(loop.v_cache)
+    tables, lens = loop.tables.cpu().numpy(), loop.lens.cpu().numpy()
+    got = oracle.widen(bits(out), "bf16")
+    for slot in range(B):
+        sid = int(loop.seq[slot])
+        if sid < 0:
+            continue
+        hist = history[sid]
+        L = len(hist)
+        assert lens[slot] == L
+        for kv in range(Hk):
+            k_rec = np.stack([h[0][kv] for h in hist])
+            v_rec = np.stack([h[1][kv] for h in hist])
+            assert np.array_equal(oracle.gather_kv(kc, tables[slot], L, kv, 16), k_rec)
+            assert np.array_equal(oracle.gather_kv(vc, tables[slot], L, kv, 16), v_rec)
+            for h in range(kv * (Hq // Hk), (kv + 1) * (Hq // Hk)):
+                ref = oracle.attend_one(oracle.widen(bits(q[slot, h]), "bf16"), oracle.widen(k_rec, "bf16"),
+                                        oracle.widen(v_rec, "bf16"), 1 / math.sqrt(D))[0]
+                assert np.all(np.abs(got[slot, h] - ref) <= 2e-3 + 1e-2 * np.abs(ref))
