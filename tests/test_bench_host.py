@@ -94,10 +94,13 @@ def test_ncu_traffic_is_dropped_when_the_kernel_changed(tmp_path, monkeypatch):
     (tmp_path / "profiles").mkdir()
     csrc = tmp_path / "paged_kv_cache_26_gb300" / "csrc"
     csrc.mkdir(parents=True)
-    (csrc / "k.cu").write_text("one")
+    for name in bench.DECODE_KERNEL_SOURCES:
+        (csrc / name).write_text("one")
     h = bench.kernel_source_hash()
     (tmp_path / "profiles" / "decode_persistent_kernel_x.md").write_text(
         f"source_sha256: {h}\ntraffic_bytes_per_launch: 123\n")
     assert bench.ncu_traffic("x") == 123.0
-    (csrc / "k.cu").write_text("two")
+    (csrc / "other_kernel.cuh").write_text("a kernel the profile does not describe")
+    assert bench.ncu_traffic("x") == 123.0
+    (csrc / bench.DECODE_KERNEL_SOURCES[0]).write_text("two")
     assert bench.ncu_traffic("x") is None
