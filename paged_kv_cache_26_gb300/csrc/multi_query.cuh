@@ -28,7 +28,7 @@ namespace pkv {
 
 constexpr int kMaxQueryLen = 8;
 constexpr int kMaxQueryWarps = kMaxGroup * kMaxQueryLen / 8;  // 8 consumer warps
-constexpr int kMultiStages = 8;
+constexpr int kMultiStages = 4;
 
 // Token (b, i) of k_new / v_new ([B][q_len][Hkv][D]) goes to position
 // context_lens[b] - q_len + i through the block table (nothing for a negative
