@@ -870,8 +870,17 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
 
   // First window of the head (block-table and query inputs only), then wait:
   // from here on this grid reads the cache and writes the workspace and out,
-  // which the previous kernels in the stream (append, merge) touch.
+  // which the previous kernels in the stream (append, merge) touch.  Before
+  // the wait, the tiles of the first stages are only prefetched into L2: a
+  // prefetch moves no data into this grid's view, and the loads after the
+  // wait see every earlier write, so they just find the lines in L2.
   if (ip < seg_e) fill_window();
+  if (lane < SW * NPS && win_s + lane < win_e && wrow >= 0) {
+    constexpr int kCacheRowBytes = F8 ? D : 2 * D;
+    const int64_t off = static_cast<int64_t>(wrow) * kCacheRowBytes;
+    prefetch_l2_bulk(static_cast<const uint8_t*>(a.k_cache_w) + off, Tile::kTileBytes);
+    prefetch_l2_bulk(static_cast<const uint8_t*>(a.v_cache_w) + off, Tile::kTileBytes);
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- consume side
