@@ -12,12 +12,15 @@
 //                              of positions L - q_len .. L - 1 of its table.
 //  decode_multi_query_kernel-- one CTA per (split, KV head, sequence).  A TMA
 //                              producer warp streams the split's blocks through
-//                              a ring; NQ = ceil(g * q_len / 8) consumer warps
-//                              each own 8 of the unit's g * q_len query rows and
-//                              all of them read every staged block, so K/V leave
-//                              HBM once for all the new tokens of the group.
-//                              Rows are ordered token-major (row r = token
-//                              r / g, head r % g), the order of q in memory.
+//                              a ring; the consumer warps each own 16 (or, for
+//                              at most 8 rows in all, 8) of the unit's
+//                              g * q_len query rows and all of them read every
+//                              staged block, so K/V leave HBM once for all the
+//                              new tokens of the group.  Rows are ordered
+//                              token-major (row r = token r / g, head r % g),
+//                              the order of q in memory.  With more than 8 rows
+//                              the query rows are the mma M dimension (16 per
+//                              warp), unlike the one-token kernels.
 // The split partials are combined by merge_split_kernel with q_len * Hq rows
 // per sequence.
 #pragma once
@@ -27,7 +30,8 @@
 namespace pkv {
 
 constexpr int kMaxQueryLen = 8;
-constexpr int kMaxQueryWarps = kMaxGroup * kMaxQueryLen / 8;  // 8 consumer warps
+constexpr int kQueryRowsPerWarp = 16;
+constexpr int kMaxQueryWarps = kMaxGroup * kMaxQueryLen / kQueryRowsPerWarp;  // 4 consumer warps
 constexpr int kMultiStages = 4;
 
 // Token (b, i) of k_new / v_new ([B][q_len][Hkv][D]) goes to position
@@ -162,10 +166,179 @@ struct WarpAttnCausal : WarpAttn<T, D> {
   }
 };
 
+// ldmatrix: four 8x8 matrices of 16-bit elements from shared memory; lane l
+// supplies the address of row l % 8 of matrix l / 8, and r[m] receives this
+// lane's part of matrix m (row lane / 4, elements 2 (lane % 4) and + 1; with
+// .trans, of the transposed matrix).
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// One warp's attention state for 16 query rows (rows gid and gid + 8 of the
+// mma layout, gid = lane / 4, c = lane % 4) over the blocks of one unit.
+//  * S = Q K^T per block: M = the 16 rows, N = 2 tiles of 8 tokens, K = head_dim
+//    in steps of 16; K fragments come from the swizzled tile with ldmatrix.
+//  * The score accumulators are already the A fragments of P V (rows gid,
+//    gid + 8; tokens 2c, 2c+1 and 2c+8, 2c+9), so P never leaves registers.
+//  * O = P V: M = the 16 rows, N = head_dim in tiles of 8, K = the 16 tokens;
+//    V fragments come with ldmatrix.trans.  The lane holds O for rows gid and
+//    gid + 8, columns 8 nd + 2c and + 1.
+//  * Each row has its own causal limit: the first vc0 (vc1) tokens of a block
+//    are visible to row gid (gid + 8).  A row with nothing visible so far keeps
+//    m = -inf and l = 0; O is rescaled only when a row's maximum grows.
+//  * bf16 weights enter P V as two bf16 terms, p = hi + lo (fp16: one term).
+template <typename T, int D>
+struct WarpAttnRows {
+  static constexpr int kKSteps = D / 16;
+  static constexpr int kNTiles = D / 8;
+  uint32_t qa[kKSteps][4];
+  float o[kNTiles][4];
+  float m0, m1, l0, l1;
+
+  __device__ __forceinline__ void reset() {
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < kNTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  }
+
+  // rows gid (row0) and gid + 8 (row1) of q; null: a padding row of zeros.
+  __device__ __forceinline__ void load_q(const T* row0, const T* row1, int lane) {
+    const int c = lane & 3;
+#pragma unroll
+    for (int kk = 0; kk < kKSteps; ++kk) {
+      const int d = 16 * kk + 2 * c;
+      qa[kk][0] = row0 ? __ldg(reinterpret_cast<const uint32_t*>(row0 + d)) : 0u;
+      qa[kk][1] = row1 ? __ldg(reinterpret_cast<const uint32_t*>(row1 + d)) : 0u;
+      qa[kk][2] = row0 ? __ldg(reinterpret_cast<const uint32_t*>(row0 + d + 8)) : 0u;
+      qa[kk][3] = row1 ? __ldg(reinterpret_cast<const uint32_t*>(row1 + d + 8)) : 0u;
+    }
+  }
+
+  __device__ __forceinline__ void block(uint32_t ks, uint32_t vs, int valid_v, int vc0, int vc1, float scale_log2,
+                                        int lane) {
+    const int gid = lane >> 2, c = lane & 3;
+    const int mi = lane >> 3, rr = lane & 7;  // the matrix and row this lane addresses
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int kk = 0; kk < kKSteps; ++kk) {
+      // matrices: (tokens 0-7, d lo), (tokens 0-7, d hi), (tokens 8-15, d lo), (tokens 8-15, d hi)
+      const int token = 8 * (mi >> 1) + rr;
+      const int chunk = 2 * (kk & 3) + (mi & 1);
+      uint32_t kb[4];
+      ldmatrix_x4(ks + (kk >> 2) * 2048 + token * 128 + ((chunk ^ rr) << 4), kb);
+      mma16816<T>(s[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], kb[0], kb[1]);
+      mma16816<T>(s[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], kb[2], kb[3]);
+    }
+    float x[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int t = 8 * nt + 2 * c + e;
+        x[nt][e] = t < vc0 ? s[nt][e] * scale_log2 : -INFINITY;
+        x[nt][2 + e] = t < vc1 ? s[nt][2 + e] * scale_log2 : -INFINITY;
+      }
+    }
+    float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+    float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    if (__any_sync(0xffffffffu, mn0 > m0 || mn1 > m1)) {
+      const float al0 = mn0 > m0 ? exp2f(m0 - mn0) : 1.f, al1 = mn1 > m1 ? exp2f(m1 - mn1) : 1.f;
+      l0 *= al0;
+      l1 *= al1;
+#pragma unroll
+      for (int nd = 0; nd < kNTiles; ++nd) {
+        o[nd][0] *= al0;
+        o[nd][1] *= al0;
+        o[nd][2] *= al1;
+        o[nd][3] *= al1;
+      }
+      m0 = mn0;
+      m1 = mn1;
+    }
+    const float r0 = m0 == -INFINITY ? 0.f : m0, r1 = m1 == -INFINITY ? 0.f : m1;  // nothing visible yet
+    float p[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      p[nt][0] = exp2f(x[nt][0] - r0);
+      p[nt][1] = exp2f(x[nt][1] - r0);
+      p[nt][2] = exp2f(x[nt][2] - r1);
+      p[nt][3] = exp2f(x[nt][3] - r1);
+    }
+    uint32_t ph[4], pl[4] = {0u, 0u, 0u, 0u};
+    ph[0] = pack2<T>(p[0][0], p[0][1]);  // row gid, tokens 2c, 2c+1
+    ph[1] = pack2<T>(p[0][2], p[0][3]);  // row gid + 8
+    ph[2] = pack2<T>(p[1][0], p[1][1]);  // row gid, tokens 2c+8, 2c+9
+    ph[3] = pack2<T>(p[1][2], p[1][3]);
+    if constexpr (MmaKind<T>::kBf16) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 h = unpack2<T>(ph[i]);
+        const int nt = i >> 1, e = (i & 1) * 2;
+        pl[i] = pack2<T>(p[nt][e] - h.x, p[nt][e + 1] - h.y);
+      }
+      l0 += (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+      l1 += (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
+    } else {
+      const float2 a = unpack2<T>(ph[0]), b = unpack2<T>(ph[1]), cc = unpack2<T>(ph[2]), dd = unpack2<T>(ph[3]);
+      l0 += (a.x + a.y) + (cc.x + cc.y);  // the rounded weights the product uses
+      l1 += (b.x + b.y) + (dd.x + dd.y);
+    }
+    // V rows at or past valid_v read as zeros (never 0 * NaN).
+    const uint32_t keep0 = (2 * c < valid_v ? 0x0000FFFFu : 0u) | (2 * c + 1 < valid_v ? 0xFFFF0000u : 0u);
+    const uint32_t keep1 = (2 * c + 8 < valid_v ? 0x0000FFFFu : 0u) | (2 * c + 9 < valid_v ? 0xFFFF0000u : 0u);
+#pragma unroll
+    for (int pr = 0; pr < kNTiles / 2; ++pr) {
+      // matrices: (tokens 0-7, d tile 2pr), (tokens 8-15, 2pr), (0-7, 2pr+1), (8-15, 2pr+1)
+      const int nd = 2 * pr + (mi >> 1);
+      const int token = 8 * (mi & 1) + rr;
+      uint32_t vb[4];
+      ldmatrix_x4_trans(vs + (nd >> 3) * 2048 + token * 128 + (((nd & 7) ^ rr) << 4), vb);
+      if (valid_v < kBlockSize) {
+        vb[0] &= keep0;
+        vb[1] &= keep1;
+        vb[2] &= keep0;
+        vb[3] &= keep1;
+      }
+      mma16816<T>(o[2 * pr], ph[0], ph[1], ph[2], ph[3], vb[0], vb[1]);
+      mma16816<T>(o[2 * pr + 1], ph[0], ph[1], ph[2], ph[3], vb[2], vb[3]);
+      if constexpr (MmaKind<T>::kBf16) {
+        mma16816<T>(o[2 * pr], pl[0], pl[1], pl[2], pl[3], vb[0], vb[1]);
+        mma16816<T>(o[2 * pr + 1], pl[0], pl[1], pl[2], pl[3], vb[2], vb[3]);
+      }
+    }
+  }
+
+  // Complete the row sums (each lane summed its own columns).
+  __device__ __forceinline__ void finish_sums() {
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+  }
+};
+
 // args.num_q_heads = Hq; q / out are T[B][q_len][Hq][D]; split partials are
 // indexed by row = (b * q_len + i) * Hq + h (args.num_splits, args.split_blocks).
-template <typename T, int D, int S>
-__global__ void __launch_bounds__((kMaxQueryWarps + 1) * 32)
+// ROWS: query rows in the mma M dimension, 16 per warp (WarpAttnRows), for
+// more than 8 rows per KV head; else 8 rows per warp in the N dimension
+// (WarpAttnCausal), which pads less when the rows are few.
+template <typename T, int D, int S, bool ROWS>
+__global__ void __launch_bounds__((ROWS ? kMaxQueryWarps : 1) * 32 + 32)
     decode_multi_query_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                               const DecodeArgs args, int32_t q_len) {
   using Shape = TileShape<D>;
@@ -185,15 +358,16 @@ __global__ void __launch_bounds__((kMaxQueryWarps + 1) * 32)
   const int nblk = (ctx + kBlockSize - 1) / kBlockSize;
   const int blk0 = split * args.split_blocks;
   const int nb = min(nblk, blk0 + args.split_blocks) - blk0;
+  auto row_index = [&](int r) -> int64_t {  // output row of query row r
+    return (static_cast<int64_t>(b) * n + r / g) * Hq + kvh * g + r % g;
+  };
 
   if (nb <= 0) {
     // Empty split.  In one pass this is an empty context: zero rows.
     if (args.num_splits == 1) {
       for (int idx = threadIdx.x; idx < nrows * D; idx += blockDim.x) {
         const int r = idx / D, d = idx - r * D;
-        T* out = static_cast<T*>(args.out) +
-                 ((static_cast<int64_t>(b) * n + r / g) * Hq + kvh * g + r % g) * D + d;
-        *out = T(0.0f);
+        static_cast<T*>(args.out)[row_index(r) * D + d] = T(0.0f);
       }
     }
     return;
@@ -251,68 +425,111 @@ __global__ void __launch_bounds__((kMaxQueryWarps + 1) * 32)
 
   // -------------------------------------------------------------- consumers
   const int gid = lane >> 2, c = lane & 3;
-  WarpAttnCausal<T, D> at;
-  {
-    const int rq = 8 * warp + gid;  // the query row this lane loads
-    const T* rowp = rq < nrows ? static_cast<const T*>(args.q) +
-                                     ((static_cast<int64_t>(b) * n + rq / g) * Hq + kvh * g + rq % g) * D
-                               : nullptr;
-    at.load_q_row(rowp, lane);
-  }
-  at.reset();
-  // Last position each of this lane's two columns attends to (-1: padding row).
-  const int r0 = 8 * warp + 2 * c, r1 = r0 + 1;
-  const int lim0 = r0 < nrows ? ctx - n + r0 / g : -1;
-  const int lim1 = r1 < nrows ? ctx - n + r1 / g : -1;
-  bool ok = true;
-  for (int i = 0; i < nb; ++i) {
-    if (*reinterpret_cast<volatile int*>(&s_abort)) {
-      ok = false;
-      break;
+  if constexpr (ROWS) {
+    const int ra = kQueryRowsPerWarp * warp + gid, rb = ra + 8;  // this lane's two rows
+    WarpAttnRows<T, D> at;
+    {
+      const T* q = static_cast<const T*>(args.q);
+      at.load_q(ra < nrows ? q + row_index(ra) * D : nullptr, rb < nrows ? q + row_index(rb) * D : nullptr, lane);
     }
-    const int st = i % S;
-    if (!mbar_wait(smem_u32(&full_bar[st]), (i / S) & 1)) {
-      s_abort = 1;
-      ok = false;
-      break;
+    at.reset();
+    // Last position each row attends to (-1: a padding row).
+    const int lim_a = ra < nrows ? ctx - n + ra / g : -1;
+    const int lim_b = rb < nrows ? ctx - n + rb / g : -1;
+    for (int i = 0; i < nb; ++i) {
+      if (*reinterpret_cast<volatile int*>(&s_abort)) return;
+      const int st = i % S;
+      if (!mbar_wait(smem_u32(&full_bar[st]), (i / S) & 1)) {
+        s_abort = 1;
+        return;
+      }
+      const int t0 = (blk0 + i) * kBlockSize;
+      const int vc0 = max(0, min(kBlockSize, lim_a + 1 - t0));
+      const int vc1 = max(0, min(kBlockSize, lim_b + 1 - t0));
+      const uint32_t ks = smem_u32(smem + st * Shape::kStageBytes);
+      at.block(ks, ks + Shape::kTileBytes, min(kBlockSize, ctx - t0), vc0, vc1, args.scale_log2, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));  // this warp is done with the stage
     }
-    const int t0 = (blk0 + i) * kBlockSize;
-    const int vc0 = max(0, min(kBlockSize, lim0 + 1 - t0));
-    const int vc1 = max(0, min(kBlockSize, lim1 + 1 - t0));
-    const uint8_t* ks = smem + st * Shape::kStageBytes;
-    at.block_causal(ks, ks + Shape::kTileBytes, min(kBlockSize, ctx - t0), vc0, vc1, args.scale_log2, lane);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));  // this warp is done with the stage
-  }
-  if (!ok) return;
-  at.finish_sums();
+    at.finish_sums();
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int r = r0 + e;
-    if (r >= nrows) continue;
-    const float l = e ? at.l1 : at.l0;
-    const float inv = l > 0.f ? 1.0f / l : 0.f;  // no visible token: a zero row
-    const int64_t orow = (static_cast<int64_t>(b) * n + r / g) * Hq + kvh * g + r % g;
-    if (args.num_splits == 1) {
-      T* dst = static_cast<T*>(args.out) + orow * D;
+    for (int half = 0; half < 2; ++half) {
+      const int r = half ? rb : ra;
+      if (r >= nrows) continue;
+      const float l = half ? at.l1 : at.l0;
+      const float inv = l > 0.f ? 1.0f / l : 0.f;  // no visible token: a zero row
+      const int64_t orow = row_index(r);
+      if (args.num_splits == 1) {
+        T* dst = static_cast<T*>(args.out) + orow * D + 2 * c;
 #pragma unroll
-      for (int kk = 0; kk < WarpAttn<T, D>::kChunks; ++kk) {
-        float v[8];
-        at.chunk_values(e, kk, inv, v);
-        *reinterpret_cast<uint4*>(dst + WarpAttn<T, D>::chunk_dim(lane, kk)) = pack8<T>(v);
+        for (int nd = 0; nd < WarpAttnRows<T, D>::kNTiles; ++nd)
+          *reinterpret_cast<uint32_t*>(dst + 8 * nd) =
+              pack2<T>(at.o[nd][2 * half] * inv, at.o[nd][2 * half + 1] * inv);
+      } else {
+        const int64_t prow = orow * args.num_splits + split;
+        float* dst = args.part_o + prow * D + 2 * c;
+#pragma unroll
+        for (int nd = 0; nd < WarpAttnRows<T, D>::kNTiles; ++nd)
+          *reinterpret_cast<float2*>(dst + 8 * nd) =
+              make_float2(at.o[nd][2 * half] * inv, at.o[nd][2 * half + 1] * inv);
+        if (c == 0) args.part_lse[prow] = l > 0.f ? (half ? at.m1 : at.m0) + log2f(l) : -INFINITY;
       }
-    } else {
-      const int64_t prow = orow * args.num_splits + split;
-      float* dst = args.part_o + prow * D;
-#pragma unroll
-      for (int kk = 0; kk < WarpAttn<T, D>::kChunks; ++kk) {
-        float v[8];
-        at.chunk_values(e, kk, inv, v);
-        float4* d4 = reinterpret_cast<float4*>(dst + WarpAttn<T, D>::chunk_dim(lane, kk));
-        d4[0] = make_float4(v[0], v[1], v[2], v[3]);
-        d4[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+  } else {
+    WarpAttnCausal<T, D> at;
+    {
+      const int rq = 8 * warp + gid;  // the query row this lane loads
+      at.load_q_row(rq < nrows ? static_cast<const T*>(args.q) + row_index(rq) * D : nullptr, lane);
+    }
+    at.reset();
+    // Last position each of this lane's two columns attends to (-1: padding row).
+    const int r0 = 8 * warp + 2 * c, r1 = r0 + 1;
+    const int lim0 = r0 < nrows ? ctx - n + r0 / g : -1;
+    const int lim1 = r1 < nrows ? ctx - n + r1 / g : -1;
+    for (int i = 0; i < nb; ++i) {
+      if (*reinterpret_cast<volatile int*>(&s_abort)) return;
+      const int st = i % S;
+      if (!mbar_wait(smem_u32(&full_bar[st]), (i / S) & 1)) {
+        s_abort = 1;
+        return;
       }
-      if (gid == 0) args.part_lse[prow] = l > 0.f ? (e ? at.m1 : at.m0) + log2f(l) : -INFINITY;
+      const int t0 = (blk0 + i) * kBlockSize;
+      const int vc0 = max(0, min(kBlockSize, lim0 + 1 - t0));
+      const int vc1 = max(0, min(kBlockSize, lim1 + 1 - t0));
+      const uint8_t* ks = smem + st * Shape::kStageBytes;
+      at.block_causal(ks, ks + Shape::kTileBytes, min(kBlockSize, ctx - t0), vc0, vc1, args.scale_log2, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));  // this warp is done with the stage
+    }
+    at.finish_sums();
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = r0 + e;
+      if (r >= nrows) continue;
+      const float l = e ? at.l1 : at.l0;
+      const float inv = l > 0.f ? 1.0f / l : 0.f;  // no visible token: a zero row
+      const int64_t orow = row_index(r);
+      if (args.num_splits == 1) {
+        T* dst = static_cast<T*>(args.out) + orow * D;
+#pragma unroll
+        for (int kk = 0; kk < WarpAttn<T, D>::kChunks; ++kk) {
+          float v[8];
+          at.chunk_values(e, kk, inv, v);
+          *reinterpret_cast<uint4*>(dst + WarpAttn<T, D>::chunk_dim(lane, kk)) = pack8<T>(v);
+        }
+      } else {
+        const int64_t prow = orow * args.num_splits + split;
+        float* dst = args.part_o + prow * D;
+#pragma unroll
+        for (int kk = 0; kk < WarpAttn<T, D>::kChunks; ++kk) {
+          float v[8];
+          at.chunk_values(e, kk, inv, v);
+          float4* d4 = reinterpret_cast<float4*>(dst + WarpAttn<T, D>::chunk_dim(lane, kk));
+          d4[0] = make_float4(v[0], v[1], v[2], v[3]);
+          d4[1] = make_float4(v[4], v[5], v[6], v[7]);
+        }
+        if (gid == 0) args.part_lse[prow] = l > 0.f ? (e ? at.m1 : at.m0) + log2f(l) : -INFINITY;
+      }
     }
   }
 }

@@ -569,10 +569,14 @@ int decode_multi_impl(const void* q, const void* k_new, const void* v_new, void*
   args.num_blocks = d->num_blocks;
   args.num_splits = splits;
   args.split_blocks = split_blocks;
-  const int nq = (args.group * q_len + 7) / 8;
+  // More than 8 query rows per KV head: 16 rows per warp in the mma M
+  // dimension; else one warp with the rows in N.
+  const bool rows_in_m = args.group * q_len > 8;
+  const int nq = rows_in_m ? (args.group * q_len + pkv::kQueryRowsPerWarp - 1) / pkv::kQueryRowsPerWarp : 1;
   const dim3 grid(splits, d->num_kv_heads, d->num_seqs);
-  auto launch = [&](auto kern, auto merge, int stage_bytes, auto typed_out) -> int {
+  auto launch = [&](auto kern_rows, auto kern_cols, auto merge, int stage_bytes, auto typed_out) -> int {
     const int smem = pkv::kMultiStages * stage_bytes + 1024;
+    auto kern = rows_in_m ? kern_rows : kern_cols;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute(decode_multi_query_kernel)");
     kern<<<grid, (nq + 1) * 32, smem, stream>>>(mk, mv, args, q_len);
@@ -590,17 +594,21 @@ int decode_multi_impl(const void* q, const void* k_new, const void* v_new, void*
   };
   if (d->head_dim == 128) {
     if (bf16)
-      return launch(pkv::decode_multi_query_kernel<__nv_bfloat16, 128, pkv::kMultiStages>,
+      return launch(pkv::decode_multi_query_kernel<__nv_bfloat16, 128, pkv::kMultiStages, true>,
+                    pkv::decode_multi_query_kernel<__nv_bfloat16, 128, pkv::kMultiStages, false>,
                     pkv::merge_split_kernel<__nv_bfloat16, 128>, pkv::TileShape<128>::kStageBytes,
                     static_cast<__nv_bfloat16*>(nullptr));
-    return launch(pkv::decode_multi_query_kernel<__half, 128, pkv::kMultiStages>, pkv::merge_split_kernel<__half, 128>,
+    return launch(pkv::decode_multi_query_kernel<__half, 128, pkv::kMultiStages, true>,
+                  pkv::decode_multi_query_kernel<__half, 128, pkv::kMultiStages, false>, pkv::merge_split_kernel<__half, 128>,
                   pkv::TileShape<128>::kStageBytes, static_cast<__half*>(nullptr));
   }
   if (bf16)
-    return launch(pkv::decode_multi_query_kernel<__nv_bfloat16, 64, pkv::kMultiStages>,
+    return launch(pkv::decode_multi_query_kernel<__nv_bfloat16, 64, pkv::kMultiStages, true>,
+                  pkv::decode_multi_query_kernel<__nv_bfloat16, 64, pkv::kMultiStages, false>,
                   pkv::merge_split_kernel<__nv_bfloat16, 64>, pkv::TileShape<64>::kStageBytes,
                   static_cast<__nv_bfloat16*>(nullptr));
-  return launch(pkv::decode_multi_query_kernel<__half, 64, pkv::kMultiStages>, pkv::merge_split_kernel<__half, 64>,
+  return launch(pkv::decode_multi_query_kernel<__half, 64, pkv::kMultiStages, true>,
+                pkv::decode_multi_query_kernel<__half, 64, pkv::kMultiStages, false>, pkv::merge_split_kernel<__half, 64>,
                 pkv::TileShape<64>::kStageBytes, static_cast<__half*>(nullptr));
 }
 
