@@ -410,11 +410,13 @@ def run_ours(args, rank, world, local):
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.time()
+    torch.cuda.nvtx.range_push(f"timed {K} steps")
     start.record(stream)
     for _ in range(K):
         for l in range(nl):
             f_step(*step_args[l])
     end.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     t_wall1 = time.time()
     barrier(world)

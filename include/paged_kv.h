@@ -322,6 +322,14 @@ int paged_kv_slot_mapping_multi(const int32_t* block_tables, const int32_t* cont
 int paged_kv_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs, int32_t num_pairs,
                          const pkv_dims* dims, int32_t cache_elem_bytes, void* stream);
 
+/* Self-test of the kernels' bounded waits (device); no counterpart on the
+ * pages.  Launches one warp that waits on a barrier nothing ever signals: the
+ * wait gives up after its limit (1.5 s), sets the timeout bit of the error
+ * word and the kernel returns, so the next paged_kv_check_status(stream)
+ * returns PKV_ERR_TIMEOUT and the device stays usable.  Lets a caller (and the
+ * tests) check the failure path without a real hang. */
+int paged_kv_selftest_wait(void* stream);
+
 /* Synchronises `stream`, then reads and clears this device's error word.
  * Returns PKV_OK, PKV_ERR_OUT_OF_RANGE, PKV_ERR_TIMEOUT or PKV_ERR_CUDA. */
 int paged_kv_check_status(void* stream);
@@ -451,6 +459,12 @@ void decode_engine_destroy(pkv_decode_engine* e);
 int decode_engine_admit(pkv_decode_engine* e, int32_t prompt_tokens, int32_t gen_tokens, const void* prompt_k,
                         const void* prompt_v, void* k_cache, void* v_cache, int32_t* slot_staging_dev,
                         const pkv_dims* dims, void* stream, int32_t* batch_slot);
+
+/* E4M3 pools: with k_scale / v_scale (float32[num_kv_heads], device, owned by
+ * the caller) set, the engine's pools hold E4M3 codes: admission appends
+ * with paged_kv_append_fp8, steps run paged_decode_step_fp8, and
+ * copy-on-write copies 1-byte elements.  NULL for both: fp16/bf16 pools. */
+int decode_engine_set_kv_scales(pkv_decode_engine* e, const float* k_scale, const float* v_scale);
 
 /* Parallel sampling: a new sequence in a free batch slot that shares every
  * block of the sequence in src_slot (its whole context so far; reference

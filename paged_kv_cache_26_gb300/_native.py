@@ -66,6 +66,7 @@ _SIGNATURES = {
     "paged_decode_multi_resolve_splits": (ctypes.c_int32, [ctypes.POINTER(PkvDims), ctypes.c_int32, ctypes.c_int32]),
     "paged_kv_slot_mapping_multi": (ctypes.c_int, [c_int32_p, c_int32_p, ctypes.c_int32, ctypes.c_int32,
                                                    ctypes.c_int32, ctypes.c_int32, c_int32_p]),
+    "paged_kv_selftest_wait": (ctypes.c_int, [ctypes.c_void_p]),
     "paged_kv_check_status": (ctypes.c_int, [ctypes.c_void_p]),
     "paged_kv_last_error": (ctypes.c_char_p, []),
     "paged_kv_slot_mapping": (ctypes.c_int, [c_int32_p, c_int32_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
@@ -100,6 +101,7 @@ _SIGNATURES = {
                                           ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
                                           ctypes.c_size_t, ctypes.POINTER(PkvDims), ctypes.c_void_p]),
     "decode_engine_fork": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, c_int32_p]),
+    "decode_engine_set_kv_scales": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "decode_engine_finish": (ctypes.c_int, [ctypes.c_void_p, c_int32_p, c_int32_p]),
     "decode_engine_state": (ctypes.c_int, [ctypes.c_void_p, c_int32_p, c_int32_p]),
     "block_allocator_refcount": (ctypes.c_int32, [ctypes.c_void_p, ctypes.c_int32]),

@@ -434,6 +434,12 @@ def paged_kv_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, block_pai
            "paged_kv_copy_blocks")
 
 
+def paged_kv_selftest_wait(stream=None) -> None:
+    """Launch the bounded-wait self-test: the next paged_kv_check_status
+    raises PagedKVError with PKV_ERR_TIMEOUT (-4) after about 1.5 s."""
+    _check(lib().paged_kv_selftest_wait(_stream(stream)), "paged_kv_selftest_wait")
+
+
 def paged_kv_check_status(stream=None) -> None:
     """Synchronise the stream and raise if a kernel flagged an error."""
     _check(lib().paged_kv_check_status(_stream(stream)), "paged_kv_check_status")

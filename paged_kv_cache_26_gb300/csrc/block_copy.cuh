@@ -35,4 +35,17 @@ __global__ void copy_blocks_kernel(const int32_t* __restrict__ pairs, int32_t nu
   }
 }
 
+// Self-test of the bounded waits: one warp waits on an mbarrier that nothing
+// ever arrives on.  The wait gives up after kWaitLimitNs, flags kErrTimeout
+// and the kernel returns; the context stays usable.
+__global__ void wait_selftest_kernel() {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0);
+}
+
 }  // namespace pkv

@@ -43,6 +43,8 @@ struct pkv_decode_engine {
   int parity = 0;
   int last = -1;                         // table buffer of the last step
   int32_t* slots_h[kSlotRing] = {};
+  const float* k_scale = nullptr;        // set: the pools hold E4M3 codes with these per-KV-head scales
+  const float* v_scale = nullptr;
   cudaEvent_t adm_ev[kSlotRing] = {};
   bool adm_pending[kSlotRing] = {};
   int adm_i = 0;
@@ -142,7 +144,9 @@ int decode_engine_admit(pkv_decode_engine* e, int32_t prompt_tokens, int32_t gen
     }
     cudaEventRecord(e->adm_ev[i], s);
     e->adm_pending[i] = true;
-    rc = paged_kv_append(prompt_k, prompt_v, dev, prompt_tokens, k_cache, v_cache, dims, stream);
+    rc = e->k_scale ? paged_kv_append_fp8(prompt_k, prompt_v, dev, prompt_tokens, k_cache, v_cache, e->k_scale,
+                                          e->v_scale, dims, stream)
+                    : paged_kv_append(prompt_k, prompt_v, dev, prompt_tokens, k_cache, v_cache, dims, stream);
     if (rc != PKV_OK) {
       block_allocator_free_seq(e->alloc, sid);
       return rc;
@@ -205,11 +209,22 @@ int decode_engine_step(pkv_decode_engine* e, int32_t* tables_dev, int32_t* lens_
   e->last = i;
   e->parity ^= 1;
   if (ncopy > 0) {
-    rc = paged_kv_copy_blocks(k_cache, v_cache, copy_pairs_dev, ncopy, dims, 2, stream);
+    rc = paged_kv_copy_blocks(k_cache, v_cache, copy_pairs_dev, ncopy, dims, e->k_scale ? 1 : 2, stream);
     if (rc != PKV_OK) return rc;
   }
+  if (e->k_scale)
+    return paged_decode_step_fp8(q, k_new, v_new, k_cache, v_cache, e->k_scale, e->v_scale, tables_dev, lens_dev,
+                                 scale, out, workspace, workspace_bytes, dims, stream);
   return paged_decode_step(q, k_new, v_new, k_cache, v_cache, tables_dev, lens_dev, scale, out, 0, workspace,
                            workspace_bytes, dims, stream);
+}
+
+int decode_engine_set_kv_scales(pkv_decode_engine* e, const float* k_scale, const float* v_scale) {
+  if (!e || (k_scale == nullptr) != (v_scale == nullptr))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "decode_engine_set_kv_scales: give both scales or neither");
+  e->k_scale = k_scale;
+  e->v_scale = v_scale;
+  return PKV_OK;
 }
 
 int decode_engine_finish(pkv_decode_engine* e, int32_t* freed_slots, int32_t* num_freed) {

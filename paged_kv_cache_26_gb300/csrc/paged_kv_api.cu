@@ -675,6 +675,13 @@ int paged_kv_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pair
   return PKV_OK;
 }
 
+int paged_kv_selftest_wait(void* stream) {
+  pkv::wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "wait_selftest_kernel launch");
+  return PKV_OK;
+}
+
 int paged_kv_append_fp8(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t num_tokens,
                         void* k_cache, void* v_cache, const float* k_scale, const float* v_scale,
                         const pkv_dims* dims, void* stream) {

@@ -20,6 +20,11 @@ waiting ones enter at every iteration):
 * finish_step(): sequences whose generation budget is spent free their blocks.
 
 Empty batch slots have context length 0 (zero output, nothing appended).
+
+With ``k_scale`` / ``v_scale`` (float32[num_kv_heads]) the pools hold E4M3
+codes (design.babushkai.com "GPU推論の内部構造", section "KVキャッシュの台帳":
+an FP8 cache halves the bytes per token); prompts and new tokens stay
+fp16/bf16 and are quantised as they are appended.
 """
 from __future__ import annotations
 
@@ -38,14 +43,26 @@ BLOCK_SIZE = 16
 
 class DecodeLoop:
     def __init__(self, num_blocks: int, num_q_heads: int, num_kv_heads: int, head_dim: int, max_batch: int,
-                 max_context: int, dtype=torch.bfloat16, device="cuda", seed: int = 0):
+                 max_context: int, dtype=torch.bfloat16, device="cuda", seed: int = 0,
+                 k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None):
         self.device = torch.device(device)
         self.dtype = dtype
         self.H, self.Hk, self.D = num_q_heads, num_kv_heads, head_dim
         self.B = max_batch
         self.max_blocks = math.ceil(max_context / BLOCK_SIZE)
-        self.k_cache = torch.zeros(num_blocks, num_kv_heads, BLOCK_SIZE, head_dim, dtype=dtype, device=self.device)
+        self.fp8 = k_scale is not None
+        if self.fp8 != (v_scale is not None):
+            raise ValueError("give both k_scale and v_scale, or neither")
+        cache_dtype = torch.uint8 if self.fp8 else dtype
+        self.k_cache = torch.zeros(num_blocks, num_kv_heads, BLOCK_SIZE, head_dim, dtype=cache_dtype,
+                                   device=self.device)
         self.v_cache = torch.zeros_like(self.k_cache)
+        if self.fp8:
+            for n, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+                api._need_cuda(n, t, torch.float32)
+                if t.shape != (num_kv_heads,):
+                    raise ValueError(f"{n} must be float32[num_kv_heads]")
+            self.k_scale, self.v_scale = k_scale, v_scale
         self.alloc = api.BlockAllocator(num_blocks, BLOCK_SIZE, seed)
         self._eng = lib().decode_engine_create(self.alloc._h, max_batch, self.max_blocks)
         if not self._eng:
@@ -56,8 +73,15 @@ class DecodeLoop:
         self.copy_pairs = torch.empty(max_batch, 2, dtype=torch.int32, device=self.device)
         self.out = torch.empty(max_batch, num_q_heads, head_dim, dtype=dtype, device=self.device)
         probe_q = torch.empty(max_batch, num_q_heads, head_dim, dtype=dtype, device=self.device)
-        self.workspace = api.make_workspace(probe_q, self.k_cache, self.tables, 0)
-        self._dims = api.make_dims(probe_q, self.k_cache, self.tables)
+        if self.fp8:
+            api._check(lib().decode_engine_set_kv_scales(self._eng, ctypes.c_void_p(k_scale.data_ptr()),
+                                                         ctypes.c_void_p(v_scale.data_ptr())), "set_kv_scales")
+            self._dims = api.make_dims_fp8(probe_q, self.k_cache, self.tables)
+            need = int(lib().paged_decode_workspace_bytes(ctypes.byref(self._dims), 0))
+            self.workspace = torch.zeros(need, dtype=torch.uint8, device=self.device) if need else None
+        else:
+            self.workspace = api.make_workspace(probe_q, self.k_cache, self.tables, 0)
+            self._dims = api.make_dims(probe_q, self.k_cache, self.tables)
         self._freed = np.empty(max_batch, np.int32)
         self._nfreed = ctypes.c_int32(0)
         self._slot = ctypes.c_int32(-1)

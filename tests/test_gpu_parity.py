@@ -405,3 +405,17 @@ def test_fused_and_separate_steps_give_identical_bits():
     assert torch.equal(ka.view(torch.int16), kb.view(torch.int16))
     assert torch.equal(va.view(torch.int16), vb.view(torch.int16))
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_bounded_wait_gives_up_reports_timeout_and_the_device_stays_usable():
+    """A wait on a barrier nothing signals: the kernel gives up after its limit,
+    the host reads PKV_ERR_TIMEOUT, and the next decode is still correct."""
+    import time
+    t0 = time.time()
+    pkv.paged_kv_selftest_wait()
+    with pytest.raises(pkv.PagedKVError) as e:
+        pkv.paged_kv_check_status()
+    assert e.value.code == -4 and "bounded wait" in str(e.value)
+    assert 1.0 < time.time() - t0 < 30.0
+    pkv.paged_kv_check_status()  # cleared
+    full_check(wl.generate(wl.TINY, seed=4), 0)

@@ -207,3 +207,78 @@ def test_decode_loop_with_parallel_sampling_against_the_oracle():
                 ref = oracle.attend_one(oracle.widen(bits(q[slot, h]), "bf16"), oracle.widen(k_rec, "bf16"),
                                         oracle.widen(v_rec, "bf16"), 1 / math.sqrt(D))[0]
                 assert np.all(np.abs(got[slot, h] - ref) <= 2e-3 + 1e-2 * np.abs(ref))
+
+
+@pytest.mark.gpu
+def test_decode_loop_on_an_fp8_pool_with_forks_against_the_oracle():
+    """The loop over an E4M3 pool: every sequence's codes are the oracle's
+    quantisation of its history (forks included), and the output matches the
+    oracle's attention over the dequantised pool."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_26_gb300.loop import DecodeLoop
+
+    dev = torch.device("cuda")
+    Hq, Hk, D, B = 8, 2, 128, 6
+    rng = np.random.default_rng(2)
+    g = torch.Generator(device=dev).manual_seed(2)
+    ks = torch.tensor([0.011, 0.017], dtype=torch.float32, device=dev)
+    vs = torch.tensor([0.013, 0.009], dtype=torch.float32, device=dev)
+    loop = DecodeLoop(num_blocks=60, num_q_heads=Hq, num_kv_heads=Hk, head_dim=D, max_batch=B, max_context=128,
+                      dtype=torch.bfloat16, device=dev, seed=9, k_scale=ks, v_scale=vs)
+    history = {}
+
+    def bits(t):
+        return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+    forks = 0
+    q = out = None
+    for step in range(30):
+        while loop.free_slots().size:
+            active = loop.active_slots()
+            if active.size and rng.random() < 0.5:
+                src = int(rng.choice(active))
+                slot = loop.fork(src, int(rng.integers(3, 20)))
+                if slot is None:
+                    break
+                history[int(loop.seq[slot])] = list(history[int(loop.seq[src])])
+                forks += 1
+            else:
+                P = int(rng.integers(1, 40))
+                pk = torch.randn(P, Hk, D, generator=g, device=dev).bfloat16()
+                pv = torch.randn(P, Hk, D, generator=g, device=dev).bfloat16()
+                slot = loop.admit(pk, pv, int(rng.integers(3, 20)))
+                if slot is None:
+                    break
+                history[int(loop.seq[slot])] = [(r[0], r[1]) for r in zip(bits(pk), bits(pv))]
+        q = torch.randn(B, Hq, D, generator=g, device=dev).bfloat16()
+        kn = torch.randn(B, Hk, D, generator=g, device=dev).bfloat16()
+        vn = torch.randn(B, Hk, D, generator=g, device=dev).bfloat16()
+        out = loop.step(q, kn, vn)
+        for slot in loop.active_slots():
+            history[int(loop.seq[slot])].append((bits(kn[slot]), bits(vn[slot])))
+        if step < 29:
+            loop.finish_step()
+    torch.cuda.synchronize()
+    assert forks > 0
+    kc, vc = loop.k_cache.cpu().numpy(), loop.v_cache.cpu().numpy()
+    tables, lens = loop.tables.cpu().numpy(), loop.lens.cpu().numpy()
+    ksn, vsn = ks.cpu().numpy(), vs.cpu().numpy()
+    got = oracle.widen(bits(out), "bf16")
+    for slot in range(B):
+        sid = int(loop.seq[slot])
+        if sid < 0:
+            continue
+        hist = history[sid]
+        L = len(hist)
+        assert lens[slot] == L
+        for kv in range(Hk):
+            k_codes = oracle.quantize_e4m3(np.stack([h[0][kv] for h in hist]), "bf16", ksn[kv])
+            v_codes = oracle.quantize_e4m3(np.stack([h[1][kv] for h in hist]), "bf16", vsn[kv])
+            assert np.array_equal(oracle.gather_kv(kc, tables[slot], L, kv, 16), k_codes)
+            assert np.array_equal(oracle.gather_kv(vc, tables[slot], L, kv, 16), v_codes)
+            K = oracle.dequantize_e4m3(k_codes, ksn[kv])
+            V = oracle.dequantize_e4m3(v_codes, vsn[kv])
+            for h in range(kv * (Hq // Hk), (kv + 1) * (Hq // Hk)):
+                ref = oracle.attend_one(oracle.widen(bits(q[slot, h]), "bf16"), K, V, 1 / math.sqrt(D))[0]
+                assert np.all(np.abs(got[slot, h] - ref) <= 2e-3 + 1e-2 * np.abs(ref))
