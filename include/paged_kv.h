@@ -168,7 +168,9 @@ size_t paged_decode_workspace_bytes(const pkv_dims* dims, int32_t num_splits);
  * block_tables and context_lens from host buffers (pinned for asynchronous
  * copies) into the caller's device staging buffers, runs paged_decode_step on
  * `stream`, and copies out back to out_host.  The step is complete when the
- * stream is.
+ * stream is.  Inputs laid out back to back (q, k_new, v_new, block_tables,
+ * context_lens) in one host buffer and one device region, each at the same
+ * offsets, travel in a single copy.
  */
 typedef struct pkv_step_buffers {
   const void* q_host;  const void* k_new_host;  const void* v_new_host;

@@ -766,12 +766,29 @@ int paged_decode_step_from_host(const pkv_step_buffers* s, void* k_cache, void* 
              {s->v_new_dev, s->v_new_host, kv_bytes},
              {s->block_tables_dev, s->block_tables_host, tbl_bytes},
              {s->context_lens_dev, s->context_lens_host, B * sizeof(int32_t)}};
+  // Copies whose host and device ranges both continue the previous one are
+  // merged: inputs packed back to back in one pinned buffer and one device
+  // region travel in a single copy (each copy costs a fixed latency).
+  const Copy* run = nullptr;
+  size_t run_n = 0;
+  auto flush = [&]() -> int {
+    if (!run || run_n == 0) return PKV_OK;
+    cudaError_t e = cudaMemcpyAsync(run->dst, run->src, run_n, cudaMemcpyHostToDevice, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "step: host-to-device copy");
+  };
   for (const auto& c : h2d) {
     if (c.n == 0) continue;
     if (!c.dst || !c.src) return pkv_fail(PKV_ERR_INVALID_ARG, "step: NULL staging or host buffer");
-    cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "step: host-to-device copy");
+    if (run && static_cast<const uint8_t*>(run->src) + run_n == c.src &&
+        static_cast<uint8_t*>(run->dst) + run_n == c.dst) {
+      run_n += c.n;
+      continue;
+    }
+    if ((rc = flush()) != PKV_OK) return rc;
+    run = &c;
+    run_n = c.n;
   }
+  if ((rc = flush()) != PKV_OK) return rc;
   if (B == 0) return PKV_OK;
   rc = decode_impl(s->q_dev, s->k_new_dev, s->v_new_dev, k_cache, v_cache, s->block_tables_dev,
                    s->context_lens_dev, scale, s->out_dev, num_splits, workspace, workspace_bytes, d, stream);
