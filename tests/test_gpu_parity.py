@@ -419,3 +419,44 @@ def test_bounded_wait_gives_up_reports_timeout_and_the_device_stays_usable():
     assert 1.0 < time.time() - t0 < 30.0
     pkv.paged_kv_check_status()  # cleared
     full_check(wl.generate(wl.TINY, seed=4), 0)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_decode_step_replays_from_a_cuda_graph(fp8):
+    """A step captured in a CUDA graph and replayed gives the same bits as the
+    direct call (the step is idempotent: same token, same slot)."""
+    spec = wl.LLAMA3_8B.replace(name="graph", batch=9, lengths=("uniform", 1, 600), num_q_heads=16,
+                                num_kv_heads=4)
+    w = wl.generate(spec, seed=6)
+    dev = torch.device("cuda")
+    q, kn, vn = w.q[0].to(dev), w.k_new[0].to(dev), w.v_new[0].to(dev)
+    bt, cl = torch.from_numpy(w.block_tables).to(dev), torch.from_numpy(w.context_lens).to(dev)
+    if fp8:
+        f8 = wl.fp8_caches(w, seed=6)
+        kc, vc = f8.k_cache[0].to(dev, copy=True), f8.v_cache[0].to(dev, copy=True)
+        ks, vs = f8.k_scale[0].to(dev), f8.v_scale[0].to(dev)
+        ws = torch.zeros(pkv.paged_decode_workspace_bytes(q, w.k_cache[0], bt, 0), dtype=torch.uint8, device=dev)
+
+        def step(out, stream=None):
+            pkv.paged_decode_step_fp8(q, kn, vn, kc, vc, ks, vs, bt, cl, w.scale, out=out, workspace=ws,
+                                      stream=stream)
+    else:
+        kc, vc = w.k_cache[0].to(dev, copy=True), w.v_cache[0].to(dev, copy=True)
+        ws = pkv.make_workspace(q, kc, bt, 0)
+
+        def step(out, stream=None):
+            pkv.paged_decode_step(q, kn, vn, kc, vc, bt, cl, w.scale, out=out, workspace=ws, stream=stream)
+
+    direct = torch.empty_like(q)
+    step(direct)
+    torch.cuda.synchronize()
+    replayed = torch.zeros_like(q)
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=cap):
+        step(replayed, stream=cap)
+    for _ in range(5):
+        g.replay()
+    torch.cuda.synchronize()
+    pkv.paged_kv_check_status()
+    assert torch.equal(direct.view(torch.int16), replayed.view(torch.int16))
