@@ -185,7 +185,7 @@ struct WorkspaceLayout {
 
 // Segments of the persistent partition for the largest grid (one CTA per SM).
 size_t persistent_segments() {
-  return static_cast<size_t>(device_sms()) * pkv::kMaxPersistentWarps * (1 + pkv::Partition::kTailChunks);
+  return static_cast<size_t>(device_sms()) * pkv::kMaxPersistentWarps * (1 + pkv::Partition::kMaxTailChunks);
 }
 
 WorkspaceLayout workspace_layout(const pkv_dims* d, const SplitPlan& p) {

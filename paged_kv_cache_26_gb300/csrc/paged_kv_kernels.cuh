@@ -673,26 +673,37 @@ constexpr int persistent_max_seqs() {
 
 // Work partition of the persistent kernel.  The flattened block space
 // [0, total) is cut into equal shares of R blocks, one per warp.  Each share
-// is a static head, processed by its own warp, followed by four tail chunks
-// (4/10, 3/10, 2/10, 1/10 of the tail).  Chunk k of share w is segment
-// nwarps + k * nwarps + w; warps claim chunks in that order from a counter
-// once their head is done, so SMs with more memory bandwidth take more of the
-// tails.  The head is 7/10 of a share, or all of it when shares are shorter
-// than kMinDynamicShare blocks (there the chunks would be too small to pay for
-// their hand-over).  Every segment is a contiguous block range; the decode and
-// merge kernels derive all boundaries from (total, nwarps) alone.
+// is a static head, processed by its own warp, followed by tail chunks that
+// warps claim in order from a counter once their head is done, so SMs with
+// more memory bandwidth take more of the tails.  The head is 7/10 of a
+// share; the tail is cut into four chunks (4/10, 3/10, 2/10, 1/10) for shares
+// of 200 blocks or more, three (5/10, 3/10, 2/10) from 100, two (6/10, 4/10)
+// below: every segment boundary inside a unit leaves a piece for the merge,
+// and fewer, larger chunks keep those few where a share is short.  Shares under kMinDynamicShare blocks are all head, with nothing
+// to claim (the chunks would be too small to pay for their hand-over).  Chunk
+// k of share w is segment nwarps + k * nwarps + w.  Every segment is a
+// contiguous block range; the decode and merge kernels derive all boundaries
+// from (total, nwarps) alone.
 struct Partition {
-  static constexpr int kTailChunks = 4;
+  static constexpr int kMaxTailChunks = 4;
   static constexpr int kMinDynamicShare = 48;
-  int total, nwarps, R;
+  static constexpr int kThreeChunkShare = 100;
+  static constexpr int kFourChunkShare = 200;
+  int total, nwarps, R, nchunks;
 
   __device__ __forceinline__ Partition(int total_, int nwarps_)
-      : total(total_), nwarps(nwarps_), R(total_ > 0 ? (total_ + nwarps_ - 1) / nwarps_ : 1) {}
-  __device__ __forceinline__ static int cum(int k) { return k == 0 ? 0 : k == 1 ? 4 : k == 2 ? 7 : k == 3 ? 9 : 10; }
+      : total(total_), nwarps(nwarps_), R(total_ > 0 ? (total_ + nwarps_ - 1) / nwarps_ : 1),
+        nchunks(R < kMinDynamicShare ? 0 : R < kThreeChunkShare ? 2 : R < kFourChunkShare ? 3 : 4) {}
+  // Cumulative tenths of the tail before chunk k.
+  __device__ __forceinline__ int cum(int k) const {
+    if (nchunks == 2) return k == 0 ? 0 : k == 1 ? 6 : 10;
+    if (nchunks == 3) return k == 0 ? 0 : k == 1 ? 5 : k == 2 ? 8 : 10;
+    return k == 0 ? 0 : k == 1 ? 4 : k == 2 ? 7 : k == 3 ? 9 : 10;
+  }
   __device__ __forceinline__ void head(int w, int& s, int& e) const {
     s = min(total, w * R);
     const int len = min(total, (w + 1) * R) - s;
-    e = s + (R < kMinDynamicShare ? len : len * 7 / 10);
+    e = s + (nchunks == 0 ? len : len * 7 / 10);
   }
   __device__ __forceinline__ void chunk(int k, int w, int& s, int& e) const {
     int hs, he;
@@ -701,14 +712,15 @@ struct Partition {
     s = he + tail * cum(k) / 10;
     e = he + tail * cum(k + 1) / 10;
   }
-  __device__ __forceinline__ int num_chunks() const { return nwarps * kTailChunks; }
-  __device__ __forceinline__ int num_segments() const { return nwarps * (1 + kTailChunks); }
+  __device__ __forceinline__ int num_chunks() const { return nwarps * nchunks; }
+  __device__ __forceinline__ int seg_per_share() const { return 1 + nchunks; }
+  __device__ __forceinline__ int num_segments() const { return nwarps * (1 + nchunks); }
   // Segment holding block p (0 <= p < total): its id and [s, e).
   __device__ __forceinline__ int segment_of(int p, int& s, int& e) const {
     const int w = p / R;
     head(w, s, e);
     if (p < e) return w;
-    for (int k = 0; k < kTailChunks; ++k) {
+    for (int k = 0; k < nchunks; ++k) {
       chunk(k, w, s, e);
       if (p < e) return nwarps + k * nwarps + w;
     }
@@ -840,6 +852,10 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
   auto advance = [&]() {
     if (ip < seg_e) {
       fill_window();
+      return;
+    }
+    if (part.nchunks == 0) {  // all head: nothing to claim, the counters stay untouched
+      more = false;
       return;
     }
     while (true) {
@@ -1078,7 +1094,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, COOP ? 6 : 8)
     merge_persistent_kernel(const DecodeArgs a, int32_t nwarps) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int kPer = D / 32;
-  constexpr int kSegPerShare = 1 + Partition::kTailChunks;
+
   extern __shared__ int merge_smem[];
   __shared__ int s_warp_sum[kMergeWarps];
   __shared__ int64_t s_row[kMergeWarps][32];
@@ -1096,6 +1112,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, COOP ? 6 : 8)
   const int sub = warp % wpr;                      // this warp's part of its row
   const int Hkv = a.num_kv_heads;
   const Partition part(Hkv * s_P[a.num_seqs], nwarps);
+  const int kSegPerShare = part.seg_per_share();
   const int rows = a.num_seqs * a.num_q_heads;
   // Every warp of the CTA runs the same number of iterations (barriers inside).
   for (int base_row = blockIdx.x * rows_per_cta; base_row < rows; base_row += gridDim.x * rows_per_cta) {
