@@ -873,42 +873,50 @@ def run_loop(args, rank, world, local):
     q = torch.randn(B, spec.num_q_heads, spec.head_dim, generator=g, device=dev).to(dt)
     kn = torch.randn(B, spec.num_kv_heads, spec.head_dim, generator=g, device=dev).to(dt)
     vn = torch.randn_like(kn)
-    counts = {"admitted": 0, "retired": 0}
+    # The arrival queue: prompt lengths from the configuration's length law,
+    # 32..256 generated tokens each, drawn up front (requests wait in it).
+    n_queue = B + (args.steps + args.warmup) * B // 16 + 64
+    queue_p = wl.draw_lengths(spec.replace(batch=n_queue), rng).astype(np.int64)
+    queue_g = rng.integers(32, 257, size=n_queue)
+    counts = {"admitted": 0, "retired": 0, "next": 0}
 
     def admit_all():
-        while loop.free_slots().size:
-            P = int(wl.draw_lengths(spec.replace(batch=1), rng)[0])
-            if loop.admit(prompt_k[:P], prompt_v[:P], int(rng.integers(32, 257))) is None:
+        while loop.num_free_slots:
+            i = counts["next"] % n_queue
+            P = int(queue_p[i])
+            if loop.admit(prompt_k[:P], prompt_v[:P], int(queue_g[i])) is None:
                 break
+            counts["next"] += 1
             counts["admitted"] += 1
 
     def one_step():
         admit_all()
         loop.step(q, kn, vn)
-        L = loop.context_lengths()
         counts["retired"] += len(loop.finish_step())
-        return L
 
     for _ in range(args.warmup):
         one_step()
     torch.cuda.synchronize()
     counts.update(admitted=0, retired=0)
-    kv_bytes, tokens, waste = 0, 0, []
+    loop.reset_stats()
     barrier(world)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
     start.record()
     for _ in range(args.steps):
-        L = one_step()
-        kv_bytes += attention_bytes(L, B, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, 2)
-        tokens += int((L > 0).sum())
-        waste.append(loop.waste_blocks())
+        one_step()
     end.record()
     torch.cuda.synchronize()
     wall_s = time.perf_counter() - t0
     pkv.paged_kv_check_status()
     gpu_s = max_over_ranks(start.elapsed_time(end) * 1e-3, world, dev)
     wall_s = max_over_ranks(wall_s, world, dev)
+    st = loop.stats()
+    elem = 2
+    blocks = (st["context_tokens"] + st["unused_tail_slots"]) // 16
+    kv_bytes = (st["context_tokens"] * spec.num_kv_heads * spec.head_dim * 2 * elem
+                + st["steps"] * (2 * B * spec.num_q_heads * spec.head_dim * elem + 4 * B) + 4 * blocks)
+    tokens = st["sequence_steps"]
     if rank == 0:
         print(json.dumps({
             "metric": "continuous-batching decode steps/s (paged_decode_step per step, host scheduling included)",
@@ -921,7 +929,7 @@ def run_loop(args, rank, world, local):
             "generated_tokens_per_s": round(world * tokens / wall_s, 1),
             "attention_GBs": round(world * kv_bytes / wall_s / 1e9, 1),
             "gpu_busy_frac": round(gpu_s / wall_s, 3),
-            "mean_unused_tail_blocks": round(float(np.mean(waste)), 3),
+            "mean_unused_tail_blocks": round(st["unused_tail_slots"] / max(1, st["sequence_steps"]) / 16, 3),
             "admitted": counts["admitted"], "retired": counts["retired"],
         }), flush=True)
 

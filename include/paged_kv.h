@@ -440,10 +440,13 @@ int32_t block_allocator_seq_len(const pkv_block_allocator* a, int32_t seq_id);
  * generation budget is spent, so later sequences reuse them (kasblo.com
  * "vLLMとは？" section "blockはrequestの成長に合わせて割り当てる"; magi "Inference
  * Batching", continuous batching).  One call does a step's host work: growth
- * of every active sequence, export of every table row into pinned host
- * staging, the asynchronous copies, and the launch of paged_decode_step.
- * The engine allocates pinned host memory only; device buffers are the
- * caller's.  Not thread-safe; one stream per engine.
+ * of every active sequence, export of every table row, and the launch of
+ * paged_decode_step.  The tables, context lengths, copy-on-write pairs and
+ * prompt slot mappings are written into mapped pinned host memory that the
+ * engine owns, and the kernels read them there in place: no host-to-device
+ * copy is issued.  The engine allocates that host memory only; the caches,
+ * q / k_new / v_new / out and the workspace are the caller's.  Not
+ * thread-safe; one stream per engine.
  * ---------------------------------------------------------------------- */
 typedef struct pkv_decode_engine pkv_decode_engine;
 
@@ -454,13 +457,12 @@ void decode_engine_destroy(pkv_decode_engine* e);
 
 /* Admit a sequence whose prompt_tokens K/V rows (prompt_k, prompt_v: device,
  * T[prompt_tokens][Hkv][D]) are written into the cache through a slot-mapped
- * append, and which will take gen_tokens decode steps.  slot_staging_dev is a
- * device int32 buffer of 4 * max_blocks_per_seq * 16 entries the engine uses
- * for the prompts' slot mappings.  *batch_slot receives the slot (-1 and
- * PKV_ERR_NO_BLOCKS when no slot or too few blocks are free). */
+ * append (its slot mapping is read from the engine's mapped host staging), and
+ * which will take gen_tokens decode steps.  *batch_slot receives the slot (-1
+ * and PKV_ERR_NO_BLOCKS when no slot or too few blocks are free). */
 int decode_engine_admit(pkv_decode_engine* e, int32_t prompt_tokens, int32_t gen_tokens, const void* prompt_k,
-                        const void* prompt_v, void* k_cache, void* v_cache, int32_t* slot_staging_dev,
-                        const pkv_dims* dims, void* stream, int32_t* batch_slot);
+                        const void* prompt_v, void* k_cache, void* v_cache, const pkv_dims* dims, void* stream,
+                        int32_t* batch_slot);
 
 /* E4M3 pools: with k_scale / v_scale (float32[num_kv_heads], device, owned by
  * the caller) set, the engine's pools hold E4M3 codes: admission appends
@@ -475,18 +477,35 @@ int decode_engine_set_kv_scales(pkv_decode_engine* e, const float* k_scale, cons
  * decode_engine_step).  PKV_ERR_NO_BLOCKS if no batch slot is free. */
 int decode_engine_fork(pkv_decode_engine* e, int32_t src_slot, int32_t gen_tokens, int32_t* batch_slot);
 
-/* One decode step for every active slot: tables_dev (int32[max_batch][max_blocks_per_seq])
- * and lens_dev (int32[max_batch]) receive the step's tables; blocks shared by
- * forked sequences that this step writes into are first copied
- * (copy_pairs_dev, int32[max_batch][2] device scratch, receives the pairs; it
- * may be NULL when no sequence was forked); then paged_decode_step runs with
+/* One decode step for every active slot.  Blocks shared by forked sequences
+ * that this step writes into are first copied (paged_kv_copy_blocks); then
+ * paged_decode_step (paged_decode_step_fp8 with kv scales set) runs with
  * q / k_new / v_new / out covering all max_batch slots (empty slots: context
- * 0, zero output, nothing appended) and num_splits 0.  dims->num_seqs must be
- * max_batch; the pools are fp16/bf16. */
-int decode_engine_step(pkv_decode_engine* e, int32_t* tables_dev, int32_t* lens_dev, int32_t* copy_pairs_dev,
-                       const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
-                       float scale, void* out, void* workspace, size_t workspace_bytes, const pkv_dims* dims,
-                       void* stream);
+ * 0, zero output, nothing appended) and num_splits 0.  The step's block
+ * tables, lengths and copy pairs come from a ring of three mapped pinned host
+ * buffers; an entry is rewritten only after the kernels that read it have
+ * finished (the call waits for them if the host is that far ahead).
+ * dims->num_seqs must be max_batch and dims->max_blocks_per_seq the engine's
+ * table width. */
+int decode_engine_step(pkv_decode_engine* e, const void* q, const void* k_new, const void* v_new, void* k_cache,
+                       void* v_cache, float scale, void* out, void* workspace, size_t workspace_bytes,
+                       const pkv_dims* dims, void* stream);
+
+/* The block tables (int32[max_batch][max_blocks_per_seq], -1 padded) and
+ * context lengths (int32[max_batch]) the last step ran with, copied into
+ * host arrays.  PKV_ERR_INVALID_ARG before the first step. */
+int decode_engine_last_step(const pkv_decode_engine* e, int32_t* tables, int32_t* context_lens);
+
+/* Totals over the steps since creation or the last reset. */
+typedef struct pkv_engine_stats {
+  int64_t steps;              /* decode_engine_step calls that launched */
+  int64_t sequence_steps;     /* active sequences summed over steps = tokens generated */
+  int64_t context_tokens;     /* context lengths summed over steps = tokens attended */
+  int64_t unused_tail_slots;  /* unused slots of each active sequence's last block, summed over steps */
+  int64_t copied_blocks;      /* copy-on-write block copies */
+} pkv_engine_stats;
+int decode_engine_get_stats(const pkv_decode_engine* e, pkv_engine_stats* stats);
+int decode_engine_reset_stats(pkv_decode_engine* e);
 
 /* Count the step against every active sequence; those that spent their
  * budget free their blocks.  freed_slots (host, max_batch entries) receives

@@ -21,6 +21,11 @@ class PkvStepBuffers(ctypes.Structure):
         "q_dev", "k_new_dev", "v_new_dev", "block_tables_dev", "context_lens_dev", "out_dev")]
 
 
+class PkvEngineStats(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int64) for name in (
+        "steps", "sequence_steps", "context_tokens", "unused_tail_slots", "copied_blocks")]
+
+
 _SIGNATURES = {
     "paged_kv_append": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(PkvDims), ctypes.c_void_p]),
@@ -94,12 +99,15 @@ _SIGNATURES = {
     "decode_engine_create": (ctypes.c_void_p, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32]),
     "decode_engine_destroy": (None, [ctypes.c_void_p]),
     "decode_engine_admit": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
-                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                            ctypes.POINTER(PkvDims), ctypes.c_void_p, c_int32_p]),
     "decode_engine_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                                          ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
-                                          ctypes.c_size_t, ctypes.POINTER(PkvDims), ctypes.c_void_p]),
+                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(PkvDims),
+                                          ctypes.c_void_p]),
+    "decode_engine_last_step": (ctypes.c_int, [ctypes.c_void_p, c_int32_p, c_int32_p]),
+    "decode_engine_get_stats": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(PkvEngineStats)]),
+    "decode_engine_reset_stats": (ctypes.c_int, [ctypes.c_void_p]),
     "decode_engine_fork": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, c_int32_p]),
     "decode_engine_set_kv_scales": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "decode_engine_finish": (ctypes.c_int, [ctypes.c_void_p, c_int32_p, c_int32_p]),

@@ -7,10 +7,15 @@
 // and magi "Inference Batching", continuous batching (finished sequences leave
 // and waiting ones enter at every iteration).
 //
-// The engine owns only host memory: pinned staging for the block tables, the
-// copy-on-write block pairs and the prompts' slot mappings (two table / pair
-// buffers, a ring of four slot buffers), each reused only after an event shows
-// that the copy reading it finished.  Device buffers are the caller's.
+// The engine owns only host memory: mapped pinned staging for the block
+// tables, context lengths and copy-on-write block pairs of a step (a ring of
+// three) and for the prompts' slot mappings (a ring of four).  The kernels of
+// a step read that staging in place through its device mapping, so a step
+// issues no host-to-device copy: a stream-ordered copy between two decode
+// steps would cost more than the table it moves, since the next step's kernel
+// could then no longer launch while the previous one finishes.  A staging
+// buffer is rewritten only after an event shows that the kernels reading it
+// have finished.
 //
 // Parallel sampling (kasblo.com "vLLMとは？", section "block共有とAutomatic
 // Prefix Caching"): decode_engine_fork starts a sequence that shares all of
@@ -19,6 +24,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 #include <string>
 #include <vector>
 
@@ -27,7 +33,25 @@
 
 namespace {
 constexpr int kSlotRing = 4;
+constexpr int kStepRing = 3;
 constexpr int kBlockSize = 16;
+
+// One mapped pinned allocation: host address and the address kernels use.
+struct Mapped {
+  int32_t* h = nullptr;
+  int32_t* d = nullptr;
+  bool alloc(size_t entries) {
+    if (cudaHostAlloc(reinterpret_cast<void**>(&h), entries * sizeof(int32_t), cudaHostAllocMapped) != cudaSuccess) {
+      h = nullptr;
+      return false;
+    }
+    return cudaHostGetDevicePointer(reinterpret_cast<void**>(&d), h, 0) == cudaSuccess;
+  }
+  void release() {
+    if (h) cudaFreeHost(h);
+    h = d = nullptr;
+  }
+};
 }  // namespace
 
 struct pkv_decode_engine {
@@ -35,31 +59,33 @@ struct pkv_decode_engine {
   int32_t max_batch = 0, max_blocks = 0;
   std::vector<int32_t> seq;              // sequence id per batch slot, -1 = empty
   std::vector<int64_t> remaining;        // tokens still to generate
-  int32_t* tables_h[2] = {nullptr, nullptr};
-  int32_t* lens_h[2] = {nullptr, nullptr};
-  int32_t* pairs_h[2] = {nullptr, nullptr};
-  cudaEvent_t copied[2] = {nullptr, nullptr};
-  bool pending[2] = {false, false};
-  int parity = 0;
-  int last = -1;                         // table buffer of the last step
-  int32_t* slots_h[kSlotRing] = {};
-  const float* k_scale = nullptr;        // set: the pools hold E4M3 codes with these per-KV-head scales
-  const float* v_scale = nullptr;
+  // Step staging, per ring entry: [tables: max_batch * max_blocks][lens: max_batch][pairs: 2 * max_batch].
+  Mapped step_buf[kStepRing];
+  cudaEvent_t step_ev[kStepRing] = {};
+  bool step_pending[kStepRing] = {};
+  int step_i = 0;
+  int last = -1;                         // ring entry of the last step
+  Mapped slots[kSlotRing];
   cudaEvent_t adm_ev[kSlotRing] = {};
   bool adm_pending[kSlotRing] = {};
   int adm_i = 0;
+  const float* k_scale = nullptr;        // set: the pools hold E4M3 codes with these per-KV-head scales
+  const float* v_scale = nullptr;
   std::vector<int32_t> row;
+  pkv_engine_stats stats = {};
+
+  int32_t* tables(int i, bool dev) { return dev ? step_buf[i].d : step_buf[i].h; }
+  int32_t* lens(int i, bool dev) { return tables(i, dev) + static_cast<int64_t>(max_batch) * max_blocks; }
+  int32_t* pairs(int i, bool dev) { return lens(i, dev) + max_batch; }
 
   ~pkv_decode_engine() {
-    for (int i = 0; i < 2; ++i) {
-      if (copied[i]) cudaEventSynchronize(copied[i]), cudaEventDestroy(copied[i]);
-      if (tables_h[i]) cudaFreeHost(tables_h[i]);
-      if (lens_h[i]) cudaFreeHost(lens_h[i]);
-      if (pairs_h[i]) cudaFreeHost(pairs_h[i]);
+    for (int i = 0; i < kStepRing; ++i) {
+      if (step_ev[i]) cudaEventSynchronize(step_ev[i]), cudaEventDestroy(step_ev[i]);
+      step_buf[i].release();
     }
     for (int i = 0; i < kSlotRing; ++i) {
       if (adm_ev[i]) cudaEventSynchronize(adm_ev[i]), cudaEventDestroy(adm_ev[i]);
-      if (slots_h[i]) cudaFreeHost(slots_h[i]);
+      slots[i].release();
     }
   }
 };
@@ -84,22 +110,17 @@ pkv_decode_engine* decode_engine_create(pkv_block_allocator* alloc, int32_t max_
   e->seq.assign(max_batch, -1);
   e->remaining.assign(max_batch, 0);
   e->row.resize(max_blocks_per_seq);
-  const size_t tbl = static_cast<size_t>(max_batch) * max_blocks_per_seq * sizeof(int32_t);
-  const size_t cap = static_cast<size_t>(max_blocks_per_seq) * kBlockSize * sizeof(int32_t);
+  const size_t step_entries = static_cast<size_t>(max_batch) * max_blocks_per_seq + 3 * static_cast<size_t>(max_batch);
+  const size_t slot_entries = static_cast<size_t>(max_blocks_per_seq) * kBlockSize;
   bool ok = true;
-  for (int i = 0; i < 2 && ok; ++i) {
-    ok = cudaHostAlloc(reinterpret_cast<void**>(&e->tables_h[i]), tbl, cudaHostAllocDefault) == cudaSuccess &&
-         cudaHostAlloc(reinterpret_cast<void**>(&e->lens_h[i]), max_batch * sizeof(int32_t),
-                       cudaHostAllocDefault) == cudaSuccess &&
-         cudaHostAlloc(reinterpret_cast<void**>(&e->pairs_h[i]), 2 * max_batch * sizeof(int32_t),
-                       cudaHostAllocDefault) == cudaSuccess &&
-         cudaEventCreateWithFlags(&e->copied[i], cudaEventDisableTiming) == cudaSuccess;
-  }
+  for (int i = 0; i < kStepRing && ok; ++i)
+    ok = e->step_buf[i].alloc(step_entries) &&
+         cudaEventCreateWithFlags(&e->step_ev[i], cudaEventDisableTiming) == cudaSuccess;
   for (int i = 0; i < kSlotRing && ok; ++i)
-    ok = cudaHostAlloc(reinterpret_cast<void**>(&e->slots_h[i]), cap, cudaHostAllocDefault) == cudaSuccess &&
+    ok = e->slots[i].alloc(slot_entries) &&
          cudaEventCreateWithFlags(&e->adm_ev[i], cudaEventDisableTiming) == cudaSuccess;
   if (!ok) {
-    pkv_set_error("decode_engine_create: pinned host staging or event creation failed");
+    pkv_set_error("decode_engine_create: mapped pinned host staging or event creation failed");
     delete e;
     return nullptr;
   }
@@ -109,10 +130,10 @@ pkv_decode_engine* decode_engine_create(pkv_block_allocator* alloc, int32_t max_
 void decode_engine_destroy(pkv_decode_engine* e) { delete e; }
 
 int decode_engine_admit(pkv_decode_engine* e, int32_t prompt_tokens, int32_t gen_tokens, const void* prompt_k,
-                        const void* prompt_v, void* k_cache, void* v_cache, int32_t* slot_staging_dev,
-                        const pkv_dims* dims, void* stream, int32_t* batch_slot) {
+                        const void* prompt_v, void* k_cache, void* v_cache, const pkv_dims* dims, void* stream,
+                        int32_t* batch_slot) {
   if (!e || !batch_slot || !dims || prompt_tokens < 0 || gen_tokens < 1 ||
-      (prompt_tokens > 0 && (!prompt_k || !prompt_v || !slot_staging_dev)))
+      (prompt_tokens > 0 && (!prompt_k || !prompt_v)))
     return pkv_fail(PKV_ERR_INVALID_ARG, "decode_engine_admit: bad argument");
   *batch_slot = -1;
   if (static_cast<int64_t>(prompt_tokens) + gen_tokens > static_cast<int64_t>(e->max_blocks) * kBlockSize)
@@ -132,25 +153,20 @@ int decode_engine_admit(pkv_decode_engine* e, int32_t prompt_tokens, int32_t gen
     block_allocator_block_tables(e->alloc, &sid, 1, e->max_blocks, e->row.data(), &len);
     const int i = e->adm_i;
     e->adm_i = (i + 1) % kSlotRing;
-    if (e->adm_pending[i]) cudaEventSynchronize(e->adm_ev[i]);
-    int32_t* host = e->slots_h[i];
+    if (e->adm_pending[i]) cudaEventSynchronize(e->adm_ev[i]);  // the append that last read this buffer is done
+    int32_t* host = e->slots[i].h;
     for (int32_t p = 0; p < prompt_tokens; ++p) host[p] = e->row[p / kBlockSize] * kBlockSize + p % kBlockSize;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int32_t* dev = slot_staging_dev + static_cast<int64_t>(i) * e->max_blocks * kBlockSize;
-    cudaError_t ce = cudaMemcpyAsync(dev, host, prompt_tokens * sizeof(int32_t), cudaMemcpyHostToDevice, s);
-    if (ce != cudaSuccess) {
-      block_allocator_free_seq(e->alloc, sid);
-      return cuda_err(ce, "decode_engine_admit: slot copy");
-    }
-    cudaEventRecord(e->adm_ev[i], s);
-    e->adm_pending[i] = true;
-    rc = e->k_scale ? paged_kv_append_fp8(prompt_k, prompt_v, dev, prompt_tokens, k_cache, v_cache, e->k_scale,
-                                          e->v_scale, dims, stream)
-                    : paged_kv_append(prompt_k, prompt_v, dev, prompt_tokens, k_cache, v_cache, dims, stream);
+    rc = e->k_scale ? paged_kv_append_fp8(prompt_k, prompt_v, e->slots[i].d, prompt_tokens, k_cache, v_cache,
+                                          e->k_scale, e->v_scale, dims, stream)
+                    : paged_kv_append(prompt_k, prompt_v, e->slots[i].d, prompt_tokens, k_cache, v_cache, dims,
+                                      stream);
     if (rc != PKV_OK) {
       block_allocator_free_seq(e->alloc, sid);
       return rc;
     }
+    const cudaError_t ce = cudaEventRecord(e->adm_ev[i], static_cast<cudaStream_t>(stream));
+    if (ce != cudaSuccess) return cuda_err(ce, "decode_engine_admit: event record");
+    e->adm_pending[i] = true;
   }
   e->seq[slot] = sid;
   e->remaining[slot] = gen_tokens;
@@ -182,41 +198,69 @@ int decode_engine_fork(pkv_decode_engine* e, int32_t src_slot, int32_t gen_token
   return PKV_OK;
 }
 
-int decode_engine_step(pkv_decode_engine* e, int32_t* tables_dev, int32_t* lens_dev, int32_t* copy_pairs_dev,
-                       const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache, float scale,
-                       void* out, void* workspace, size_t workspace_bytes, const pkv_dims* dims, void* stream) {
-  if (!e || !tables_dev || !lens_dev || !dims) return pkv_fail(PKV_ERR_INVALID_ARG, "decode_engine_step: bad argument");
+int decode_engine_step(pkv_decode_engine* e, const void* q, const void* k_new, const void* v_new, void* k_cache,
+                       void* v_cache, float scale, void* out, void* workspace, size_t workspace_bytes,
+                       const pkv_dims* dims, void* stream) {
+  if (!e || !dims) return pkv_fail(PKV_ERR_INVALID_ARG, "decode_engine_step: bad argument");
   if (dims->num_seqs != e->max_batch || dims->max_blocks_per_seq != e->max_blocks)
     return pkv_fail(PKV_ERR_INVALID_ARG, "decode_engine_step: dims must match the engine's batch and table width");
-  const int i = e->parity;
-  if (e->pending[i]) cudaEventSynchronize(e->copied[i]);  // the copies that last read these buffers are done
+  const int i = e->step_i;
+  if (e->step_pending[i]) cudaEventSynchronize(e->step_ev[i]);  // the kernels that last read this entry are done
   int32_t ncopy = 0;
-  int rc = block_allocator_step_batch_cow(e->alloc, e->seq.data(), e->max_batch, e->max_blocks, e->tables_h[i],
-                                          e->lens_h[i], e->pairs_h[i], &ncopy);
+  int rc = block_allocator_step_batch_cow(e->alloc, e->seq.data(), e->max_batch, e->max_blocks, e->tables(i, false),
+                                          e->lens(i, false), e->pairs(i, false), &ncopy);
   if (rc != PKV_OK) return rc;
-  if (ncopy > 0 && !copy_pairs_dev)
-    return pkv_fail(PKV_ERR_INVALID_ARG, "decode_engine_step: shared blocks need copying but copy_pairs_dev is NULL");
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t tbl = static_cast<size_t>(e->max_batch) * e->max_blocks * sizeof(int32_t);
-  cudaError_t ce = cudaMemcpyAsync(tables_dev, e->tables_h[i], tbl, cudaMemcpyHostToDevice, s);
-  if (ce == cudaSuccess)
-    ce = cudaMemcpyAsync(lens_dev, e->lens_h[i], e->max_batch * sizeof(int32_t), cudaMemcpyHostToDevice, s);
-  if (ce == cudaSuccess && ncopy > 0)
-    ce = cudaMemcpyAsync(copy_pairs_dev, e->pairs_h[i], 2 * ncopy * sizeof(int32_t), cudaMemcpyHostToDevice, s);
-  if (ce == cudaSuccess) ce = cudaEventRecord(e->copied[i], s);
-  if (ce != cudaSuccess) return cuda_err(ce, "decode_engine_step: table copy");
-  e->pending[i] = true;
   e->last = i;
-  e->parity ^= 1;
+  e->step_i = (i + 1) % kStepRing;
   if (ncopy > 0) {
-    rc = paged_kv_copy_blocks(k_cache, v_cache, copy_pairs_dev, ncopy, dims, e->k_scale ? 1 : 2, stream);
+    rc = paged_kv_copy_blocks(k_cache, v_cache, e->pairs(i, true), ncopy, dims, e->k_scale ? 1 : 2, stream);
     if (rc != PKV_OK) return rc;
   }
   if (e->k_scale)
-    return paged_decode_step_fp8(q, k_new, v_new, k_cache, v_cache, e->k_scale, e->v_scale, tables_dev, lens_dev,
-                                 scale, out, workspace, workspace_bytes, dims, stream);
-  return paged_decode_step(q, k_new, v_new, k_cache, v_cache, tables_dev, lens_dev, scale, out, 0, workspace,
-                           workspace_bytes, dims, stream);
+    rc = paged_decode_step_fp8(q, k_new, v_new, k_cache, v_cache, e->k_scale, e->v_scale, e->tables(i, true),
+                               e->lens(i, true), scale, out, workspace, workspace_bytes, dims, stream);
+  else
+    rc = paged_decode_step(q, k_new, v_new, k_cache, v_cache, e->tables(i, true), e->lens(i, true), scale, out, 0,
+                           workspace, workspace_bytes, dims, stream);
+  // Recorded even after a failed launch, so that the entry is never reused
+  // while an earlier kernel (the block copy) may still read it.
+  const cudaError_t ce = cudaEventRecord(e->step_ev[i], static_cast<cudaStream_t>(stream));
+  e->step_pending[i] = ce == cudaSuccess;
+  if (ce != cudaSuccess) cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (rc != PKV_OK) return rc;
+  if (ce != cudaSuccess) return cuda_err(ce, "decode_engine_step: event record");
+  const int32_t* L = e->lens(i, false);
+  auto& st = e->stats;
+  ++st.steps;
+  st.copied_blocks += ncopy;
+  for (int32_t b = 0; b < e->max_batch; ++b)
+    if (L[b] > 0) {
+      ++st.sequence_steps;
+      st.context_tokens += L[b];
+      st.unused_tail_slots += (L[b] + kBlockSize - 1) / kBlockSize * kBlockSize - L[b];
+    }
+  return PKV_OK;
+}
+
+int decode_engine_last_step(const pkv_decode_engine* e, int32_t* tables, int32_t* context_lens) {
+  if (!e || !tables || !context_lens) return pkv_fail(PKV_ERR_INVALID_ARG, "decode_engine_last_step: bad argument");
+  if (e->last < 0) return pkv_fail(PKV_ERR_INVALID_ARG, "decode_engine_last_step: no step has run");
+  auto* me = const_cast<pkv_decode_engine*>(e);
+  std::memcpy(tables, me->tables(e->last, false), sizeof(int32_t) * static_cast<size_t>(e->max_batch) * e->max_blocks);
+  std::memcpy(context_lens, me->lens(e->last, false), sizeof(int32_t) * static_cast<size_t>(e->max_batch));
+  return PKV_OK;
+}
+
+int decode_engine_get_stats(const pkv_decode_engine* e, pkv_engine_stats* stats) {
+  if (!e || !stats) return pkv_fail(PKV_ERR_INVALID_ARG, "decode_engine_get_stats: bad argument");
+  *stats = e->stats;
+  return PKV_OK;
+}
+
+int decode_engine_reset_stats(pkv_decode_engine* e) {
+  if (!e) return pkv_fail(PKV_ERR_INVALID_ARG, "decode_engine_reset_stats: bad argument");
+  e->stats = pkv_engine_stats{};
+  return PKV_OK;
 }
 
 int decode_engine_set_kv_scales(pkv_decode_engine* e, const float* k_scale, const float* v_scale) {

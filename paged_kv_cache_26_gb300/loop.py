@@ -12,7 +12,8 @@ waiting ones enter at every iteration):
   needs; the prompt's K/V (produced elsewhere: prefill is not this path) is
   written through a slot-mapped append;
 * step(): every active sequence gets one token: the engine grows each
-  sequence (a new block at a block boundary), ships the block tables and runs
+  sequence (a new block at a block boundary), writes the block tables into
+  mapped pinned host memory that the kernels read in place (no copy) and runs
   one paged_decode_step (append + attention) -- one native call per step;
 * fork(): parallel sampling -- a new sequence sharing all of an active one's
   blocks; the shared block a step writes into is copied first (copy-on-write,
@@ -36,7 +37,7 @@ import numpy as np
 import torch
 
 from . import api
-from ._native import c_int32_p, lib
+from ._native import PkvEngineStats, c_int32_p, lib
 
 BLOCK_SIZE = 16
 
@@ -67,21 +68,17 @@ class DecodeLoop:
         self._eng = lib().decode_engine_create(self.alloc._h, max_batch, self.max_blocks)
         if not self._eng:
             raise api.PagedKVError(-3, "decode_engine_create")
-        self.tables = torch.full((max_batch, self.max_blocks), -1, dtype=torch.int32, device=self.device)
-        self.lens = torch.zeros(max_batch, dtype=torch.int32, device=self.device)
-        self.slot_staging = torch.empty(4 * self.max_blocks * BLOCK_SIZE, dtype=torch.int32, device=self.device)
-        self.copy_pairs = torch.empty(max_batch, 2, dtype=torch.int32, device=self.device)
         self.out = torch.empty(max_batch, num_q_heads, head_dim, dtype=dtype, device=self.device)
         probe_q = torch.empty(max_batch, num_q_heads, head_dim, dtype=dtype, device=self.device)
         if self.fp8:
             api._check(lib().decode_engine_set_kv_scales(self._eng, ctypes.c_void_p(k_scale.data_ptr()),
                                                          ctypes.c_void_p(v_scale.data_ptr())), "set_kv_scales")
-            self._dims = api.make_dims_fp8(probe_q, self.k_cache, self.tables)
-            need = int(lib().paged_decode_workspace_bytes(ctypes.byref(self._dims), 0))
-            self.workspace = torch.zeros(need, dtype=torch.uint8, device=self.device) if need else None
+            self._dims = api.make_dims_fp8(probe_q, self.k_cache)
         else:
-            self.workspace = api.make_workspace(probe_q, self.k_cache, self.tables, 0)
-            self._dims = api.make_dims(probe_q, self.k_cache, self.tables)
+            self._dims = api.make_dims(probe_q, self.k_cache)
+        self._dims.max_blocks_per_seq = self.max_blocks
+        need = int(lib().paged_decode_workspace_bytes(ctypes.byref(self._dims), 0))
+        self.workspace = torch.zeros(need, dtype=torch.uint8, device=self.device) if need else None
         self._freed = np.empty(max_batch, np.int32)
         self._nfreed = ctypes.c_int32(0)
         self._slot = ctypes.c_int32(-1)
@@ -89,6 +86,7 @@ class DecodeLoop:
         self._lens = np.zeros(max_batch, np.int32)
         self._step_args = None
         self._step_key = None
+        self._num_free = max_batch
         self.steps = 0
 
     def close(self):
@@ -117,6 +115,11 @@ class DecodeLoop:
     def free_slots(self):
         return np.flatnonzero(self.seq < 0)
 
+    @property
+    def num_free_slots(self) -> int:
+        """Empty batch slots (kept on the host side of the binding: no native call)."""
+        return self._num_free
+
     def active_slots(self):
         return np.flatnonzero(self.seq >= 0)
 
@@ -127,12 +130,12 @@ class DecodeLoop:
         P = int(prompt_k.shape[0])
         rc = lib().decode_engine_admit(self._eng, P, int(gen_len), ctypes.c_void_p(prompt_k.data_ptr()),
                                        ctypes.c_void_p(prompt_v.data_ptr()), ctypes.c_void_p(self.k_cache.data_ptr()),
-                                       ctypes.c_void_p(self.v_cache.data_ptr()),
-                                       ctypes.c_void_p(self.slot_staging.data_ptr()), ctypes.byref(self._dims),
+                                       ctypes.c_void_p(self.v_cache.data_ptr()), ctypes.byref(self._dims),
                                        api._stream(None), ctypes.byref(self._slot))
         if rc == -5:
             return None
         api._check(rc, "decode_engine_admit")
+        self._num_free -= 1
         return int(self._slot.value)
 
     def fork(self, src_slot: int, gen_len: int) -> Optional[int]:
@@ -143,6 +146,7 @@ class DecodeLoop:
         if rc == -5:
             return None
         api._check(rc, "decode_engine_fork")
+        self._num_free -= 1
         return int(self._slot.value)
 
     # ------------------------------------------------------------------ one step
@@ -160,12 +164,11 @@ class DecodeLoop:
                 raise ValueError("q / k_new / v_new must cover every batch slot")
             P = ctypes.c_void_p
             ws = self.workspace
-            self._step_args = (self._eng, P(self.tables.data_ptr()), P(self.lens.data_ptr()),
-                               P(self.copy_pairs.data_ptr()), P(q.data_ptr()),
-                               P(k_new.data_ptr()), P(v_new.data_ptr()), P(self.k_cache.data_ptr()),
-                               P(self.v_cache.data_ptr()), ctypes.c_float(1.0 / math.sqrt(self.D)),
-                               P(self.out.data_ptr()), P(ws.data_ptr() if ws is not None else 0),
-                               ws.numel() if ws is not None else 0, ctypes.byref(self._dims))
+            self._step_args = (self._eng, P(q.data_ptr()), P(k_new.data_ptr()), P(v_new.data_ptr()),
+                               P(self.k_cache.data_ptr()), P(self.v_cache.data_ptr()),
+                               ctypes.c_float(1.0 / math.sqrt(self.D)), P(self.out.data_ptr()),
+                               P(ws.data_ptr() if ws is not None else 0), ws.numel() if ws is not None else 0,
+                               ctypes.byref(self._dims))
             self._step_key = key
         api._check(lib().decode_engine_step(*self._step_args, api._stream(None)), "decode_engine_step")
         self.steps += 1
@@ -176,9 +179,31 @@ class DecodeLoop:
         free their blocks.  Returns their former slots."""
         api._check(lib().decode_engine_finish(self._eng, self._freed.ctypes.data_as(c_int32_p),
                                               ctypes.byref(self._nfreed)), "decode_engine_finish")
-        return [int(s) for s in self._freed[:self._nfreed.value]]
+        n = self._nfreed.value
+        self._num_free += n
+        return self._freed[:n].tolist()
 
     # ------------------------------------------------------------------ accounting
+
+    def last_step(self):
+        """(block tables int32[max_batch][max_blocks], context lengths
+        int32[max_batch]) that the last step ran with."""
+        tables = np.empty((self.B, self.max_blocks), np.int32)
+        lens = np.empty(self.B, np.int32)
+        api._check(lib().decode_engine_last_step(self._eng, tables.ctypes.data_as(c_int32_p),
+                                                 lens.ctypes.data_as(c_int32_p)), "decode_engine_last_step")
+        return tables, lens
+
+    def stats(self) -> dict:
+        """Totals since creation or reset_stats(): steps, tokens generated
+        (sequence_steps), tokens attended (context_tokens), unused tail slots
+        of the last blocks, copy-on-write block copies."""
+        st = PkvEngineStats()
+        api._check(lib().decode_engine_get_stats(self._eng, ctypes.byref(st)), "decode_engine_get_stats")
+        return {name: int(getattr(st, name)) for name, _ in PkvEngineStats._fields_}
+
+    def reset_stats(self) -> None:
+        api._check(lib().decode_engine_reset_stats(self._eng), "decode_engine_reset_stats")
 
     def context_lengths(self) -> np.ndarray:
         """Current context length of every batch slot (0 = empty)."""

@@ -88,8 +88,10 @@ def test_decode_loop_end_to_end_against_the_oracle():
 
     admitted = retired = 0
     q = None
+    expect = {"steps": 0, "sequence_steps": 0, "context_tokens": 0, "unused_tail_slots": 0, "copied_blocks": 0}
     for step in range(70):
         # admit while there is room (prompts of 0..45 tokens, 3..30 steps each)
+        assert loop.num_free_slots == loop.free_slots().size
         while loop.free_slots().size:
             P = int(rng.integers(0, 46))
             pk = torch.randn(P, Hk, D, generator=g, device=dev).half()
@@ -106,14 +108,24 @@ def test_decode_loop_end_to_end_against_the_oracle():
         out = loop.step(q, kn, vn)
         for slot in loop.active_slots():
             history[int(loop.seq[slot])].append((bits(kn[slot]), bits(vn[slot])))
+        Ls = loop.context_lengths()
+        assert np.array_equal(loop.last_step()[1], Ls)
+        act = Ls[Ls > 0]
+        expect["steps"] += 1
+        expect["sequence_steps"] += act.size
+        expect["context_tokens"] += int(act.sum())
+        expect["unused_tail_slots"] += int((-(-act // 16) * 16 - act).sum())
         if step < 69:
             retired += len(loop.finish_step())
     torch.cuda.synchronize()
+    assert loop.stats() == expect
+    loop.reset_stats()
+    assert loop.stats() == dict.fromkeys(expect, 0)
     assert admitted > 2 * B and retired > B                  # sequences came and went, blocks were reused
     assert loop.waste_blocks() < 1.0
 
     kc, vc = bits(loop.k_cache), bits(loop.v_cache)
-    tables, lens = loop.tables.cpu().numpy(), loop.lens.cpu().numpy()
+    tables, lens = loop.last_step()
     ref = np.zeros((B, Hq, D))
     got = oracle.widen(bits(out), "fp16")
     for slot in range(B):
@@ -188,8 +200,9 @@ def test_decode_loop_with_parallel_sampling_against_the_oracle():
             loop.finish_step()
     torch.cuda.synchronize()
     assert forks > B
+    assert loop.stats()["copied_blocks"] > 0                # shared blocks were copied before writes
     kc, vc = bits(loop.k_cache), bits(loop.v_cache)
-    tables, lens = loop.tables.cpu().numpy(), loop.lens.cpu().numpy()
+    tables, lens = loop.last_step()
     got = oracle.widen(bits(out), "bf16")
     for slot in range(B):
         sid = int(loop.seq[slot])
@@ -262,7 +275,7 @@ def test_decode_loop_on_an_fp8_pool_with_forks_against_the_oracle():
     torch.cuda.synchronize()
     assert forks > 0
     kc, vc = loop.k_cache.cpu().numpy(), loop.v_cache.cpu().numpy()
-    tables, lens = loop.tables.cpu().numpy(), loop.lens.cpu().numpy()
+    tables, lens = loop.last_step()
     ksn, vsn = ks.cpu().numpy(), vs.cpu().numpy()
     got = oracle.widen(bits(out), "bf16")
     for slot in range(B):
