@@ -165,12 +165,18 @@ size_t paged_decode_workspace_bytes(const pkv_dims* dims, int32_t num_splits);
 
 /*
  * One whole decode step from host memory: copies q, k_new, v_new,
- * block_tables and context_lens from host buffers (pinned for asynchronous
- * copies) into the caller's device staging buffers, runs paged_decode_step on
- * `stream`, and copies out back to out_host.  The step is complete when the
- * stream is.  Inputs laid out back to back (q, k_new, v_new, block_tables,
- * context_lens) in one host buffer and one device region, each at the same
- * offsets, travel in a single copy.
+ * block_tables and context_lens from host buffers into the caller's device
+ * staging buffers, runs paged_decode_step on `stream`, and copies out back to
+ * out_host.  The step is complete when the stream is; host inputs must stay
+ * unchanged and out_host unread until then.  Inputs laid out back to back
+ * (q, k_new, v_new, block_tables, context_lens) in one host buffer and one
+ * device region, each at the same offsets, travel in a single copy.
+ * Copies whose host side lies in pinned, device-mapped memory (cudaHostAlloc,
+ * cudaHostRegister) and whose addresses and length are 4-byte aligned are made
+ * by a copy kernel in the stream's chain of programmatic launches: it reads
+ * the host inputs over the host link while the previous step's last kernel
+ * finishes, and the output is written back by the same kernel after the
+ * merge.  Other copies (pageable memory) are cudaMemcpyAsync calls.
  */
 typedef struct pkv_step_buffers {
   const void* q_host;  const void* k_new_host;  const void* v_new_host;

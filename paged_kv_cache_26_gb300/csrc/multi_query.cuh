@@ -224,7 +224,7 @@ struct WarpAttnRows {
 
   __device__ __forceinline__ void block(uint32_t ks, uint32_t vs, int valid_v, int vc0, int vc1, float scale_log2,
                                         int lane) {
-    const int gid = lane >> 2, c = lane & 3;
+    const int c = lane & 3;
     const int mi = lane >> 3, rr = lane & 7;  // the matrix and row this lane addresses
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll

@@ -13,6 +13,7 @@
 
 #include "paged_kv.h"
 #include "block_copy.cuh"
+#include "host_copy.cuh"
 #include "multi_query.cuh"
 #include "paged_kv_kernels.cuh"
 #include "pkv_errors.h"
@@ -226,7 +227,7 @@ cudaError_t configure_smem(int bytes) {
 // in-kernel (griddepcontrol.wait) before touching anything that kernel writes.
 template <typename T, int D, bool F8>
 int launch_persistent(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::DecodeArgs& args,
-                      const pkv_dims* d, int max_seqs, cudaStream_t stream) {
+                      const pkv_dims* d, int max_seqs, cudaStream_t stream, bool pdl = true) {
   using PS = pkv::PersistentShape<D, F8>;
   constexpr auto kern = pkv::decode_persistent_kernel<T, D, F8>;
   cudaError_t e = configure_smem<kern>(static_cast<int>(pkv::persistent_smem_bytes<D, F8>(max_seqs)));
@@ -244,9 +245,12 @@ int launch_persistent(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::D
   cfg.dynamicSmemBytes = pkv::persistent_smem_bytes<D, F8>(d->num_seqs);
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  // !pdl: the kernel before this one wrote its inputs (block tables, lengths,
+  // query), which it reads before griddepcontrol.wait: no early launch.
+  cfg.numAttrs = pdl ? 1 : 0;
   e = cudaLaunchKernelEx(&cfg, kern, mk, mv, args);
   if (e != cudaSuccess) return cuda_fail(e, "decode_persistent_kernel launch");
+  cfg.numAttrs = 1;
   // Long units cut into many pieces (on average 6 or more warp shares per
   // unit): a CTA per row, its warps splitting the row's pieces; otherwise a
   // warp per row.
@@ -273,9 +277,10 @@ int launch_persistent(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::D
 
 template <typename T, int D>
 int launch_decode(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::DecodeArgs& args, const SplitPlan& plan,
-                  const pkv_dims* d, cudaStream_t stream) {
+                  const pkv_dims* d, cudaStream_t stream, bool pdl) {
   using Shape = pkv::TileShape<D>;
-  if (plan.persistent) return launch_persistent<T, D, false>(mk, mv, args, d, max_persistent_seqs(d, false), stream);
+  if (plan.persistent)
+    return launch_persistent<T, D, false>(mk, mv, args, d, max_persistent_seqs(d, false), stream, pdl);
   constexpr int kSmem = kStages * Shape::kStageBytes + 1024;
   constexpr auto kern = pkv::decode_split_kernel<T, D, kConsumerWarps, kStages>;
   cudaError_t e = configure_smem<kern>(kSmem);
@@ -309,7 +314,7 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, void* k_cac
                 const int32_t* block_tables, const int32_t* context_lens, float scale, void* out,
                 int32_t num_splits, void* workspace, size_t workspace_bytes, const pkv_dims* d,
                 cudaStream_t stream, bool f8 = false, const float* k_scale = nullptr,
-                const float* v_scale = nullptr) {
+                const float* v_scale = nullptr, bool pdl = true) {
   int rc = check_dims(d, true);
   if (rc != PKV_OK) return rc;
   if (f8) {
@@ -378,14 +383,14 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, void* k_cac
   const bool bf16 = d->dtype == PKV_DTYPE_BF16;
   if (f8) {
     const int mx = max_persistent_seqs(d, true);
-    return bf16 ? launch_persistent<__nv_bfloat16, 128, true>(mk, mv, args, d, mx, stream)
-                : launch_persistent<__half, 128, true>(mk, mv, args, d, mx, stream);
+    return bf16 ? launch_persistent<__nv_bfloat16, 128, true>(mk, mv, args, d, mx, stream, pdl)
+                : launch_persistent<__half, 128, true>(mk, mv, args, d, mx, stream, pdl);
   }
   if (d->head_dim == 128)
-    return bf16 ? launch_decode<__nv_bfloat16, 128>(mk, mv, args, plan, d, stream)
-                : launch_decode<__half, 128>(mk, mv, args, plan, d, stream);
-  return bf16 ? launch_decode<__nv_bfloat16, 64>(mk, mv, args, plan, d, stream)
-              : launch_decode<__half, 64>(mk, mv, args, plan, d, stream);
+    return bf16 ? launch_decode<__nv_bfloat16, 128>(mk, mv, args, plan, d, stream, pdl)
+                : launch_decode<__half, 128>(mk, mv, args, plan, d, stream, pdl);
+  return bf16 ? launch_decode<__nv_bfloat16, 64>(mk, mv, args, plan, d, stream, pdl)
+              : launch_decode<__half, 64>(mk, mv, args, plan, d, stream, pdl);
 }
 
 int append_at_end_impl(const void* k_new, const void* v_new, const int32_t* block_tables,
@@ -614,6 +619,102 @@ int decode_multi_impl(const void* q, const void* k_new, const void* v_new, void*
 
 }  // namespace
 
+// ---- host <-> device copies of a host-buffer step
+
+namespace {
+
+// A host range and its device counterpart.
+struct HostRange {
+  void* dev;
+  const void* host;
+  size_t n;
+};
+
+// Device address of a host range that a kernel may access: both ends in
+// pinned, device-mapped host memory (cudaHostAlloc / cudaHostRegister), at
+// device addresses n - 1 apart.  False for pageable memory.
+bool mapped_host_range(const void* p, size_t n, const uint8_t** dev) {
+  cudaPointerAttributes a, b;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer) return false;
+  if (cudaPointerGetAttributes(&b, static_cast<const uint8_t*>(p) + (n - 1)) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (b.type != cudaMemoryTypeHost ||
+      static_cast<const uint8_t*>(b.devicePointer) != static_cast<const uint8_t*>(a.devicePointer) + (n - 1))
+    return false;
+  *dev = static_cast<const uint8_t*>(a.devicePointer);
+  return true;
+}
+
+// Copies host -> device (to_dev) or device -> host.  Ranges that continue one
+// another on both sides are merged first.  A merged run in mapped pinned host
+// memory, 4-byte aligned on both sides, goes into one stage_copy_kernel launch
+// (a programmatic launch in the stream's chain of kernels); any other run is
+// a cudaMemcpyAsync, issued before that launch.  *kernel_copied tells whether
+// the kernel ran.
+int copy_host_ranges(const HostRange* r, int count, bool to_dev, cudaStream_t stream, bool* kernel_copied) {
+  *kernel_copied = false;
+  HostRange run[8];
+  int nrun = 0;
+  for (int i = 0; i < count; ++i) {
+    if (r[i].n == 0) continue;
+    if (nrun > 0) {
+      HostRange& last = run[nrun - 1];
+      if (static_cast<const uint8_t*>(last.host) + last.n == r[i].host &&
+          static_cast<uint8_t*>(last.dev) + last.n == r[i].dev) {
+        last.n += r[i].n;
+        continue;
+      }
+    }
+    run[nrun++] = r[i];
+  }
+  pkv::CopyList list = {};
+  for (int i = 0; i < nrun; ++i) {
+    const HostRange& c = run[i];
+    const uint8_t* hdev = nullptr;
+    const bool mapped = mapped_host_range(c.host, c.n, &hdev);
+    const uintptr_t bits = reinterpret_cast<uintptr_t>(hdev) | reinterpret_cast<uintptr_t>(c.dev) | c.n;
+    if (mapped && (bits & 3) == 0 && list.n < pkv::kMaxCopyRuns) {
+      pkv::CopyRun& k = list.run[list.n++];
+      k.src = to_dev ? hdev : static_cast<const uint8_t*>(c.dev);
+      k.dst = to_dev ? static_cast<uint8_t*>(c.dev) : const_cast<uint8_t*>(hdev);
+      k.shift = (bits & 15) == 0 ? 4 : 2;
+      k.first = list.total;
+      list.total += static_cast<int64_t>(c.n >> k.shift);
+      continue;
+    }
+    const cudaError_t e = to_dev ? cudaMemcpyAsync(c.dev, c.host, c.n, cudaMemcpyHostToDevice, stream)
+                                 : cudaMemcpyAsync(const_cast<void*>(c.host), c.dev, c.n, cudaMemcpyDeviceToHost,
+                                                   stream);
+    if (e != cudaSuccess) return cuda_fail(e, to_dev ? "step: host-to-device copy" : "step: device-to-host copy");
+  }
+  if (list.total == 0) return PKV_OK;
+  constexpr int64_t per_cta = static_cast<int64_t>(pkv::kCopyThreads) * pkv::kCopyUnitsPerThread;
+  int64_t grid = (list.total + per_cta - 1) / per_cta;
+  if (grid > 4 * static_cast<int64_t>(device_sms())) grid = 4 * static_cast<int64_t>(device_sms());
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(pkv::kCopyThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = to_dev ? cudaLaunchKernelEx(&cfg, pkv::stage_copy_kernel<true>, list)
+                               : cudaLaunchKernelEx(&cfg, pkv::stage_copy_kernel<false>, list);
+  if (e != cudaSuccess) return cuda_fail(e, "stage_copy_kernel launch");
+  *kernel_copied = true;
+  return PKV_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int paged_decode_attention_multi(const void* q, const void* k_cache, const void* v_cache,
@@ -757,46 +858,25 @@ int paged_decode_step_from_host(const pkv_step_buffers* s, void* k_cache, void* 
   const size_t q_bytes = B * d->num_q_heads * d->head_dim * elem;
   const size_t kv_bytes = B * d->num_kv_heads * d->head_dim * elem;
   const size_t tbl_bytes = B * d->max_blocks_per_seq * sizeof(int32_t);
-  struct Copy {
-    void* dst;
-    const void* src;
-    size_t n;
-  } h2d[] = {{s->q_dev, s->q_host, q_bytes},
-             {s->k_new_dev, s->k_new_host, kv_bytes},
-             {s->v_new_dev, s->v_new_host, kv_bytes},
-             {s->block_tables_dev, s->block_tables_host, tbl_bytes},
-             {s->context_lens_dev, s->context_lens_host, B * sizeof(int32_t)}};
-  // Copies whose host and device ranges both continue the previous one are
-  // merged: inputs packed back to back in one pinned buffer and one device
-  // region travel in a single copy (each copy costs a fixed latency).
-  const Copy* run = nullptr;
-  size_t run_n = 0;
-  auto flush = [&]() -> int {
-    if (!run || run_n == 0) return PKV_OK;
-    cudaError_t e = cudaMemcpyAsync(run->dst, run->src, run_n, cudaMemcpyHostToDevice, stream);
-    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "step: host-to-device copy");
-  };
-  for (const auto& c : h2d) {
-    if (c.n == 0) continue;
-    if (!c.dst || !c.src) return pkv_fail(PKV_ERR_INVALID_ARG, "step: NULL staging or host buffer");
-    if (run && static_cast<const uint8_t*>(run->src) + run_n == c.src &&
-        static_cast<uint8_t*>(run->dst) + run_n == c.dst) {
-      run_n += c.n;
-      continue;
-    }
-    if ((rc = flush()) != PKV_OK) return rc;
-    run = &c;
-    run_n = c.n;
-  }
-  if ((rc = flush()) != PKV_OK) return rc;
+  const HostRange h2d[] = {{s->q_dev, s->q_host, q_bytes},
+                           {s->k_new_dev, s->k_new_host, kv_bytes},
+                           {s->v_new_dev, s->v_new_host, kv_bytes},
+                           {s->block_tables_dev, s->block_tables_host, tbl_bytes},
+                           {s->context_lens_dev, s->context_lens_host, B * sizeof(int32_t)}};
+  for (const auto& c : h2d)
+    if (c.n > 0 && (!c.dev || !c.host)) return pkv_fail(PKV_ERR_INVALID_ARG, "step: NULL staging or host buffer");
+  bool kernel_copied = false;
+  if ((rc = copy_host_ranges(h2d, 5, true, stream, &kernel_copied)) != PKV_OK) return rc;
   if (B == 0) return PKV_OK;
+  if (!s->out_host || !s->out_dev) return pkv_fail(PKV_ERR_INVALID_ARG, "step: out_host or out_dev is NULL");
+  // After a copy kernel the decode kernel must not launch early: it reads
+  // the staged lengths, tables and queries before its griddepcontrol.wait.
   rc = decode_impl(s->q_dev, s->k_new_dev, s->v_new_dev, k_cache, v_cache, s->block_tables_dev,
-                   s->context_lens_dev, scale, s->out_dev, num_splits, workspace, workspace_bytes, d, stream);
+                   s->context_lens_dev, scale, s->out_dev, num_splits, workspace, workspace_bytes, d, stream, false,
+                   nullptr, nullptr, !kernel_copied);
   if (rc != PKV_OK) return rc;
-  if (!s->out_host) return pkv_fail(PKV_ERR_INVALID_ARG, "step: out_host is NULL");
-  cudaError_t e = cudaMemcpyAsync(s->out_host, s->out_dev, q_bytes, cudaMemcpyDeviceToHost, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "step: device-to-host copy");
-  return PKV_OK;
+  const HostRange d2h[] = {{s->out_dev, s->out_host, q_bytes}};
+  return copy_host_ranges(d2h, 1, false, stream, &kernel_copied);
 }
 
 int paged_kv_check_status(void* stream_v) {

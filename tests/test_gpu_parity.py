@@ -263,6 +263,69 @@ def test_step_from_host_matches_device_calls():
     assert torch.equal(kc.cpu().view(torch.int16), ref_k.view(torch.int16))
 
 
+@pytest.mark.parametrize("layout", ["pinned", "packed", "pageable"])
+def test_step_from_host_chained_steps_match_device_calls(layout):
+    """Several host-buffer steps issued back to back through the same device
+    staging, each with its own host inputs and output buffer: every output
+    and the final caches equal those of the same steps run from device
+    tensors.  pinned: separate pinned buffers (kernel copies, 4-byte units for
+    the 20-byte lengths); packed: one pinned buffer and one device region (a
+    single merged copy); pageable: unpinned host memory (copy-engine copies)."""
+    w = wl.generate(wl.LLAMA3_8B.replace(batch=5), seed=6)
+    dev = torch.device("cuda")
+    g = torch.Generator().manual_seed(1)
+    steps = []
+    for _ in range(4):
+        steps.append({"q": torch.randn(w.q[0].shape, generator=g).bfloat16(),
+                      "k_new": torch.randn(w.k_new[0].shape, generator=g).bfloat16(),
+                      "v_new": torch.randn(w.v_new[0].shape, generator=g).bfloat16(),
+                      "block_tables": torch.from_numpy(w.block_tables).clone(),
+                      "context_lens": torch.from_numpy(w.context_lens).clone()})
+    kc_ref, vc_ref = w.k_cache[0].to(dev, copy=True), w.v_cache[0].to(dev, copy=True)
+    ref_out = []
+    for st in steps:
+        d = {k: v.to(dev) for k, v in st.items()}
+        ref_out.append(pkv.paged_decode_step(d["q"], d["k_new"], d["v_new"], kc_ref, vc_ref, d["block_tables"],
+                                             d["context_lens"], w.scale).cpu())
+    keys = ["q", "k_new", "v_new", "block_tables", "context_lens"]
+    kc, vc = w.k_cache[0].to(dev, copy=True), w.v_cache[0].to(dev, copy=True)
+    if layout == "packed":
+        nbytes = [steps[0][k].numel() * steps[0][k].element_size() for k in keys]
+        region = torch.empty(sum(nbytes), dtype=torch.uint8, device=dev)
+        devb, off = {}, 0
+        for k, n in zip(keys, nbytes):
+            devb[k] = region[off:off + n].view(steps[0][k].dtype).view(steps[0][k].shape)
+            off += n
+    else:
+        devb = {k: torch.empty_like(steps[0][k], device=dev) for k in keys}
+    devb["out"] = torch.empty_like(steps[0]["q"], device=dev)
+    hosts = []
+    for st in steps:
+        if layout == "packed":
+            buf = torch.empty(sum(nbytes), dtype=torch.uint8).pin_memory()
+            h, off = {}, 0
+            for k, n in zip(keys, nbytes):
+                h[k] = buf[off:off + n].view(st[k].dtype).view(st[k].shape)
+                h[k].copy_(st[k])
+                off += n
+            h["_buf"] = buf
+        else:
+            h = {k: (st[k].contiguous().pin_memory() if layout == "pinned" else st[k].contiguous()) for k in keys}
+        h["out"] = torch.full_like(st["q"], float("nan"))
+        if layout != "pageable":
+            h["out"] = h["out"].pin_memory()
+        hosts.append(h)
+    ws = pkv.make_workspace(devb["q"], kc, devb["block_tables"])
+    for h in hosts:
+        pkv.paged_decode_step_from_host(h, devb, kc, vc, w.scale, 0, ws)
+    torch.cuda.synchronize()
+    pkv.paged_kv_check_status()
+    for h, r in zip(hosts, ref_out):
+        assert torch.equal(h["out"].view(torch.int16), r.view(torch.int16))
+    assert torch.equal(kc.view(torch.int16), kc_ref.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), vc_ref.view(torch.int16))
+
+
 # ---------------------------------------------------------------- errors
 
 def test_out_of_range_inputs_are_flagged_not_faulted():
