@@ -505,35 +505,23 @@ def run_ours(args, rank, world, local):
         dbuf, dviews = pack_tensors(host_in, device=dev)
         dstage.append({**dict(zip(keys_in, dviews)), "out": outs[l], "_buf": dbuf})
     keys = STEP_KEYS
-    if fp8:
-        # No single host-buffer entry point for the E4M3 pool: the public
-        # Python API's copies (pinned host <-> device, on the same stream)
-        # around paged_decode_step_fp8, reading the staged inputs.
-        fp8_args = [(P(dstage[l]["q"].data_ptr()), P(dstage[l]["k_new"].data_ptr()), P(dstage[l]["v_new"].data_ptr()),
-                     P(f8.k_cache[l].data_ptr()), P(f8.v_cache[l].data_ptr()), P(f8.k_scale[l].data_ptr()),
-                     P(f8.v_scale[l].data_ptr()), P(dstage[l]["block_tables"].data_ptr()),
-                     P(dstage[l]["context_lens"].data_ptr()), scale, P(outs[l].data_ptr()), P(ws.data_ptr()),
-                     ws_bytes, ctypes.byref(dims), sp) for l in range(nl)]
-
-        def e2e_once():
-            for l in range(nl):
-                dstage[l]["_buf"].copy_(hbuf, non_blocking=True)
-                if f_step(*fp8_args[l]):
-                    raise RuntimeError(L.paged_kv_last_error().decode())
-                h["out"].copy_(outs[l], non_blocking=True)
-    else:
-        e2e_args = []
-        for l in range(nl):
-            bufs = PkvStepBuffers(**{f"{k}_host": h[k].data_ptr() for k in keys},
-                                  **{f"{k}_dev": dstage[l][k].data_ptr() for k in keys})
+    e2e_args = []
+    for l in range(nl):
+        bufs = PkvStepBuffers(**{f"{k}_host": h[k].data_ptr() for k in keys},
+                              **{f"{k}_dev": dstage[l][k].data_ptr() for k in keys})
+        if fp8:
+            e2e_args.append((bufs, P(f8.k_cache[l].data_ptr()), P(f8.v_cache[l].data_ptr()),
+                             P(f8.k_scale[l].data_ptr()), P(f8.v_scale[l].data_ptr()), scale, P(ws.data_ptr()),
+                             ws_bytes, ctypes.byref(dims), sp))
+        else:
             e2e_args.append((bufs, P(w.k_cache[l].data_ptr()), P(w.v_cache[l].data_ptr()), scale, args.splits,
                              P(ws.data_ptr()), ws_bytes, ctypes.byref(dims), sp))
-        f_e2e = L.paged_decode_step_from_host
+    f_e2e = L.paged_decode_step_fp8_from_host if fp8 else L.paged_decode_step_from_host
 
-        def e2e_once():
-            for a in e2e_args:
-                if f_e2e(ctypes.byref(a[0]), *a[1:]):
-                    raise RuntimeError(L.paged_kv_last_error().decode())
+    def e2e_once():
+        for a in e2e_args:
+            if f_e2e(ctypes.byref(a[0]), *a[1:]):
+                raise RuntimeError(L.paged_kv_last_error().decode())
     for _ in range(min(W, 10)):
         e2e_once()
     torch.cuda.synchronize()

@@ -190,6 +190,15 @@ int paged_decode_step_from_host(const pkv_step_buffers* bufs, void* k_cache, voi
                                 void* workspace, size_t workspace_bytes,
                                 const pkv_dims* dims, void* stream);
 
+/* paged_decode_step_fp8 from host memory: the same buffers and copies as
+ * paged_decode_step_from_host (q, k_new, v_new and out fp16/bf16 per
+ * dims->dtype), over E4M3 pools with the per-KV-head scales k_scale / v_scale
+ * (device float32[num_kv_heads]); num_splits is 0 (the persistent path). */
+int paged_decode_step_fp8_from_host(const pkv_step_buffers* bufs, void* k_cache, void* v_cache,
+                                    const float* k_scale, const float* v_scale, float scale,
+                                    void* workspace, size_t workspace_bytes,
+                                    const pkv_dims* dims, void* stream);
+
 /*
  * Paged decode attention that allocates nothing (device).  There is no
  * counterpart on the pages: this is a convenience of this library.  It is for

@@ -205,6 +205,25 @@ def paged_decode_step_from_host(host: dict, dev: dict, k_cache: torch.Tensor, v_
            "paged_decode_step_from_host")
 
 
+def paged_decode_step_fp8_from_host(host: dict, dev: dict, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                    k_scale: torch.Tensor, v_scale: torch.Tensor, scale: float,
+                                    workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """paged_decode_step_from_host over E4M3 pools (uint8 codes with float32
+    per-KV-head scales k_scale / v_scale); q / k_new / v_new / out stay fp16 or
+    bf16.  Same dict keys as paged_decode_step_from_host."""
+    for n, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        _need_cuda(n, t, torch.float32)
+    keys = STEP_KEYS
+    bufs = PkvStepBuffers(**{f"{k}_host": host[k].data_ptr() for k in keys},
+                          **{f"{k}_dev": dev[k].data_ptr() for k in keys})
+    dims = make_dims_fp8(dev["q"], k_cache, dev["block_tables"])
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().paged_decode_step_fp8_from_host(ctypes.byref(bufs), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                                 _ptr(v_scale), float(scale), _ptr(workspace), ws_bytes,
+                                                 ctypes.byref(dims), _stream(stream)),
+           "paged_decode_step_fp8_from_host")
+
+
 # ---------------------------------------------------------------- several new tokens per sequence
 
 def _multi_checks(q, k_cache, v_cache, block_tables, context_lens, out):

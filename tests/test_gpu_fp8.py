@@ -128,6 +128,44 @@ def test_fp8_fused_and_separate_give_identical_bits():
     assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
 
 
+def test_fp8_step_from_host_chained_matches_device_calls():
+    """Host-buffer E4M3 steps issued back to back through one device staging
+    area (kernel copies in and out, pinned buffers), each with its own inputs
+    and output: outputs and final codes equal those of the same steps run
+    from device tensors."""
+    w = wl.generate(wl.LLAMA3_8B.replace(batch=7), seed=9)
+    f8 = wl.fp8_caches(w, seed=9)
+    dev = torch.device(DEV)
+    ks, vs = f8.k_scale[0].to(dev), f8.v_scale[0].to(dev)
+    g = torch.Generator().manual_seed(2)
+    keys = ["q", "k_new", "v_new", "block_tables", "context_lens"]
+    steps = [{"q": torch.randn(w.q[0].shape, generator=g).bfloat16(),
+              "k_new": torch.randn(w.k_new[0].shape, generator=g).bfloat16(),
+              "v_new": torch.randn(w.v_new[0].shape, generator=g).bfloat16(),
+              "block_tables": torch.from_numpy(w.block_tables).clone(),
+              "context_lens": torch.from_numpy(w.context_lens).clone()} for _ in range(3)]
+    kc_ref, vc_ref = f8.k_cache[0].to(dev, copy=True), f8.v_cache[0].to(dev, copy=True)
+    ref = []
+    for st in steps:
+        d = {k: v.to(dev) for k, v in st.items()}
+        ref.append(pkv.paged_decode_step_fp8(d["q"], d["k_new"], d["v_new"], kc_ref, vc_ref, ks, vs,
+                                             d["block_tables"], d["context_lens"], w.scale).cpu())
+    kc, vc = f8.k_cache[0].to(dev, copy=True), f8.v_cache[0].to(dev, copy=True)
+    devb = {k: torch.empty_like(steps[0][k], device=dev) for k in keys}
+    devb["out"] = torch.empty_like(steps[0]["q"], device=dev)
+    hosts = [{**{k: st[k].contiguous().pin_memory() for k in keys},
+              "out": torch.full_like(st["q"], float("nan")).pin_memory()} for st in steps]
+    need = pkv.paged_decode_workspace_bytes(devb["q"], w.k_cache[0], devb["block_tables"])
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+    for h in hosts:
+        pkv.paged_decode_step_fp8_from_host(h, devb, kc, vc, ks, vs, w.scale, ws)
+    torch.cuda.synchronize()
+    pkv.paged_kv_check_status()
+    for h, r in zip(hosts, ref):
+        assert torch.equal(h["out"].view(torch.int16), r.view(torch.int16))
+    assert torch.equal(kc, kc_ref) and torch.equal(vc, vc_ref)
+
+
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 def test_fp8_append_rounding_saturation_and_skips(dtype):
     """Values on both sides of E4M3's range: zeros, subnormal codes, ties,
