@@ -675,15 +675,17 @@ constexpr int persistent_max_seqs() {
 // [0, total) is cut into equal shares of R blocks, one per warp.  Each share
 // is a static head, processed by its own warp, followed by tail chunks that
 // warps claim in order from a counter once their head is done, so SMs with
-// more memory bandwidth take more of the tails.  The head is 7/10 of a
-// share; the tail is cut into four chunks (4/10, 3/10, 2/10, 1/10) for shares
-// of 200 blocks or more, three (5/10, 3/10, 2/10) from 100, two (6/10, 4/10)
-// below: every segment boundary inside a unit leaves a piece for the merge,
-// and fewer, larger chunks keep those few where a share is short.  Shares under kMinDynamicShare blocks are all head, with nothing
-// to claim (the chunks would be too small to pay for their hand-over).  Chunk
-// k of share w is segment nwarps + k * nwarps + w.  Every segment is a
-// contiguous block range; the decode and merge kernels derive all boundaries
-// from (total, nwarps) alone.
+// more memory bandwidth take more of the tails.  The tail is cut into four
+// chunks (4/10, 3/10, 2/10, 1/10) for shares of 200 blocks or more, three
+// (5/10, 3/10, 2/10) from 100, two (6/10, 4/10) below, with the head 4/5 of
+// the share for three or four chunks and 17/20 for two: every segment
+// boundary inside a unit leaves a piece for the merge, and fewer, larger
+// chunks keep those few where a share is short.  Shares under
+// kMinDynamicShare blocks are all head, with nothing to claim (the chunks
+// would be too small to pay for their hand-over).  Chunk k of share w is
+// segment nwarps + k * nwarps + w.  Every segment is a contiguous block
+// range; the decode and merge kernels derive all boundaries from
+// (total, nwarps) alone.
 struct Partition {
   static constexpr int kMaxTailChunks = 4;
   static constexpr int kMinDynamicShare = 48;
@@ -703,7 +705,7 @@ struct Partition {
   __device__ __forceinline__ void head(int w, int& s, int& e) const {
     s = min(total, w * R);
     const int len = min(total, (w + 1) * R) - s;
-    e = s + (nchunks == 0 ? len : len * 7 / 10);
+    e = s + (nchunks == 0 ? len : nchunks == 2 ? len * 17 / 20 : len * 4 / 5);
   }
   __device__ __forceinline__ void chunk(int k, int w, int& s, int& e) const {
     int hs, he;

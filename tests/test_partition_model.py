@@ -3,8 +3,8 @@ arithmetic of `Partition` in paged_kv_kernels.cuh, restated in Python).
 
 The kernel cuts the flattened (sequence, KV head, block) space into one share
 per warp: R = ceil(total / warps) blocks, of which the warp streams a static
-head (all of it under 48 blocks, else 70 %) and leaves 2, 3 or 4 tail chunks
-(by R) for any warp to claim.  A unit that one segment holds whole is written
+head (all of it under 48 blocks; else 85 % with 2 tail chunks, 80 % with 3 or
+4) and leaves the tail chunks (their number set by R) for any warp to claim.  A unit that one segment holds whole is written
 directly; every other unit leaves one partial per segment that cuts it, in
 slot 0 (the segment's first flush) or 1, and the merge finds them by testing
 the segments of the shares the unit overlaps.  This checks, over random
@@ -31,7 +31,7 @@ class Part:
     def head(self, w):
         s = min(self.total, w * self.R)
         n = min(self.total, (w + 1) * self.R) - s
-        return s, s + (n if self.nchunks == 0 else n * 7 // 10)
+        return s, s + (n if self.nchunks == 0 else n * 17 // 20 if self.nchunks == 2 else n * 4 // 5)
 
     def chunk(self, k, w):
         hs, he = self.head(w)
