@@ -853,8 +853,15 @@ def run_loop(args, rank, world, local):
     max_prompt = int(wl.draw_lengths(spec.replace(batch=4096), np.random.default_rng(1)).max())
     max_ctx = max_prompt + 256
     num_blocks = int(math.ceil(1.25 * B * max_ctx / 16))
+    fp8 = args.kv == "fp8"
+    scales = {}
+    if fp8:
+        # Seeded per-KV-head scales of the E4M3 pool, as the fixed-batch workloads draw them.
+        srng = np.random.default_rng(args.seed + rank + 7)
+        scales = {n: torch.tensor(srng.uniform(0.004, 0.02, size=spec.num_kv_heads), dtype=torch.float32,
+                                  device=dev) for n in ("k_scale", "v_scale")}
     loop = DecodeLoop(num_blocks, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, B, max_ctx, dt, dev,
-                      args.seed + rank)
+                      args.seed + rank, **scales)
     g = torch.Generator(device=dev).manual_seed(args.seed + rank)
     prompt_k = torch.randn(max_prompt, spec.num_kv_heads, spec.head_dim, generator=g, device=dev).to(dt)
     prompt_v = torch.randn_like(prompt_k)
@@ -900,9 +907,9 @@ def run_loop(args, rank, world, local):
     gpu_s = max_over_ranks(start.elapsed_time(end) * 1e-3, world, dev)
     wall_s = max_over_ranks(wall_s, world, dev)
     st = loop.stats()
-    elem = 2
+    elem, kv_elem = 2, (1 if fp8 else 2)
     blocks = (st["context_tokens"] + st["unused_tail_slots"]) // 16
-    kv_bytes = (st["context_tokens"] * spec.num_kv_heads * spec.head_dim * 2 * elem
+    kv_bytes = (st["context_tokens"] * spec.num_kv_heads * spec.head_dim * 2 * kv_elem
                 + st["steps"] * (2 * B * spec.num_q_heads * spec.head_dim * elem + 4 * B) + 4 * blocks)
     tokens = st["sequence_steps"]
     if rank == 0:
@@ -910,8 +917,9 @@ def run_loop(args, rank, world, local):
             "metric": "continuous-batching decode steps/s (paged_decode_step per step, host scheduling included)",
             "value": round(world * args.steps / wall_s, 2), "unit": "steps/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall_s / args.steps * 1e3, 4),
-            "higher_is_better": True, "scaling": "weak", "dtype": spec.dtype, "data": "synthetic",
-            "config": {"workload": f"{spec.name} continuous batching", "batch_slots": B,
+            "higher_is_better": True, "scaling": "weak", "dtype": "e4m3" if fp8 else spec.dtype, "data": "synthetic",
+            "config": {"workload": f"{spec.name} continuous batching" + (", E4M3 pool" if fp8 else ""),
+                       "batch_slots": B,
                        "prompt_lengths": str(spec.lengths), "generated_tokens": "U[32,256]",
                        "num_blocks": num_blocks},
             "generated_tokens_per_s": round(world * tokens / wall_s, 1),
