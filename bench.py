@@ -568,7 +568,9 @@ def run_ours(args, rank, world, local):
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": ncu_traffic(s.name + ("_fp8" if fp8 else "")),
                      "bytes_per_launch": step_bytes // nl, "avg_launch_us": round(step_s * 1e6, 2),
-                     "isolated_call_us": round(call_avg_s * 1e6, 2)},
+                     "isolated_call_us": round(call_avg_s * 1e6, 2),
+                     "isolated_call_us_p10_p50_p90": [round(float(x) * 1e3, 2)
+                                                      for x in np.percentile(call_ms, [10, 50, 90])]},
         "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": K * nl * launches_per_step,
