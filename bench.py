@@ -600,7 +600,8 @@ def run_multi(args, rank, world, local):
     import oracle
     import paged_kv_cache_26_gb300 as pkv
     from paged_kv_cache_26_gb300 import build as pkv_build
-    from paged_kv_cache_26_gb300._native import PkvDims, lib
+    from paged_kv_cache_26_gb300._native import PkvDims, PkvStepBuffers, lib
+    from paged_kv_cache_26_gb300.api import STEP_KEYS
 
     pkv_build.build()
     dev = torch.device("cuda", local)
@@ -662,18 +663,25 @@ def run_multi(args, rank, world, local):
     value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
     peak, peak_kind = load_peaks()
 
-    # ---- end to end: pinned host inputs copied in, the output copied back, on the stream
-    h = {"q": m.q[0].cpu(), "k_new": m.k_new[0].cpu(), "v_new": m.v_new[0].cpu(),
-         "block_tables": torch.from_numpy(w.block_tables), "context_lens": torch.from_numpy(w.context_lens),
-         "out": torch.empty_like(out, device="cpu")}
-    h = {k: v.contiguous().pin_memory() for k, v in h.items()}
-    d = {"q": m.q[0], "k_new": m.k_new[0], "v_new": m.v_new[0], "block_tables": bt, "context_lens": cl}
+    # ---- end to end through the C ABI from pinned host buffers: inputs packed back
+    # to back in one pinned buffer and one device region (one copy in, one out)
+    host_in = [m.q[0].cpu(), m.k_new[0].cpu(), m.v_new[0].cpu(), torch.from_numpy(w.block_tables),
+               torch.from_numpy(w.context_lens)]
+    hbuf, hviews = pack_tensors(host_in, device=None)
+    dbuf, dviews = pack_tensors(host_in, device=dev)
+    keys_in = STEP_KEYS[:-1]
+    h = dict(zip(keys_in, hviews))
+    h["out"] = torch.empty_like(out, device="cpu").pin_memory()
+    dst = {**dict(zip(keys_in, dviews)), "out": out}
+    bufs = PkvStepBuffers(**{f"{k}_host": h[k].data_ptr() for k in STEP_KEYS},
+                          **{f"{k}_dev": dst[k].data_ptr() for k in STEP_KEYS})
+    f_e2e = L.paged_decode_step_multi_from_host
+    e2e_args = (ctypes.byref(bufs), n, P(w.k_cache[0].data_ptr()), P(w.v_cache[0].data_ptr()),
+                ctypes.c_float(w.scale), args.splits, P(ws.data_ptr()), ws_bytes, ctypes.byref(dims), sp)
 
     def e2e_once():
-        for k, t in d.items():
-            t.copy_(h[k], non_blocking=True)
-        step()
-        h["out"].copy_(out, non_blocking=True)
+        if f_e2e(*e2e_args):
+            raise RuntimeError(L.paged_kv_last_error().decode())
 
     for _ in range(min(W, 10)):
         e2e_once()
@@ -686,7 +694,7 @@ def run_multi(args, rank, world, local):
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(start.elapsed_time(end), world, dev) / K
-    h2d = sum(h[k].numel() * h[k].element_size() for k in d)
+    h2d = hbuf.numel()
     d2h = h["out"].numel() * h["out"].element_size()
 
     result = {

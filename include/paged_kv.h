@@ -190,6 +190,14 @@ int paged_decode_step_from_host(const pkv_step_buffers* bufs, void* k_cache, voi
                                 void* workspace, size_t workspace_bytes,
                                 const pkv_dims* dims, void* stream);
 
+/* paged_decode_step_multi from host memory: the same buffers and copies as
+ * paged_decode_step_from_host with q_len new tokens per sequence (q, k_new,
+ * v_new and out hold q_len rows per sequence: [B][q_len][...]); workspace as
+ * paged_decode_multi_workspace_bytes gives for num_splits. */
+int paged_decode_step_multi_from_host(const pkv_step_buffers* bufs, int32_t q_len, void* k_cache, void* v_cache,
+                                      float scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                                      const pkv_dims* dims, void* stream);
+
 /* paged_decode_step_fp8 from host memory: the same buffers and copies as
  * paged_decode_step_from_host (q, k_new, v_new and out fp16/bf16 per
  * dims->dtype), over E4M3 pools with the per-KV-head scales k_scale / v_scale

@@ -10,7 +10,7 @@ from .api import (BlockAllocator, PagedKVError, make_workspace, paged_decode_att
                   paged_decode_multi_workspace_bytes, paged_decode_multi_resolve_splits, paged_kv_slot_mapping_multi,
                   paged_kv_copy_blocks, paged_kv_selftest_wait,
                   paged_decode_resolve_splits, paged_decode_step, paged_decode_step_from_host,
-                  paged_decode_step_fp8_from_host,
+                  paged_decode_step_fp8_from_host, paged_decode_step_multi_from_host,
                   paged_decode_workspace_bytes,
                   paged_kv_append, paged_kv_check_status, paged_kv_slot_mapping)
 
@@ -18,6 +18,7 @@ __all__ = [
     "BlockAllocator", "PagedKVError", "make_workspace", "paged_decode_attention",
     "paged_decode_attention_no_alloc", "paged_decode_resolve_splits",
     "paged_decode_step", "paged_decode_step_from_host", "paged_decode_step_fp8_from_host",
+    "paged_decode_step_multi_from_host",
     "paged_decode_workspace_bytes", "paged_kv_append",
     "paged_kv_check_status", "paged_kv_slot_mapping",
     "paged_kv_append_fp8", "paged_decode_attention_fp8", "paged_decode_step_fp8",

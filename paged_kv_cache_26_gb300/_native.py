@@ -46,6 +46,10 @@ _SIGNATURES = {
     "paged_decode_step_from_host": (ctypes.c_int, [ctypes.POINTER(PkvStepBuffers), ctypes.c_void_p, ctypes.c_void_p,
                                                    ctypes.c_float, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t,
                                                    ctypes.POINTER(PkvDims), ctypes.c_void_p]),
+    "paged_decode_step_multi_from_host": (ctypes.c_int, [ctypes.POINTER(PkvStepBuffers), ctypes.c_int32,
+                                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
+                                                         ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t,
+                                                         ctypes.POINTER(PkvDims), ctypes.c_void_p]),
     "paged_decode_step_fp8_from_host": (ctypes.c_int, [ctypes.POINTER(PkvStepBuffers), ctypes.c_void_p,
                                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                        ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t,

@@ -304,6 +304,25 @@ def paged_decode_step_multi(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.T
     return out
 
 
+def paged_decode_step_multi_from_host(host: dict, dev: dict, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                      scale: float, num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+                                      stream=None) -> None:
+    """paged_decode_step_multi from (pinned) host buffers: q / k_new / v_new /
+    out hold q_len rows per sequence ([B][q_len][...]); same dict keys as
+    paged_decode_step_from_host.  A workspace is allocated when the call needs
+    one and none is given."""
+    keys = STEP_KEYS
+    q_len = int(dev["q"].shape[1])
+    bufs = PkvStepBuffers(**{f"{k}_host": host[k].data_ptr() for k in keys},
+                          **{f"{k}_dev": dev[k].data_ptr() for k in keys})
+    dims = _multi_dims(dev["q"], k_cache, dev["block_tables"])
+    workspace, ws_bytes = _multi_workspace(dev["q"], k_cache, dev["block_tables"], num_splits, workspace)
+    _check(lib().paged_decode_step_multi_from_host(ctypes.byref(bufs), q_len, _ptr(k_cache), _ptr(v_cache),
+                                                   float(scale), num_splits, _ptr(workspace), ws_bytes,
+                                                   ctypes.byref(dims), _stream(stream)),
+           "paged_decode_step_multi_from_host")
+
+
 def paged_kv_slot_mapping_multi(block_tables: np.ndarray, context_lens: np.ndarray, q_len: int,
                                 block_size: int = 16) -> np.ndarray:
     """Host: slots [B][q_len] of each sequence's q_len newest tokens (-1 below position 0)."""

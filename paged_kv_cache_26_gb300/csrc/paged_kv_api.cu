@@ -713,17 +713,21 @@ int copy_host_ranges(const HostRange* r, int count, bool to_dev, cudaStream_t st
   return PKV_OK;
 }
 
-// One step from host buffers; k_scale / v_scale set: the pools hold E4M3 codes.
-int step_from_host(const pkv_step_buffers* s, void* k_cache, void* v_cache, const float* k_scale,
+// One step from host buffers.  q_len new tokens per sequence (1: the
+// one-token step; more: the multi-token step); k_scale / v_scale set: the
+// pools hold E4M3 codes (one token only).
+int step_from_host(const pkv_step_buffers* s, int32_t q_len, void* k_cache, void* v_cache, const float* k_scale,
                    const float* v_scale, float scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
                    const pkv_dims* d, cudaStream_t stream) {
   int rc = check_dims(d, true);
   if (rc != PKV_OK) return rc;
   if (!s) return pkv_fail(PKV_ERR_INVALID_ARG, "step: buffers is NULL");
+  if (q_len < 1 || q_len > pkv::kMaxQueryLen)
+    return pkv_fail(PKV_ERR_UNSUPPORTED, "step: q_len must be 1.." + std::to_string(pkv::kMaxQueryLen));
   const size_t elem = 2;
   const size_t B = d->num_seqs;
-  const size_t q_bytes = B * d->num_q_heads * d->head_dim * elem;
-  const size_t kv_bytes = B * d->num_kv_heads * d->head_dim * elem;
+  const size_t q_bytes = B * q_len * d->num_q_heads * d->head_dim * elem;
+  const size_t kv_bytes = B * q_len * d->num_kv_heads * d->head_dim * elem;
   const size_t tbl_bytes = B * d->max_blocks_per_seq * sizeof(int32_t);
   const HostRange h2d[] = {{s->q_dev, s->q_host, q_bytes},
                            {s->k_new_dev, s->k_new_host, kv_bytes},
@@ -736,12 +740,19 @@ int step_from_host(const pkv_step_buffers* s, void* k_cache, void* v_cache, cons
   if ((rc = copy_host_ranges(h2d, 5, true, stream, &kernel_copied)) != PKV_OK) return rc;
   if (B == 0) return PKV_OK;
   if (!s->out_host || !s->out_dev) return pkv_fail(PKV_ERR_INVALID_ARG, "step: out_host or out_dev is NULL");
-  // After a copy kernel the decode kernel must not launch early: it reads
-  // the staged lengths, tables and queries before its griddepcontrol.wait.
-  const bool f8 = k_scale != nullptr;
-  rc = decode_impl(s->q_dev, s->k_new_dev, s->v_new_dev, k_cache, v_cache, s->block_tables_dev,
-                   s->context_lens_dev, scale, s->out_dev, num_splits, workspace, workspace_bytes, d, stream, f8,
-                   k_scale, v_scale, !kernel_copied);
+  if (q_len > 1) {
+    // The multi-token launches are stream-ordered after the copy kernel.
+    rc = decode_multi_impl(s->q_dev, s->k_new_dev, s->v_new_dev, k_cache, v_cache, s->block_tables_dev,
+                           s->context_lens_dev, q_len, scale, s->out_dev, num_splits, workspace, workspace_bytes, d,
+                           stream);
+  } else {
+    // After a copy kernel the decode kernel must not launch early: it reads
+    // the staged lengths, tables and queries before its griddepcontrol.wait.
+    const bool f8 = k_scale != nullptr;
+    rc = decode_impl(s->q_dev, s->k_new_dev, s->v_new_dev, k_cache, v_cache, s->block_tables_dev,
+                     s->context_lens_dev, scale, s->out_dev, num_splits, workspace, workspace_bytes, d, stream, f8,
+                     k_scale, v_scale, !kernel_copied);
+  }
   if (rc != PKV_OK) return rc;
   const HostRange d2h[] = {{s->out_dev, s->out_host, q_bytes}};
   return copy_host_ranges(d2h, 1, false, stream, &kernel_copied);
@@ -883,15 +894,22 @@ size_t paged_decode_workspace_bytes(const pkv_dims* dims, int32_t num_splits) {
 int paged_decode_step_from_host(const pkv_step_buffers* s, void* k_cache, void* v_cache, float scale,
                                 int32_t num_splits, void* workspace, size_t workspace_bytes, const pkv_dims* d,
                                 void* stream_v) {
-  return step_from_host(s, k_cache, v_cache, nullptr, nullptr, scale, num_splits, workspace, workspace_bytes, d,
+  return step_from_host(s, 1, k_cache, v_cache, nullptr, nullptr, scale, num_splits, workspace, workspace_bytes, d,
                         static_cast<cudaStream_t>(stream_v));
+}
+
+int paged_decode_step_multi_from_host(const pkv_step_buffers* s, int32_t q_len, void* k_cache, void* v_cache,
+                                      float scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                                      const pkv_dims* d, void* stream_v) {
+  return step_from_host(s, q_len, k_cache, v_cache, nullptr, nullptr, scale, num_splits, workspace, workspace_bytes,
+                        d, static_cast<cudaStream_t>(stream_v));
 }
 
 int paged_decode_step_fp8_from_host(const pkv_step_buffers* s, void* k_cache, void* v_cache, const float* k_scale,
                                     const float* v_scale, float scale, void* workspace, size_t workspace_bytes,
                                     const pkv_dims* d, void* stream_v) {
   if (!k_scale || !v_scale) return pkv_fail(PKV_ERR_INVALID_ARG, "step_fp8_from_host: NULL k_scale / v_scale");
-  return step_from_host(s, k_cache, v_cache, k_scale, v_scale, scale, 0, workspace, workspace_bytes, d,
+  return step_from_host(s, 1, k_cache, v_cache, k_scale, v_scale, scale, 0, workspace, workspace_bytes, d,
                         static_cast<cudaStream_t>(stream_v));
 }
 

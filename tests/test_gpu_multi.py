@@ -128,6 +128,42 @@ def test_multi_llama3_8b_full_sampled():
     check_multi(w, m, rows=rows)
 
 
+@pytest.mark.parametrize("splits", [1, 0])
+def test_multi_step_from_host_chained_matches_device_calls(splits):
+    """Multi-token host-buffer steps issued back to back through one device
+    staging area (kernel copies in and out, pinned buffers), each with its own
+    inputs and output: outputs and final caches equal those of the same steps
+    run from device tensors."""
+    w, m = wl.generate_multi(CASES[3][0], 4, seed=11)
+    dev = torch.device(DEV)
+    g = torch.Generator().manual_seed(4)
+    keys = ["q", "k_new", "v_new", "block_tables", "context_lens"]
+    steps = [{"q": torch.randn(m.q[0].shape, generator=g).bfloat16(),
+              "k_new": torch.randn(m.k_new[0].shape, generator=g).bfloat16(),
+              "v_new": torch.randn(m.v_new[0].shape, generator=g).bfloat16(),
+              "block_tables": torch.from_numpy(w.block_tables).clone(),
+              "context_lens": torch.from_numpy(w.context_lens).clone()} for _ in range(3)]
+    kc_ref, vc_ref = w.k_cache[0].to(dev, copy=True), w.v_cache[0].to(dev, copy=True)
+    ref = []
+    for st in steps:
+        d = {k: v.to(dev) for k, v in st.items()}
+        ref.append(pkv.paged_decode_step_multi(d["q"], d["k_new"], d["v_new"], kc_ref, vc_ref, d["block_tables"],
+                                               d["context_lens"], w.scale, num_splits=splits).cpu())
+    kc, vc = w.k_cache[0].to(dev, copy=True), w.v_cache[0].to(dev, copy=True)
+    devb = {k: torch.empty_like(steps[0][k], device=dev) for k in keys}
+    devb["out"] = torch.empty_like(steps[0]["q"], device=dev)
+    hosts = [{**{k: st[k].contiguous().pin_memory() for k in keys},
+              "out": torch.full_like(st["q"], float("nan")).pin_memory()} for st in steps]
+    for h in hosts:
+        pkv.paged_decode_step_multi_from_host(h, devb, kc, vc, w.scale, num_splits=splits)
+    torch.cuda.synchronize()
+    pkv.paged_kv_check_status()
+    for h, r in zip(hosts, ref):
+        assert torch.equal(h["out"].view(torch.int16), r.view(torch.int16))
+    assert torch.equal(kc.view(torch.int16), kc_ref.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), vc_ref.view(torch.int16))
+
+
 def test_multi_invalid_arguments_are_rejected():
     dev = torch.device(DEV)
     kc = torch.zeros(8, 2, 16, 128, dtype=torch.bfloat16, device=dev)
