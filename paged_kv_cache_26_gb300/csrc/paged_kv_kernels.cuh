@@ -677,7 +677,7 @@ constexpr int persistent_max_seqs() {
 // warps claim in order from a counter once their head is done, so SMs with
 // more memory bandwidth take more of the tails.  The tail is cut into four
 // chunks (4/10, 3/10, 2/10, 1/10) for shares of 200 blocks or more, three
-// (5/10, 3/10, 2/10) from 100, two (6/10, 4/10) below, with the head 4/5 of
+// (7/10, 2/10, 1/10) from 100, two (8/10, 2/10) below, with the head 4/5 of
 // the share for three or four chunks and 17/20 for two: every segment
 // boundary inside a unit leaves a piece for the merge, and fewer, larger
 // chunks keep those few where a share is short.  Shares under
@@ -698,8 +698,8 @@ struct Partition {
         nchunks(R < kMinDynamicShare ? 0 : R < kThreeChunkShare ? 2 : R < kFourChunkShare ? 3 : 4) {}
   // Cumulative tenths of the tail before chunk k.
   __device__ __forceinline__ int cum(int k) const {
-    if (nchunks == 2) return k == 0 ? 0 : k == 1 ? 6 : 10;
-    if (nchunks == 3) return k == 0 ? 0 : k == 1 ? 5 : k == 2 ? 8 : 10;
+    if (nchunks == 2) return k == 0 ? 0 : k == 1 ? 8 : 10;
+    if (nchunks == 3) return k == 0 ? 0 : k == 1 ? 7 : k == 2 ? 9 : 10;
     return k == 0 ? 0 : k == 1 ? 4 : k == 2 ? 7 : k == 3 ? 9 : 10;
   }
   __device__ __forceinline__ void head(int w, int& s, int& e) const {

@@ -23,9 +23,9 @@ class Part:
 
     def cum(self, k):
         if self.nchunks == 2:
-            return [0, 6, 10][k]
+            return [0, 8, 10][k]
         if self.nchunks == 3:
-            return [0, 5, 8, 10][k]
+            return [0, 7, 9, 10][k]
         return [0, 4, 7, 9, 10][k]
 
     def head(self, w):
