@@ -314,7 +314,8 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, void* k_cac
                 const int32_t* block_tables, const int32_t* context_lens, float scale, void* out,
                 int32_t num_splits, void* workspace, size_t workspace_bytes, const pkv_dims* d,
                 cudaStream_t stream, bool f8 = false, const float* k_scale = nullptr,
-                const float* v_scale = nullptr, bool pdl = true) {
+                const float* v_scale = nullptr, bool pdl = true, const int32_t* pre_lens = nullptr,
+                const int32_t* pre_tables = nullptr) {
   int rc = check_dims(d, true);
   if (rc != PKV_OK) return rc;
   if (f8) {
@@ -370,6 +371,8 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, void* k_cac
   args.sched = wl.sched_bytes ? reinterpret_cast<int32_t*>(ws + wl.o_bytes + wl.lse_bytes) : nullptr;
   args.block_tables = block_tables;
   args.context_lens = context_lens;
+  args.pre_context_lens = pre_lens;
+  args.pre_block_tables = pre_tables;
   args.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   args.num_seqs = d->num_seqs;
   args.num_q_heads = d->num_q_heads;
@@ -746,12 +749,24 @@ int step_from_host(const pkv_step_buffers* s, int32_t q_len, void* k_cache, void
                            s->context_lens_dev, q_len, scale, s->out_dev, num_splits, workspace, workspace_bytes, d,
                            stream);
   } else {
-    // After a copy kernel the decode kernel must not launch early: it reads
-    // the staged lengths, tables and queries before its griddepcontrol.wait.
+    // After a copy kernel the decode kernel reads the lengths and tables
+    // before its griddepcontrol.wait while the copy may still be staging them.
+    // With the host inputs mapped, those early reads go to the host buffers
+    // (the same values) and the decode kernel launches early, as in a chain
+    // of device steps; otherwise it waits for the copy to finish.
+    const uint8_t* pre_lens = nullptr;
+    const uint8_t* pre_tables = nullptr;
+    bool early = !kernel_copied;
+    if (kernel_copied && mapped_host_range(s->context_lens_host, B * sizeof(int32_t), &pre_lens) &&
+        (tbl_bytes == 0 || mapped_host_range(s->block_tables_host, tbl_bytes, &pre_tables)))
+      early = true;
+    else
+      pre_lens = pre_tables = nullptr;
     const bool f8 = k_scale != nullptr;
     rc = decode_impl(s->q_dev, s->k_new_dev, s->v_new_dev, k_cache, v_cache, s->block_tables_dev,
                      s->context_lens_dev, scale, s->out_dev, num_splits, workspace, workspace_bytes, d, stream, f8,
-                     k_scale, v_scale, !kernel_copied);
+                     k_scale, v_scale, early, reinterpret_cast<const int32_t*>(pre_lens),
+                     reinterpret_cast<const int32_t*>(pre_tables));
   }
   if (rc != PKV_OK) return rc;
   const HostRange d2h[] = {{s->out_dev, s->out_host, q_bytes}};

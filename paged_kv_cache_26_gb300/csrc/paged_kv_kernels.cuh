@@ -567,6 +567,10 @@ struct DecodeArgs {
   float* part_o;              // split: f32[B][Hq][splits][D]; persistent: f32[segments][2][8][D]
   float* part_lse;            // split: f32[B][Hq][splits];    persistent: f32[segments][2][8]
   int32_t* sched;             // persistent: int32[2] chunk counter and finished-warp counter, zero between calls
+  const int32_t* pre_context_lens;  // persistent: where the decode and merge prologues (before their grid
+  const int32_t* pre_block_tables;  // wait) read the lengths and tables; null: context_lens / block_tables.
+                                    // The host-buffer step points them at the mapped host inputs that a copy
+                                    // kernel, still running, is staging into context_lens / block_tables.
   const void* k_new;          // fused append (persistent only): T[B][Hkv][D], or null for no append
   const void* v_new;
   void* k_cache_w;            // the pool, for the appended rows
@@ -739,7 +743,8 @@ __device__ __forceinline__ void context_prefix(const DecodeArgs& a, int* s_P, in
   const int lo = min(B, tid * per), hi = min(B, lo + per);
   int local = 0;
   for (int b = lo; b < hi; ++b) {
-    const int ctx = clamped_context(a.context_lens, b, a.max_blocks, flag);
+    const int32_t* lens = a.pre_context_lens ? a.pre_context_lens : a.context_lens;
+    const int ctx = clamped_context(lens, b, a.max_blocks, flag);
     s_ctx[b] = ctx;
     local += (ctx + kBlockSize - 1) / kBlockSize;
   }
@@ -826,6 +831,9 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
     prefetch_tensormap(&tmap_v);
   }
 
+  // Block tables: the prologue's source until the grid wait, then the staged ones.
+  const int32_t* tables = a.pre_block_tables ? a.pre_block_tables : a.block_tables;
+
   // ---- issue side: current segment [seg_s, seg_e) and a 32-block window of it,
   // lane i describing block win_s + i (sequence, KV head, block j, pool row).
   int seg, seg_s, seg_e;
@@ -844,7 +852,7 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
       wb = b;
       wkvh = kvh;
       wj = j;
-      wrow = tile_row(__ldg(a.block_tables + static_cast<int64_t>(b) * a.max_blocks + j), kvh, a);
+      wrow = tile_row(__ldg(tables + static_cast<int64_t>(b) * a.max_blocks + j), kvh, a);
       if (j == 0 || lane == 0)  // a unit starts here: bring its query rows into L2
         prefetch_l2_bulk(static_cast<const T*>(a.q) + (static_cast<int64_t>(b) * Hkv + kvh) * g * D,
                          static_cast<uint32_t>(g * D * sizeof(T)));
@@ -900,6 +908,7 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
     prefetch_l2_bulk(static_cast<const uint8_t*>(a.v_cache_w) + off, Tile::kTileBytes);
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  tables = a.block_tables;
 
   // ---- consume side
   Attn at;
