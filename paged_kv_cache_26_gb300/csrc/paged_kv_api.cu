@@ -637,6 +637,7 @@ struct HostRange {
 // pinned, device-mapped host memory (cudaHostAlloc / cudaHostRegister), at
 // device addresses n - 1 apart.  False for pageable memory.
 bool mapped_host_range(const void* p, size_t n, const uint8_t** dev) {
+  if (!p || n == 0) return false;
   cudaPointerAttributes a, b;
   if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
     cudaGetLastError();
