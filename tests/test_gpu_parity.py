@@ -263,14 +263,16 @@ def test_step_from_host_matches_device_calls():
     assert torch.equal(kc.cpu().view(torch.int16), ref_k.view(torch.int16))
 
 
-@pytest.mark.parametrize("layout", ["pinned", "packed", "pageable"])
+@pytest.mark.parametrize("layout", ["pinned", "packed", "pageable", "mixed"])
 def test_step_from_host_chained_steps_match_device_calls(layout):
     """Several host-buffer steps issued back to back through the same device
     staging, each with its own host inputs and output buffer: every output
     and the final caches equal those of the same steps run from device
     tensors.  pinned: separate pinned buffers (kernel copies, 4-byte units for
     the 20-byte lengths); packed: one pinned buffer and one device region (a
-    single merged copy); pageable: unpinned host memory (copy-engine copies)."""
+    single merged copy); pageable: unpinned host memory (copy-engine copies);
+    mixed: pinned inputs but pageable lengths and output (kernel copies, the
+    decode kernel not launched early, a copy-engine copy of the output)."""
     w = wl.generate(wl.LLAMA3_8B.replace(batch=5), seed=6)
     dev = torch.device("cuda")
     g = torch.Generator().manual_seed(1)
@@ -310,9 +312,10 @@ def test_step_from_host_chained_steps_match_device_calls(layout):
                 off += n
             h["_buf"] = buf
         else:
-            h = {k: (st[k].contiguous().pin_memory() if layout == "pinned" else st[k].contiguous()) for k in keys}
+            pin = {"pinned": keys, "pageable": [], "mixed": ["q", "k_new", "v_new", "block_tables"]}[layout]
+            h = {k: (st[k].contiguous().pin_memory() if k in pin else st[k].contiguous().clone()) for k in keys}
         h["out"] = torch.full_like(st["q"], float("nan"))
-        if layout != "pageable":
+        if layout in ("pinned", "packed"):
             h["out"] = h["out"].pin_memory()
         hosts.append(h)
     ws = pkv.make_workspace(devb["q"], kc, devb["block_tables"])
