@@ -255,7 +255,12 @@ int launch_persistent(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::D
   // unit): a CTA per row, its warps splitting the row's pieces; otherwise a
   // warp per row.
   const int32_t nwarps = static_cast<int32_t>(grid) * PS::kWarps;
-  const bool coop = nwarps >= 6 * static_cast<int64_t>(d->num_seqs) * d->num_kv_heads;
+  const int64_t units = static_cast<int64_t>(d->num_seqs) * d->num_kv_heads;
+  const bool coop = nwarps >= 6 * units;
+  // Two or more warp shares per unit on average: rows have many pieces, so
+  // fold up to 16 per round trip (fewer registers leave room for more merge
+  // CTAs beside the decode grid, which pays when rows are many and short).
+  const bool wide = !coop && nwarps >= 2 * units;
   const int merge_smem = static_cast<int>((2 * static_cast<size_t>(max_persistent_seqs(d, false)) + 1) * 4);
   const int rows = d->num_seqs * d->num_q_heads;
   const int rows_per_cta = coop ? 1 : pkv::kMergeWarps;
@@ -264,6 +269,10 @@ int launch_persistent(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::D
   cfg.dynamicSmemBytes = (2 * static_cast<size_t>(d->num_seqs) + 1) * 4;
   if (coop) {
     constexpr auto merge = pkv::merge_persistent_kernel<T, D, true>;
+    e = configure_smem<merge>(merge_smem);
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, merge, args, nwarps);
+  } else if (wide) {
+    constexpr auto merge = pkv::merge_persistent_kernel<T, D, false, true>;
     e = configure_smem<merge>(merge_smem);
     if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, merge, args, nwarps);
   } else {

@@ -1096,13 +1096,17 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
 // the decode grid is still running; after it, only the partials are read.  The
 // unit's blocks [U, U+nb) overlap shares w0..w1 of 5 segments each; lanes test
 // those candidates in parallel, the overlapping ones are compacted into a
-// list, and their rows are accumulated with independent loads.  Small CTAs
-// (4 warps at <= 64 registers, 80 for COOP): they fit beside a decode CTA.
+// list, and their rows are accumulated with independent loads, up to kBatch
+// pieces per round trip.  Small CTAs (4 warps at <= 64 registers, 80 for
+// COOP) fit two beside a decode CTA.  WIDE (a warp per row, 16 pieces per
+// round trip, <= 128 registers, one beside a decode CTA) is for units cut
+// into many pieces, whose rows would otherwise take two round trips.
 constexpr int kMergeWarps = 4;
 
-template <typename T, int D, bool COOP>
-__global__ void __launch_bounds__(kMergeWarps * 32, COOP ? 6 : 8)
+template <typename T, int D, bool COOP, bool WIDE = false>
+__global__ void __launch_bounds__(kMergeWarps * 32, COOP ? 6 : WIDE ? 4 : 8)
     merge_persistent_kernel(const DecodeArgs a, int32_t nwarps) {
+  static_assert(!(COOP && WIDE), "WIDE is a warp-per-row variant");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int kPer = D / 32;
 
@@ -1175,7 +1179,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, COOP ? 6 : 8)
       // 32 candidates (this warp's share of them); within a batch the
       // log-sum-exps and the partial rows are loaded together (one round
       // trip), at most kBatch rows in flight.
-      constexpr int kBatch = 8;
+      constexpr int kBatch = WIDE ? 16 : 8;
       for (int base = 32 * sub; base < ncand; base += 32 * wpr) {
         const int64_t pr = base + lane < ncand ? piece(base + lane) : -1;
         const unsigned valid = __ballot_sync(0xffffffffu, pr >= 0);
