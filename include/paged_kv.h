@@ -176,7 +176,16 @@ size_t paged_decode_workspace_bytes(const pkv_dims* dims, int32_t num_splits);
  * by a copy kernel in the stream's chain of programmatic launches: it reads
  * the host inputs over the host link while the previous step's last kernel
  * finishes, and the output is written back by the same kernel after the
- * merge.  Other copies (pageable memory) are cudaMemcpyAsync calls.
+ * merge.  Other copies (pageable memory) are cudaMemcpyAsync calls.  When
+ * context_lens_host and block_tables_host are mapped, the attention kernels
+ * read them there (the same values the copy stages) before their grid wait,
+ * so the decode kernel starts while the copy still runs; otherwise it starts
+ * after the copy.  Every buffer stays the caller's; the kernels use them
+ * until the stream reaches the end of the step.
+ * Errors: PKV_ERR_INVALID_ARG for a NULL bufs, a NULL host or staging pointer
+ * of a non-empty input, or NULL out pointers (nothing is launched for
+ * num_seqs = 0 beyond the copies); PKV_ERR_CUDA for a failed copy or launch;
+ * otherwise those of paged_decode_step.
  */
 typedef struct pkv_step_buffers {
   const void* q_host;  const void* k_new_host;  const void* v_new_host;
@@ -193,7 +202,9 @@ int paged_decode_step_from_host(const pkv_step_buffers* bufs, void* k_cache, voi
 /* paged_decode_step_multi from host memory: the same buffers and copies as
  * paged_decode_step_from_host with q_len new tokens per sequence (q, k_new,
  * v_new and out hold q_len rows per sequence: [B][q_len][...]); workspace as
- * paged_decode_multi_workspace_bytes gives for num_splits. */
+ * paged_decode_multi_workspace_bytes gives for num_splits.  The multi-token
+ * kernels start after the copy.  q_len outside 1..8 gives PKV_ERR_UNSUPPORTED;
+ * other errors as paged_decode_step_from_host and paged_decode_step_multi. */
 int paged_decode_step_multi_from_host(const pkv_step_buffers* bufs, int32_t q_len, void* k_cache, void* v_cache,
                                       float scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
                                       const pkv_dims* dims, void* stream);
