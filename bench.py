@@ -5,7 +5,7 @@ One step = the per-token KV append plus paged decode attention (and the split
 merge when the context is split) for a whole batch, on inputs resident in HBM.
 Metric: achieved HBM GB/s of the step's algorithmic bytes, with decode steps/s.
 
-Algorithmic bytes of one attention call (the spec formula):
+Algorithmic bytes of one attention call:
     sum_b L_b * Hkv * D * 2 * sizeof(T)      K and V of every cached token
   + 2 * B * Hq * D * sizeof(T)               q read, out written
   + 4 * sum_b ceil(L_b / 16) + 4 * B          block-table entries used, context lengths
