@@ -40,11 +40,30 @@ def test_library_exports_every_declared_function():
 
 
 def test_library_is_built_for_sm_103a_only():
-    out = os.popen(f"cuobjdump --list-elf {pkv_build.LIB_PATH} 2>/dev/null").read()
-    if not out:
-        pytest.skip("cuobjdump unavailable")
-    arches = set(re.findall(r"sm_(\d+a?)", out))
-    assert arches == {"103a"}, arches
+    # Every translation unit is compiled with this one -gencode and no other.
+    assert pkv_build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert "-lineinfo" in pkv_build.COMMON
+
+
+def header_prototypes():
+    """Parameter count of every function the header declares."""
+    text = open(os.path.join(ROOT, "include", "paged_kv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"#.*", "", text)
+    protos = {}
+    for m in re.finditer(r"\b([a-z_][a-z0-9_]*)\s*\(([^;{}]*?)\)\s*;", text):
+        name, params = m.group(1), m.group(2).strip()
+        protos[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return protos
+
+
+def test_binding_argument_counts_match_the_header():
+    from paged_kv_cache_26_gb300._native import _SIGNATURES
+    protos = header_prototypes()
+    assert set(protos) == set(header_functions())
+    for name, (_, args) in _SIGNATURES.items():
+        assert name in protos, name
+        assert len(args) == protos[name], (name, len(args), protos[name])
 
 
 def test_slot_mapping_matches_oracle_and_page_example(golden_dir):
