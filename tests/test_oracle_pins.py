@@ -440,9 +440,11 @@ def test_fp8_attention_is_attention_on_dequantised_values():
     vq = np.stack([oracle.quantize_e4m3(vc[:, h], "bf16", vs[h]) for h in range(2)], axis=1)
     rows = [(b, h) for b in range(2) for h in range(8)]
     out = oracle.decode_attention_rows(q, kq, vq, tables, np.array(lens), 0.25, "bf16", 4, rows, kv_scales=(ks, vs))
-    # the same attention on the dequantised contiguous arrays, by brute force
-    Kd = np.stack([oracle.dequantize_e4m3(oracle.quantize_e4m3(K[:, h], "bf16", ks[h]), ks[h]) for h in range(2)], 1)
-    Vd = np.stack([oracle.dequantize_e4m3(oracle.quantize_e4m3(V[:, h], "bf16", vs[h]), vs[h]) for h in range(2)], 1)
+    # the same attention on the dequantised contiguous arrays, by brute force;
+    # the codes are decoded by torch's float8_e4m3fn and multiplied by the
+    # float32 scale here, not by the oracle's dequantisation
+    Kd = np.stack([_torch_dequant(oracle.quantize_e4m3(K[:, h], "bf16", ks[h]), ks[h]) for h in range(2)], 1)
+    Vd = np.stack([_torch_dequant(oracle.quantize_e4m3(V[:, h], "bf16", vs[h]), vs[h]) for h in range(2)], 1)
     qd = oracle.widen(q, "bf16")
     for i, (b, h) in enumerate(rows):
         s = [0.25 * float(qd[b, h] @ Kd[b, h // 4, t]) for t in range(lens[b])]
@@ -459,6 +461,115 @@ def test_fp8_attention_is_attention_on_dequantised_values():
         assert np.all(np.abs(c - y) <= half)
 
 
+def _torch_dequant(codes, scale):
+    """value = code's E4M3 value (torch's float8_e4m3fn decoding) x float32(scale)."""
+    v = torch.from_numpy(np.ascontiguousarray(codes, np.uint8)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return v * float(np.float32(scale))
+
+
+def _torch_quant(x_f32, scale):
+    """E4M3 code of float32(x) / float32(scale) by torch: the float32 quotient,
+    clamped to +-448 (saturation), then torch's float8_e4m3fn rounding."""
+    y = torch.from_numpy(np.asarray(x_f32, np.float32)) / torch.tensor(np.float32(scale))
+    return y.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _dequant_pins_pass():
+    """dequantize_e4m3 against closed forms: value = E4M3(code) x scale, with
+    the scale as the float32 the library stores (design.babushkai.com
+    "GPU推論の内部構造", section "KVキャッシュの台帳": FP8 codes with a scale)."""
+    for s in (1.0, 0.25, 0.1, 0.0137, 3.5):
+        s32 = float(np.float32(s))
+        d = oracle.dequantize_e4m3
+        checks = [
+            (0x38, s32),                 # 0.0111.000 = 1
+            (0x7E, 448.0 * s32),         # 0.1111.110 = largest finite
+            (0xB8, -s32),                # sign bit
+            (0x40, 2.0 * s32),           # 0.1000.000 = 2
+            (0x30, 0.5 * s32),           # 0.0110.000 = 1/2
+            (0x3C, 1.5 * s32),           # 0.0111.100 = 1 + 4/8
+        ]
+        checks += [(k, k * 2.0 ** -9 * s32) for k in range(1, 8)]       # subnormals k 2^-9
+        checks += [(0x80 | k, -k * 2.0 ** -9 * s32) for k in range(1, 8)]
+        for code, want in checks:
+            if d(np.array([code], np.uint8), s)[0] != want:
+                return False
+        if d(np.array([0x00], np.uint8), s)[0] != 0.0 or not np.isnan(d(np.array([0x7F], np.uint8), s)[0]):
+            return False
+    return True
+
+
+def test_dequantize_closed_forms():
+    assert _dequant_pins_pass()
+
+
+def test_dequantize_equals_torch_decode_times_float32_scale():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    for s in (0.004, 0.0199, 0.1, 1.0, 7.25):
+        assert np.array_equal(oracle.dequantize_e4m3(codes, s), _torch_dequant(codes, s))
+
+
+def test_quantize_then_dequantize_within_half_a_step():
+    """|dequantize(quantize(x, s), s) - x| <= s * (half the E4M3 spacing at
+    x / s) + |x| 2^-23 (the float32 rounding of the quotient), for |x / s| <= 448."""
+    g = torch.Generator().manual_seed(5)
+    for s in (0.004, 0.02, 0.3):
+        x = (torch.randn(50000, generator=g) * 3.0).to(torch.bfloat16)
+        xb = bits_of(x)
+        xv = oracle.widen(xb, "bf16")
+        keep = np.abs(xv / s) <= 440.0
+        got = oracle.dequantize_e4m3(oracle.quantize_e4m3(xb, "bf16", s), s)
+        y = np.abs(xv / float(np.float32(s)))
+        half = 0.5 * 2.0 ** (np.floor(np.log2(np.maximum(y, 2.0 ** -6))) - 3)
+        bound = float(np.float32(s)) * half + np.abs(xv) * 2.0 ** -23
+        assert np.all(np.abs(got - xv)[keep] <= bound[keep])
+        # and outside the range the value saturates at +-448 s
+        big = np.abs(xv / s) > 470.0
+        if big.any():
+            assert np.all(np.abs(got[big]) == 448.0 * float(np.float32(s)))
+
+
+def _fp8_append_case():
+    """Two KV heads whose K and V scales differ by orders of magnitude, three
+    tokens (one skipped) in a pool of 3 blocks of 4 slots."""
+    g = torch.Generator().manual_seed(11)
+    kn = (torch.randn(3, 2, 16, generator=g) * torch.tensor([0.5, 40.0]).view(1, 2, 1)).to(torch.bfloat16)
+    vn = (torch.randn(3, 2, 16, generator=g) * torch.tensor([20.0, 0.02]).view(1, 2, 1)).to(torch.bfloat16)
+    ks = np.array([0.003, 0.25], np.float32)
+    vs = np.array([0.09, 0.0001], np.float32)
+    slots = np.array([9, -1, 2], np.int32)
+    kc = np.full((3, 2, 4, 16), 0x7F, np.uint8)
+    vc = np.full((3, 2, 4, 16), 0x7F, np.uint8)
+    return kn, vn, ks, vs, slots, kc, vc
+
+
+def _fp8_append_pin_passes():
+    """kv_append_fp8 against codes built by torch: token i, KV head h holds
+    E4M3(float32(k) / k_scale[h]) in k_cache[slot // 4][h][slot % 4] and
+    E4M3(float32(v) / v_scale[h]) in v_cache likewise; other slots keep their
+    bytes."""
+    kn, vn, ks, vs, slots, kc, vc = _fp8_append_case()
+    k_out, v_out = oracle.kv_append_fp8(kc, vc, bits_of(kn), bits_of(vn), slots, 4, ks, vs, "bf16")
+    k_want, v_want = kc.copy(), vc.copy()
+    for i, slot in enumerate(slots):
+        if slot < 0:
+            continue
+        for h in range(2):
+            k_want[slot // 4, h, slot % 4] = _torch_quant(kn[i, h].float().numpy(), ks[h])
+            v_want[slot // 4, h, slot % 4] = _torch_quant(vn[i, h].float().numpy(), vs[h])
+    return np.array_equal(k_out, k_want) and np.array_equal(v_out, v_want)
+
+
+def test_fp8_append_uses_each_heads_own_k_and_v_scale():
+    assert _fp8_append_pin_passes()
+    kn, vn, ks, vs, slots, kc, vc = _fp8_append_case()
+    k_out, _ = oracle.kv_append_fp8(kc, vc, bits_of(kn), bits_of(vn), slots, 4, ks, vs, "bf16")
+    # the values really do depend on the scale chosen: head 0's K with head 1's scale differs
+    assert not np.array_equal(k_out[2, 0, 1], _torch_quant(kn[0, 0].float().numpy(), ks[1]))
+    # untouched slots keep the NaN code
+    assert np.all(k_out[0, :, 0] == 0x7F) and np.all(k_out[1] == 0x7F)
+
+
 def _fp8_pins_pass():
     """The E4M3 pins above, as a function of the current oracle."""
     codes = np.arange(256, dtype=np.uint8)
@@ -471,7 +582,9 @@ def _fp8_pins_pass():
     x = x[np.abs(x) < 448]
     if not np.array_equal(oracle.e4m3_encode(x), torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()):
         return False
-    return list(oracle.e4m3_encode(np.array([1e9, -1e9], np.float32))) == [0x7E, 0xFE]
+    if list(oracle.e4m3_encode(np.array([1e9, -1e9], np.float32))) != [0x7E, 0xFE]:
+        return False
+    return _dequant_pins_pass() and _fp8_append_pin_passes()
 
 
 def _truncating_encode(x, f=oracle.e4m3_encode):
@@ -487,6 +600,15 @@ FP8_MUTATIONS = {
     "no saturation": ("e4m3_encode", lambda x, f=oracle.e4m3_encode: np.where(np.abs(np.asarray(x, np.float32)) > 448, 0x7F, f(x)).astype(np.uint8)),
     "round toward zero": ("e4m3_encode", _truncating_encode),
     "subnormals flushed": ("e4m3_decode", lambda c, f=oracle.e4m3_decode: np.where((np.asarray(c) & 0x78) == 0, 0.0, f(c))),
+    "dequantise by division": ("dequantize_e4m3", lambda c, s, f=oracle.e4m3_decode: f(c) / float(np.float32(s))),
+    "dequantise with a float64 scale": ("dequantize_e4m3", lambda c, s, f=oracle.e4m3_decode: f(c) * float(s)),
+    "append: K and V scales swapped": (
+        "kv_append_fp8", lambda kc, vc, kn, vn, sl, bs, ks, vs, dt, f=oracle.kv_append_fp8: f(kc, vc, kn, vn, sl, bs, vs, ks, dt)),
+    "append: KV head index off by one": (
+        "kv_append_fp8", lambda kc, vc, kn, vn, sl, bs, ks, vs, dt, f=oracle.kv_append_fp8:
+        f(kc, vc, kn, vn, sl, bs, np.roll(ks, 1), np.roll(vs, 1), dt)),
+    "append: quantise by multiplication": (
+        "quantize_e4m3", lambda b, dt, s, f=oracle.quantize_e4m3: f(b, dt, 1.0 / float(s))),
 }
 
 
