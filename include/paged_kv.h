@@ -91,7 +91,11 @@ typedef struct pkv_dims {
 } pkv_dims;
 
 /*
- * KV append (device).  For each token i in [0, num_tokens) with
+ * KV append (device).  Passage: "How to Scale Your Model, Part 7: Inference",
+ * section "Transformer 推論の基礎: Prefill と Generation" (each generated token's
+ * K/V is stored in the cache for later steps), through the slot of youngju.dev's
+ * PagedAttention layout figure (virtual slot -> block table -> physical block).
+ * For each token i in [0, num_tokens) with
  * slot_mapping[i] >= 0, copies k_new[i][:][:] into k_cache at slot
  * slot_mapping[i] (block slot / block_size, offset slot % block_size, every KV
  * head) and v_new[i] into v_cache likewise.  A negative slot skips the token.
@@ -105,7 +109,12 @@ int paged_kv_append(const void* k_new, const void* v_new, const int32_t* slot_ma
                     const pkv_dims* dims, void* stream);
 
 /*
- * Paged decode attention (device).  For every sequence b and query head h,
+ * Paged decode attention (device).  Passages: youngju.dev "LLM サービング最適化
+ * 完全ガイド", AttentionWithKVCache listing (one query token: softmax(q K^T /
+ * sqrt(d_k)) V); kasblo.com "vLLMとは？", section "PagedAttentionはKV Cacheを
+ * blockで管理する" (K/V read through the block table); the GQA figure of "How to
+ * Scale Your Model, Part 7", section "生成スループット/レイテンシ改善のテクニック".
+ * For every sequence b and query head h,
  *   out[b][h] = sum_t softmax_t(scale * q[b][h] . K_t) V_t,  t in [0, context_lens[b]),
  * where K_t / V_t is token t of sequence b for KV head h / g, read from
  * physical block block_tables[b][t / block_size] at offset t % block_size.
@@ -233,7 +242,10 @@ int paged_decode_step_fp8_from_host(const pkv_step_buffers* bufs, void* k_cache,
  *    splits * (head_dim + 1) * 4 bytes, each region rounded up to 256) is
  *    rejected with PKV_ERR_INVALID_ARG and a message giving both sizes.
  *  - The first call on a device looks up the array's device address (with that
- *    device current); make that first call before any stream capture.
+ *    device current); make that first call before any stream capture.  The
+ *    stream must belong to the current device (PKV_ERR_INVALID_ARG
+ *    otherwise).  The address is kept for the life of the process: calls made
+ *    after a cudaDeviceReset of that device are not supported.
  *  - Every call on a device shares the one array and nothing in it needs to
  *    start at zero, but calls that overlap on the GPU (other streams, other
  *    host threads) race on it: serialise them, e.g. on one stream.
@@ -389,30 +401,36 @@ int paged_kv_slot_mapping(const int32_t* block_tables, const int32_t* context_le
  * ---------------------------------------------------------------------- */
 typedef struct pkv_block_allocator pkv_block_allocator;
 
-/* Returns NULL if num_blocks <= 0 or block_size <= 0. */
+/* A pool of num_blocks free blocks (kasblo.com "vLLMとは？", section
+ * "blockはrequestの成長に合わせて割り当てる": blocks come from a pool).
+ * Returns NULL if num_blocks <= 0 or block_size <= 0. */
 pkv_block_allocator* block_allocator_create(int32_t num_blocks, int32_t block_size, uint64_t seed);
 void block_allocator_destroy(pkv_block_allocator* a);
 
-/* New sequence holding num_tokens tokens: ceil(num_tokens / block_size) blocks.
+/* New sequence holding num_tokens tokens: ceil(num_tokens / block_size) blocks
+ * (kasblo.com "vLLMとは？", section "blockはrequestの成長に合わせて割り当てる").
  * PKV_ERR_NO_BLOCKS (and no change) if the pool is short. */
 int block_allocator_add_seq(pkv_block_allocator* a, int32_t num_tokens, int32_t* seq_id);
 
 /* New sequence of num_tokens tokens whose first prefix_tokens tokens are the
- * blocks of src_seq (reference counts raised, nothing copied).  prefix_tokens
+ * blocks of src_seq (reference counts raised, nothing copied; kasblo.com
+ * "vLLMとは？", section "block共有とAutomatic Prefix Caching").  prefix_tokens
  * must be a multiple of block_size and <= the length of src_seq. */
 int block_allocator_fork_prefix(pkv_block_allocator* a, int32_t src_seq, int32_t prefix_tokens,
                                 int32_t num_tokens, int32_t* seq_id);
 
 /* A new sequence holding the first prefix_tokens tokens of src_seq (any
- * count 0..length): it shares the ceil(prefix_tokens / block_size) blocks that
+ * count 0..length; kasblo.com "vLLMとは？", section "block共有とAutomatic
+ * Prefix Caching": shared blocks with reference counts): it shares the ceil(prefix_tokens / block_size) blocks that
  * hold them (their reference counts rise), the last possibly partly filled.
  * Parallel sampling forks the whole prompt; a request reusing part of
  * another's context forks that part.  Its writes go through the _cow calls
  * below, which copy a shared block before writing into it. */
 int block_allocator_fork(pkv_block_allocator* a, int32_t src_seq, int32_t prefix_tokens, int32_t* seq_id);
 
-/* append_slot with copy-on-write: if the block that receives the token is
- * shared, the sequence gets a fresh block in its place (the old block loses a
+/* append_slot with copy-on-write (kasblo.com "vLLMとは？", section "block共有と
+ * Automatic Prefix Caching": a shared block is copied when one holder writes
+ * into it): if the block that receives the token is shared, the sequence gets a fresh block in its place (the old block loses a
  * reference) and *num_copies = 1 with copy_pair = {old, fresh}: the caller
  * copies the block (paged_kv_copy_blocks) before writing the token.  Else
  * *num_copies = 0.  PKV_ERR_NO_BLOCKS (nothing changed) if a block is needed
@@ -420,7 +438,7 @@ int block_allocator_fork(pkv_block_allocator* a, int32_t src_seq, int32_t prefix
 int block_allocator_append_slot_cow(pkv_block_allocator* a, int32_t seq_id, int32_t* slot,
                                     int32_t* copy_pair, int32_t* num_copies);
 
-/* step_batch with copy-on-write: as block_allocator_step_batch, but a
+/* step_batch with copy-on-write (the same passage): as block_allocator_step_batch, but a
  * sequence whose next token lands in a shared block gets a private copy
  * instead of an error.  copy_pairs (int32[n][2], host) receives the
  * *num_copies {src, dst} block copies to perform before this step's append;
@@ -432,17 +450,21 @@ int block_allocator_step_batch_cow(pkv_block_allocator* a, const int32_t* slot_s
                                    int32_t* copy_pairs, int32_t* num_copies);
 
 /* Grow seq_id by one token and return its slot (block * block_size + offset).
- * Takes a new block when the last one is full.  PKV_ERR_SHARED_BLOCK if the
+ * Takes a new block when the last one is full (kasblo.com "vLLMとは？", section
+ * "blockはrequestの成長に合わせて割り当てる": one more block when the current
+ * one fills).  PKV_ERR_SHARED_BLOCK if the
  * token would land in a partly filled block that another sequence shares. */
 int block_allocator_append_slot(pkv_block_allocator* a, int32_t seq_id, int32_t* slot);
 
-/* One decode step's growth for a batch: block_allocator_append_slot for each
+/* One decode step's growth for a batch (the same passage): block_allocator_append_slot for each
  * of seq_ids[0..n), slots[i] receiving sequence i's new slot.  All or nothing:
  * PKV_ERR_NO_BLOCKS / PKV_ERR_SHARED_BLOCK / PKV_ERR_INVALID_ARG (a sequence
  * not live or listed twice) leave the allocator unchanged. */
 int block_allocator_append_slots(pkv_block_allocator* a, const int32_t* seq_ids, int32_t n, int32_t* slots);
 
-/* The host side of one continuous-batching decode step, in one call: for a
+/* The host side of one continuous-batching decode step (magi "Inference
+ * Batching", continuous batching; kasblo.com section "blockはrequestの成長に
+ * 合わせて割り当てる"), in one call: for a
  * batch of n slots (slot_seq_ids[i] = a live sequence, or -1 for an empty
  * slot) grow every listed sequence by one token and write row i of
  * tables (int32[n][max_blocks], -1 padded) and context_lens[i] (0 for an empty
@@ -451,17 +473,23 @@ int block_allocator_append_slots(pkv_block_allocator* a, const int32_t* seq_ids,
 int block_allocator_step_batch(pkv_block_allocator* a, const int32_t* slot_seq_ids, int32_t n, int32_t max_blocks,
                                int32_t* tables, int32_t* context_lens);
 
-/* Drop seq_id; blocks whose count reaches zero return to the pool. */
+/* Drop seq_id; blocks whose count reaches zero return to the pool (kasblo.com
+ * "vLLMとは？", section "blockはrequestの成長に合わせて割り当てる": a finished
+ * request's blocks go back to the pool). */
 int block_allocator_free_seq(pkv_block_allocator* a, int32_t seq_id);
 
-/* Export rows for seq_ids[0..n): tables int32[n][max_blocks] (-1 padded) and
+/* The block tables themselves (kasblo.com "vLLMとは？", section
+ * "PagedAttentionはKV Cacheをblockで管理する": logical block j -> physical
+ * block).  Export rows for seq_ids[0..n): tables int32[n][max_blocks] (-1 padded) and
  * context_lens int32[n].  PKV_ERR_INVALID_ARG if a sequence needs more than
  * max_blocks blocks. */
 int block_allocator_block_tables(const pkv_block_allocator* a, const int32_t* seq_ids, int32_t n,
                                  int32_t max_blocks, int32_t* tables, int32_t* context_lens);
 
+/* Free blocks left in the pool. */
 int32_t block_allocator_num_free(const pkv_block_allocator* a);
-/* Reference count of a physical block (0 = free); -1 if out of range. */
+/* Reference count of a physical block (0 = free; kasblo.com section "block共有と
+ * Automatic Prefix Caching"); -1 if out of range. */
 int32_t block_allocator_refcount(const pkv_block_allocator* a, int32_t block);
 /* Tokens held by a live sequence; -1 if seq_id is not live. */
 int32_t block_allocator_seq_len(const pkv_block_allocator* a, int32_t seq_id);

@@ -65,6 +65,17 @@ def make_dims(q_or_new: torch.Tensor, k_cache: torch.Tensor, block_tables: Optio
                    dtype=_DTYPE_CODE[k_cache.dtype])
 
 
+def _check_attention_shapes(q: torch.Tensor, out: torch.Tensor, k_cache: torch.Tensor,
+                            block_tables: torch.Tensor, context_lens: torch.Tensor) -> None:
+    """Shape checks shared by the one-token attention calls, made before any
+    launch: the kernels read context_lens[b] and row b of block_tables for
+    every sequence b of q, so both must have a row per sequence."""
+    if out.shape != q.shape or q.dim() != 3 or q.shape[2] != k_cache.shape[3]:
+        raise ValueError("q / out must be [num_seqs][num_q_heads][head_dim]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != q.shape[0] or context_lens.shape != (q.shape[0],):
+        raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
+
+
 def paged_kv_append(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
                     k_cache: torch.Tensor, v_cache: torch.Tensor, stream=None) -> None:
     """Store token i's K/V (k_new[i], v_new[i]: [Hkv][D]) at slot slot_mapping[i]
@@ -114,10 +125,7 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     if out is None:
         out = torch.empty_like(q)
     _need_cuda("out", out, q.dtype)
-    if out.shape != q.shape or q.dim() != 3 or q.shape[2] != k_cache.shape[3]:
-        raise ValueError("q / out must be [num_seqs][num_q_heads][head_dim]")
-    if block_tables.dim() != 2 or block_tables.shape[0] != q.shape[0] or context_lens.shape != (q.shape[0],):
-        raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
+    _check_attention_shapes(q, out, k_cache, block_tables, context_lens)
     dims = make_dims(q, k_cache, block_tables)
     need = int(lib().paged_decode_workspace_bytes(ctypes.byref(dims), num_splits))
     if need and workspace is None:
@@ -145,8 +153,7 @@ def paged_decode_attention_no_alloc(q: torch.Tensor, k_cache: torch.Tensor, v_ca
         _need_cuda(n, t, k_cache.dtype)
     _need_cuda("block_tables", block_tables, torch.int32)
     _need_cuda("context_lens", context_lens, torch.int32)
-    if out.shape != q.shape or q.dim() != 3 or q.shape[2] != k_cache.shape[3]:
-        raise ValueError("q / out must be [num_seqs][num_q_heads][head_dim]")
+    _check_attention_shapes(q, out, k_cache, block_tables, context_lens)
     dims = make_dims(q, k_cache, block_tables)
     _check(lib().paged_decode_attention_no_alloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                                  _ptr(context_lens), float(scale), _ptr(out), num_splits,
@@ -171,10 +178,7 @@ def paged_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
     _need_cuda("out", out, q.dtype)
     if k_new.shape != (q.shape[0], k_cache.shape[1], k_cache.shape[3]) or v_new.shape != k_new.shape:
         raise ValueError("k_new / v_new must be [num_seqs][num_kv_heads][head_dim]")
-    if out.shape != q.shape or q.dim() != 3 or q.shape[2] != k_cache.shape[3]:
-        raise ValueError("q / out must be [num_seqs][num_q_heads][head_dim]")
-    if block_tables.dim() != 2 or block_tables.shape[0] != q.shape[0] or context_lens.shape != (q.shape[0],):
-        raise ValueError("block_tables must be [num_seqs][max_blocks], context_lens [num_seqs]")
+    _check_attention_shapes(q, out, k_cache, block_tables, context_lens)
     dims = make_dims(q, k_cache, block_tables)
     need = int(lib().paged_decode_workspace_bytes(ctypes.byref(dims), num_splits))
     if need and workspace is None:

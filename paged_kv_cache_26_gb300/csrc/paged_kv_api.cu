@@ -984,14 +984,22 @@ namespace {
 
 // Device address of the scratch array for the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is looked up
-// once per device (with that device current) and kept.
-int static_scratch(void** ptr) {
+// once per device (with that device current) and kept.  The stream must
+// belong to the current device: the address is that device's, and kernels on
+// another device's stream would write to the wrong GPU.
+int static_scratch(cudaStream_t stream, void** ptr) {
   static void* addr[kMaxDevices] = {};
   static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "no_alloc: cudaGetDevice");
   if (dev >= kMaxDevices) return pkv_fail(PKV_ERR_UNSUPPORTED, "no_alloc: device index too large");
+  int stream_dev = dev;
+  e = cudaStreamGetDevice(stream, &stream_dev);
+  if (e != cudaSuccess) return cuda_fail(e, "no_alloc: cudaStreamGetDevice");
+  if (stream_dev != dev)
+    return pkv_fail(PKV_ERR_INVALID_ARG, "no_alloc: the stream belongs to device " + std::to_string(stream_dev) +
+                                             " but device " + std::to_string(dev) + " is current");
   std::lock_guard<std::mutex> lock(mu);
   if (!addr[dev]) {
     void* p = nullptr;
@@ -1028,7 +1036,7 @@ extern "C" int paged_decode_attention_no_alloc(const void* q, const void* k_cach
                         " bytes of split scratch; the library's static scratch holds " +
                         std::to_string(kStaticScratchBytes) + " (use fewer splits or paged_decode_attention)");
   void* scratch = nullptr;
-  rc = static_scratch(&scratch);
+  rc = static_scratch(static_cast<cudaStream_t>(stream), &scratch);
   if (rc != PKV_OK) return rc;
   return decode_impl(q, nullptr, nullptr, const_cast<void*>(k_cache), const_cast<void*>(v_cache), block_tables,
                      context_lens, scale, out, n, scratch, kStaticScratchBytes, dims,

@@ -175,3 +175,21 @@ def test_slot_mapping_multi_matches_oracle():
     assert np.array_equal(got, oracle.slot_mapping_multi(tables, lens, n, 16))
     with pytest.raises(pkv.PagedKVError):
         pkv.paged_kv_slot_mapping_multi(tables, np.array([97] * B, np.int32), n)   # past the table
+
+
+def test_attention_shape_checks_refuse_short_lengths_and_tables_before_any_launch():
+    """The kernels read context_lens[b] and block_tables row b for every
+    sequence b of q: shorter tensors are refused by the binding (no GPU
+    needed: the check runs before any call into the library)."""
+    import torch
+    from paged_kv_cache_26_gb300.api import _check_attention_shapes
+    q = torch.zeros(4, 8, 64, dtype=torch.float16)
+    kc = torch.zeros(32, 2, 16, 64, dtype=torch.float16)
+    bt = torch.zeros(4, 7, dtype=torch.int32)
+    cl = torch.zeros(4, dtype=torch.int32)
+    _check_attention_shapes(q, torch.empty_like(q), kc, bt, cl)
+    for bad_bt, bad_cl in ((bt, cl[:3]), (bt[:3], cl), (bt[0], cl), (bt, cl.view(4, 1))):
+        with pytest.raises(ValueError):
+            _check_attention_shapes(q, torch.empty_like(q), kc, bad_bt, bad_cl)
+    with pytest.raises(ValueError):
+        _check_attention_shapes(q, torch.empty(4, 8, 32, dtype=torch.float16), kc, bt, cl)
