@@ -49,12 +49,15 @@
  *
  * The automatic (persistent) attention path launches its kernels as
  * programmatic dependents of the kernel before them in the stream: they may
- * start while that kernel finishes, and read their inputs q, block_tables and
- * context_lens before waiting for it; the cache, the workspace and out are
- * touched only after the wait.  A kernel that writes those inputs right
- * before the call and signals programmatic launch completion early
- * (cudaTriggerProgrammaticLaunchCompletion) must not do so before it has
- * written them; kernels that never signal it, and copies, are always safe.
+ * start while that kernel finishes.  Before waiting for it they read
+ * block_tables and context_lens (and prefetch q) only as a guess, to start
+ * their first loads early; after the wait they read the lengths and the
+ * tables they started on again and rebuild everything derived from them if
+ * anything changed, and only then use them.  So inputs written on the GPU
+ * right before the call (a serving loop advancing context_lens, a new block
+ * id stored into block_tables) are always seen, whether or not the kernel
+ * that writes them signals programmatic launch completion early.  The cache,
+ * the workspace, q and out are touched only after the wait.
  */
 #ifndef PAGED_KV_H_
 #define PAGED_KV_H_
@@ -377,6 +380,23 @@ int paged_kv_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pair
  * returns PKV_ERR_TIMEOUT and the device stays usable.  Lets a caller (and the
  * tests) check the failure path without a real hang. */
 int paged_kv_selftest_wait(void* stream);
+
+/* Self-test of the kernels' re-check of their early inputs (device); no
+ * counterpart on the pages.  paged_decode_step on the automatic path, except
+ * that the decode and merge prologues -- which run before the grid wait, while
+ * the previous kernel in the stream may still be writing the inputs -- read
+ * stale_block_tables / stale_context_lens (same shapes as block_tables /
+ * context_lens, device or mapped host memory) instead of the real inputs.
+ * Such a read stands in for inputs whose latest writes are not yet visible.
+ * After their wait the kernels read block_tables / context_lens again and
+ * rebuild what they derived from the stale values, so out and the caches must
+ * be exactly what paged_decode_step gives on the real inputs.  Arguments and
+ * errors otherwise as paged_decode_step with num_splits = 0. */
+int paged_kv_selftest_stale_prologue(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                                     void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+                                     const int32_t* stale_block_tables, const int32_t* stale_context_lens,
+                                     float scale, void* out, void* workspace, size_t workspace_bytes,
+                                     const pkv_dims* dims, void* stream);
 
 /* Synchronises `stream`, then reads and clears this device's error word.
  * Returns PKV_OK, PKV_ERR_OUT_OF_RANGE, PKV_ERR_TIMEOUT or PKV_ERR_CUDA. */

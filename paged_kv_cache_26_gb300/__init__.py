@@ -8,7 +8,7 @@ from .api import (BlockAllocator, PagedKVError, make_workspace, paged_decode_att
                   paged_decode_attention_fp8, paged_decode_attention_no_alloc, paged_decode_step_fp8,
                   paged_kv_append_fp8, paged_decode_attention_multi, paged_decode_step_multi,
                   paged_decode_multi_workspace_bytes, paged_decode_multi_resolve_splits, paged_kv_slot_mapping_multi,
-                  paged_kv_copy_blocks, paged_kv_selftest_wait,
+                  paged_kv_copy_blocks, paged_kv_selftest_wait, paged_kv_selftest_stale_prologue,
                   paged_decode_resolve_splits, paged_decode_step, paged_decode_step_from_host,
                   paged_decode_step_fp8_from_host, paged_decode_step_multi_from_host,
                   paged_decode_workspace_bytes,
@@ -24,5 +24,5 @@ __all__ = [
     "paged_kv_append_fp8", "paged_decode_attention_fp8", "paged_decode_step_fp8",
     "paged_decode_attention_multi", "paged_decode_step_multi", "paged_decode_multi_workspace_bytes",
     "paged_decode_multi_resolve_splits", "paged_kv_slot_mapping_multi", "paged_kv_copy_blocks",
-    "paged_kv_selftest_wait",
+    "paged_kv_selftest_wait", "paged_kv_selftest_stale_prologue",
 ]

@@ -482,6 +482,40 @@ def paged_kv_selftest_wait(stream=None) -> None:
     _check(lib().paged_kv_selftest_wait(_stream(stream)), "paged_kv_selftest_wait")
 
 
+def paged_kv_selftest_stale_prologue(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                                     k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                     context_lens: torch.Tensor, stale_block_tables: torch.Tensor,
+                                     stale_context_lens: torch.Tensor, scale: float,
+                                     out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                                     stream=None) -> torch.Tensor:
+    """paged_decode_step (automatic path) whose kernels read the stale
+    tables / lengths before their grid wait, as if the real ones were still
+    being written: the result must be that of the real inputs.  Returns out."""
+    for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need_cuda(n, t, k_cache.dtype)
+    for n, t in (("block_tables", block_tables), ("context_lens", context_lens),
+                 ("stale_block_tables", stale_block_tables), ("stale_context_lens", stale_context_lens)):
+        _need_cuda(n, t, torch.int32)
+    if out is None:
+        out = torch.empty_like(q)
+    _need_cuda("out", out, q.dtype)
+    _check_attention_shapes(q, out, k_cache, block_tables, context_lens)
+    if stale_block_tables.shape != block_tables.shape or stale_context_lens.shape != context_lens.shape:
+        raise ValueError("stale inputs must have the shapes of the real ones")
+    if k_new.shape != (q.shape[0], k_cache.shape[1], k_cache.shape[3]) or v_new.shape != k_new.shape:
+        raise ValueError("k_new / v_new must be [num_seqs][num_kv_heads][head_dim]")
+    dims = make_dims(q, k_cache, block_tables)
+    need = int(lib().paged_decode_workspace_bytes(ctypes.byref(dims), 0))
+    if need and workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().paged_kv_selftest_stale_prologue(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        _ptr(stale_block_tables), _ptr(stale_context_lens), float(scale), _ptr(out), _ptr(workspace), ws_bytes,
+        ctypes.byref(dims), _stream(stream)), "paged_kv_selftest_stale_prologue")
+    return out
+
+
 def paged_kv_check_status(stream=None) -> None:
     """Synchronise the stream and raise if a kernel flagged an error."""
     _check(lib().paged_kv_check_status(_stream(stream)), "paged_kv_check_status")

@@ -30,6 +30,7 @@
 
 #include "paged_kv.h"
 #include "pkv_errors.h"
+#include "pkv_internal.h"
 
 namespace {
 constexpr int kSlotRing = 4;
@@ -216,12 +217,10 @@ int decode_engine_step(pkv_decode_engine* e, const void* q, const void* k_new, c
     rc = paged_kv_copy_blocks(k_cache, v_cache, e->pairs(i, true), ncopy, dims, e->k_scale ? 1 : 2, stream);
     if (rc != PKV_OK) return rc;
   }
-  if (e->k_scale)
-    rc = paged_decode_step_fp8(q, k_new, v_new, k_cache, v_cache, e->k_scale, e->v_scale, e->tables(i, true),
-                               e->lens(i, true), scale, out, workspace, workspace_bytes, dims, stream);
-  else
-    rc = paged_decode_step(q, k_new, v_new, k_cache, v_cache, e->tables(i, true), e->lens(i, true), scale, out, 0,
-                           workspace, workspace_bytes, dims, stream);
+  // The tables and lengths were written by the host above and no kernel writes
+  // them: the kernels may trust what they read before their grid wait.
+  rc = decode_step_host_written(q, k_new, v_new, k_cache, v_cache, e->k_scale, e->v_scale, e->tables(i, true),
+                                e->lens(i, true), scale, out, workspace, workspace_bytes, dims, stream);
   // Recorded even after a failed launch, so that the entry is never reused
   // while an earlier kernel (the block copy) may still read it.
   const cudaError_t ce = cudaEventRecord(e->step_ev[i], static_cast<cudaStream_t>(stream));

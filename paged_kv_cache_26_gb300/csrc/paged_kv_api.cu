@@ -17,6 +17,7 @@
 #include "multi_query.cuh"
 #include "paged_kv_kernels.cuh"
 #include "pkv_errors.h"
+#include "pkv_internal.h"
 
 namespace {
 
@@ -324,7 +325,7 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, void* k_cac
                 int32_t num_splits, void* workspace, size_t workspace_bytes, const pkv_dims* d,
                 cudaStream_t stream, bool f8 = false, const float* k_scale = nullptr,
                 const float* v_scale = nullptr, bool pdl = true, const int32_t* pre_lens = nullptr,
-                const int32_t* pre_tables = nullptr) {
+                const int32_t* pre_tables = nullptr, bool recheck = true) {
   int rc = check_dims(d, true);
   if (rc != PKV_OK) return rc;
   if (f8) {
@@ -383,6 +384,7 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, void* k_cac
   args.pre_context_lens = pre_lens;
   args.pre_block_tables = pre_tables;
   args.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  args.recheck = recheck ? 1 : 0;
   args.num_seqs = d->num_seqs;
   args.num_q_heads = d->num_q_heads;
   args.num_kv_heads = d->num_kv_heads;
@@ -578,6 +580,7 @@ int decode_multi_impl(const void* q, const void* k_new, const void* v_new, void*
   args.part_lse = need ? reinterpret_cast<float*>(ws + align256(rows * splits * d->head_dim * sizeof(float)))
                        : nullptr;
   args.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  args.recheck = 0;  // the multi-token kernels are stream-ordered: no early reads
   args.num_seqs = d->num_seqs;
   args.num_q_heads = d->num_q_heads;
   args.num_kv_heads = d->num_kv_heads;
@@ -773,10 +776,12 @@ int step_from_host(const pkv_step_buffers* s, int32_t q_len, void* k_cache, void
     else
       pre_lens = pre_tables = nullptr;
     const bool f8 = k_scale != nullptr;
+    // The host buffers hold their final values before this call (the caller
+    // wrote them), so the early reads need no re-check after the grid wait.
     rc = decode_impl(s->q_dev, s->k_new_dev, s->v_new_dev, k_cache, v_cache, s->block_tables_dev,
                      s->context_lens_dev, scale, s->out_dev, num_splits, workspace, workspace_bytes, d, stream, f8,
                      k_scale, v_scale, early, reinterpret_cast<const int32_t*>(pre_lens),
-                     reinterpret_cast<const int32_t*>(pre_tables));
+                     reinterpret_cast<const int32_t*>(pre_tables), pre_lens == nullptr);
   }
   if (rc != PKV_OK) return rc;
   const HostRange d2h[] = {{s->out_dev, s->out_host, q_bytes}};
@@ -784,6 +789,16 @@ int step_from_host(const pkv_step_buffers* s, int32_t q_len, void* k_cache, void
 }
 
 }  // namespace
+
+int decode_step_host_written(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                             const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                             const int32_t* context_lens, float scale, void* out, void* workspace,
+                             size_t workspace_bytes, const pkv_dims* dims, void* stream) {
+  if (!k_new || !v_new) return pkv_fail(PKV_ERR_INVALID_ARG, "decode_step: NULL k_new / v_new");
+  return decode_impl(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, out, 0, workspace,
+                     workspace_bytes, dims, static_cast<cudaStream_t>(stream), k_scale != nullptr, k_scale, v_scale,
+                     true, nullptr, nullptr, false);
+}
 
 extern "C" {
 
@@ -851,6 +866,19 @@ int paged_kv_selftest_wait(void* stream) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "wait_selftest_kernel launch");
   return PKV_OK;
+}
+
+int paged_kv_selftest_stale_prologue(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                                     void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+                                     const int32_t* stale_block_tables, const int32_t* stale_context_lens,
+                                     float scale, void* out, void* workspace, size_t workspace_bytes,
+                                     const pkv_dims* dims, void* stream) {
+  if (!stale_block_tables || !stale_context_lens || !aligned(stale_block_tables, 4) ||
+      !aligned(stale_context_lens, 4))
+    return pkv_fail(PKV_ERR_INVALID_ARG, "selftest_stale_prologue: stale inputs missing or misaligned");
+  return decode_impl(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, out, 0, workspace,
+                     workspace_bytes, dims, static_cast<cudaStream_t>(stream), false, nullptr, nullptr, true,
+                     stale_context_lens, stale_block_tables);
 }
 
 int paged_kv_append_fp8(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t num_tokens,

@@ -578,6 +578,9 @@ struct DecodeArgs {
   const float* k_scale;       // E4M3 pool only: f32[Hkv] scales of K and V codes
   const float* v_scale;
   float scale_log2;           // scale * log2(e)
+  int32_t recheck;            // persistent: 1 = the lengths / tables read before the grid wait may be stale
+                              // (device inputs a previous kernel may still write) and are read again after
+                              // it; 0 = they are final when the kernel starts (written by the host)
   int32_t num_seqs;
   int32_t num_q_heads;
   int32_t num_kv_heads;
@@ -589,8 +592,7 @@ struct DecodeArgs {
 };
 
 // Context length as the kernels see it: clamped to [0, max_blocks * 16].
-__device__ __forceinline__ int clamped_context(const int32_t* lens, int b, int max_blocks, bool flag) {
-  int ctx = lens[b];
+__device__ __forceinline__ int clamp_context(int ctx, int max_blocks, bool flag) {
   const int cap = max_blocks * kBlockSize;
   if (ctx < 0 || ctx > cap) {
     if (flag) flag_error(kErrContext);
@@ -598,12 +600,16 @@ __device__ __forceinline__ int clamped_context(const int32_t* lens, int b, int m
   }
   return ctx;
 }
+__device__ __forceinline__ int clamped_context(const int32_t* lens, int b, int max_blocks, bool flag) {
+  return clamp_context(lens[b], max_blocks, flag);
+}
 
-// Pool row of (physical block, KV head); a block id outside the pool is
-// flagged and mapped to a row range entirely outside the tensor (reads zeros).
-__device__ __forceinline__ int tile_row(int phys, int kvh, const DecodeArgs& a) {
+// Pool row of (physical block, KV head); a block id outside the pool maps to
+// a row range entirely outside the tensor (reads zeros) and, with `flag`, is
+// flagged.
+__device__ __forceinline__ int tile_row(int phys, int kvh, const DecodeArgs& a, bool flag = true) {
   if (phys < 0 || phys >= a.num_blocks) {
-    flag_error(kErrBlockId);
+    if (flag) flag_error(kErrBlockId);
     return -kBlockSize;
   }
   return (phys * a.num_kv_heads + kvh) * kBlockSize;
@@ -735,16 +741,17 @@ struct Partition {
 };
 
 // Exclusive prefix of blocks per sequence into s_P[0..B] and clamped contexts
-// into s_ctx[0..B), computed by the whole CTA (nthreads threads).
-__device__ __forceinline__ void context_prefix(const DecodeArgs& a, int* s_P, int* s_ctx, int* s_warp_sum,
-                                               int nthreads, bool flag) {
+// into s_ctx[0..B), computed by the whole CTA (nthreads threads) from `lens`.
+// Loads go to L2 (ld.global.cg), never to a per-SM cache that an earlier
+// read before the grid wait could have filled.
+__device__ __forceinline__ void context_prefix(const DecodeArgs& a, const int32_t* lens, int* s_P, int* s_ctx,
+                                               int* s_warp_sum, int nthreads, bool flag) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, B = a.num_seqs;
   const int per = (B + nthreads - 1) / nthreads;
   const int lo = min(B, tid * per), hi = min(B, lo + per);
   int local = 0;
   for (int b = lo; b < hi; ++b) {
-    const int32_t* lens = a.pre_context_lens ? a.pre_context_lens : a.context_lens;
-    const int ctx = clamped_context(lens, b, a.max_blocks, flag);
+    const int ctx = clamp_context(__ldcg(lens + b), a.max_blocks, flag);
     s_ctx[b] = ctx;
     local += (ctx + kBlockSize - 1) / kBlockSize;
   }
@@ -766,10 +773,33 @@ __device__ __forceinline__ void context_prefix(const DecodeArgs& a, int* s_P, in
   __syncthreads();
 }
 
+// context_prefix from the staged lengths, for the rare rebuild after the grid
+// wait: kept out of line so that it costs the kernels no registers.
+__device__ __noinline__ void context_prefix_again(const DecodeArgs& a, int* s_P, int* s_ctx, int* s_warp_sum,
+                                                  int nthreads) {
+  context_prefix(a, a.context_lens, s_P, s_ctx, s_warp_sum, nthreads, false);
+}
+
+// After the grid wait: do the lengths this CTA read before the wait (s_ctx)
+// still hold?  Each thread re-reads its share of context_lens from L2 (the
+// previous kernels' writes are visible now) and the CTA votes; the result is
+// the same in every thread.  With `flag`, out-of-range lengths are flagged
+// here, from the values the kernel finally uses.
+__device__ __forceinline__ bool context_changed(const DecodeArgs& a, const int* s_ctx, int nthreads, bool flag) {
+  const int tid = threadIdx.x, B = a.num_seqs;
+  const int per = (B + nthreads - 1) / nthreads;
+  const int lo = min(B, tid * per), hi = min(B, lo + per);
+  int diff = 0;
+  for (int b = lo; b < hi; ++b) diff |= clamp_context(__ldcg(a.context_lens + b), a.max_blocks, flag) != s_ctx[b];
+  return __syncthreads_or(diff) != 0;
+}
+
 // F8: the pool holds E4M3 codes (D = 128 only); the query, output and the
 // appended token's K/V stay fp16/bf16 and the append quantises in-kernel.
+// Registers are capped so that two 4-warp merge CTAs (64 registers a thread)
+// fit beside a decode CTA (8 warps x 192 registers) on an SM.
 template <typename T, int D, bool F8 = false>
-__global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
+__global__ void __maxnreg__(F8 ? 168 : 192)
     decode_persistent_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                              const DecodeArgs a) {
   static_assert(!F8 || D == 128, "the E4M3 path is built for head_dim 128");
@@ -802,10 +832,17 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
     fence_mbar_init();
   }
   // Inputs only (context lengths, and below the block tables and query rows)
-  // are read before the wait for the previous kernel in the stream.
-  context_prefix(a, s_P, s_ctx, s_warp_sum, NW * 32, blockIdx.x == 0);
+  // are read before the wait for the previous kernel in the stream.  What is
+  // read there is a guess: a previous kernel may still be writing the lengths
+  // or tables (a serving loop that advances context_lens on the GPU), and
+  // nothing makes its writes visible before the wait.  After the wait both
+  // are read again and everything derived from them is rebuilt if they
+  // changed (see below), so the guess only decides how early the first loads
+  // can start.  Errors are flagged from the values read after the wait.
+  context_prefix(a, a.pre_context_lens ? a.pre_context_lens : a.context_lens, s_P, s_ctx, s_warp_sum, NW * 32,
+                 !a.recheck && blockIdx.x == 0);
 
-  const Partition part(Hkv * s_P[B], gridDim.x * NW);
+  Partition part(Hkv * s_P[B], gridDim.x * NW);
   const int gw = blockIdx.x * NW + warp;
 
   // Sequence b, KV head kvh and block j of flattened block f: units are
@@ -831,32 +868,42 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
     prefetch_tensormap(&tmap_v);
   }
 
-  // Block tables: the prologue's source until the grid wait, then the staged ones.
+  // Block tables: the prologue's source until the grid wait, then the staged
+  // ones.  Read through L2 only (ld.global.cg), like the lengths.
   const int32_t* tables = a.pre_block_tables ? a.pre_block_tables : a.block_tables;
+  bool after_wait = !a.recheck;  // block ids are flagged only from values known to be final
 
   // ---- issue side: current segment [seg_s, seg_e) and a 32-block window of it,
-  // lane i describing block win_s + i (sequence, KV head, block j, pool row).
+  // lane i describing block win_s + i (sequence, KV head, block j, table entry,
+  // pool row).
   int seg, seg_s, seg_e;
-  part.head(gw, seg_s, seg_e);
-  seg = gw;
-  int win_s = seg_s, win_e = seg_s, ip = seg_s;
-  int wb = -1, wkvh = -1, wj = 0, wrow = -kBlockSize;
+  int win_s, win_e, ip;
+  int wb = -1, wkvh = -1, wj = 0, wphys = -1, wrow = -kBlockSize;
   bool more = true;
   auto fill_window = [&]() {
     win_s = ip;
     win_e = min(seg_e, ip + 32);
-    wb = -1; wkvh = -1; wj = 0; wrow = -kBlockSize;
+    wb = -1; wkvh = -1; wj = 0; wphys = -1; wrow = -kBlockSize;
     if (win_s + lane < win_e) {
       int b, kvh, j;
       locate(win_s + lane, b, kvh, j);
       wb = b;
       wkvh = kvh;
       wj = j;
-      wrow = tile_row(__ldg(tables + static_cast<int64_t>(b) * a.max_blocks + j), kvh, a);
+      wphys = __ldcg(tables + static_cast<int64_t>(b) * a.max_blocks + j);
+      wrow = tile_row(wphys, kvh, a, after_wait);
       if (j == 0 || lane == 0)  // a unit starts here: bring its query rows into L2
         prefetch_l2_bulk(static_cast<const T*>(a.q) + (static_cast<int64_t>(b) * Hkv + kvh) * g * D,
                          static_cast<uint32_t>(g * D * sizeof(T)));
     }
+  };
+  // Start on this warp's static head segment.
+  auto start_head = [&]() {
+    part.head(gw, seg_s, seg_e);
+    seg = gw;
+    ip = win_s = win_e = seg_s;
+    more = true;
+    if (ip < seg_e) fill_window();
   };
   // Next window: the rest of this segment, else the next claimed chunk.
   auto advance = [&]() {
@@ -894,34 +941,15 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
     }
   };
 
-  // First window of the head (block-table and query inputs only), then wait:
-  // from here on this grid reads the cache and writes the workspace and out,
-  // which the previous kernels in the stream (append, merge) touch.  Before
-  // the wait, the tiles of the first stages are only prefetched into L2: a
-  // prefetch moves no data into this grid's view, and the loads after the
-  // wait see every earlier write, so they just find the lines in L2.
-  if (ip < seg_e) fill_window();
-  if (lane < SW * NPS && win_s + lane < win_e && wrow >= 0) {
-    constexpr int kCacheRowBytes = F8 ? D : 2 * D;
-    const int64_t off = static_cast<int64_t>(wrow) * kCacheRowBytes;
-    prefetch_l2_bulk(static_cast<const uint8_t*>(a.k_cache_w) + off, Tile::kTileBytes);
-    prefetch_l2_bulk(static_cast<const uint8_t*>(a.v_cache_w) + off, Tile::kTileBytes);
-  }
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  tables = a.block_tables;
-
-  // ---- consume side
-  Attn at;
-  float unit_sl2 = a.scale_log2, unit_vs = 1.f;  // logit scale (log2 units) and output factor of the unit
-  int unit_first_j = 0;
-  bool seg_first_flush = true;
   int issued = 0, consumed = 0;
   int st_i = 0;                  // stage the next issue fills
   int st_c = 0, ph_c = 0;        // stage the next consume reads, and its phase parity
-  bool ok = true;
-  while (true) {
+  // Fill free stages of the ring.  With may_advance false the issue stops at
+  // the end of the current window: no chunk is claimed from the counter.
+  auto issue_stages = [&](bool may_advance) {
     while (more && issued - consumed < SW) {
       if (ip == win_e) {
+        if (!may_advance) break;
         advance();
         if (!more) break;
       }
@@ -968,6 +996,69 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
       ip += n;
       st_i = st_i + 1 == SW ? 0 : st_i + 1;
     }
+  };
+  // Wait for every issued stage and drop it (bounded; false on a timeout).
+  auto drain = [&]() -> bool {
+    for (; consumed < issued; ++consumed) {
+      if (!mbar_wait(smem_u32(&full_bar[warp][st_c]), ph_c)) return false;
+      if (++st_c == SW) {
+        st_c = 0;
+        ph_c ^= 1;
+      }
+    }
+    return true;
+  };
+
+  // First window of the head (block-table and query inputs only), then wait:
+  // from here on this grid reads the cache and writes the workspace and out,
+  // which the previous kernels in the stream (append, merge) touch.  Before
+  // the wait, the tiles of the first stages are only prefetched into L2: a
+  // prefetch moves no data into this grid's view, and the loads after the
+  // wait see every earlier write, so they just find the lines in L2.
+  start_head();
+  if (lane < SW * NPS && win_s + lane < win_e && wrow >= 0) {
+    constexpr int kCacheRowBytes = F8 ? D : 2 * D;
+    const int64_t off = static_cast<int64_t>(wrow) * kCacheRowBytes;
+    prefetch_l2_bulk(static_cast<const uint8_t*>(a.k_cache_w) + off, Tile::kTileBytes);
+    prefetch_l2_bulk(static_cast<const uint8_t*>(a.v_cache_w) + off, Tile::kTileBytes);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  tables = a.block_tables;
+  after_wait = true;
+
+  // The first stages go out on the prologue's reading of the inputs; then the
+  // lengths (CTA vote) and this warp's first window of table entries are read
+  // again.  If either changed, the stages are dropped and the partition and
+  // window are rebuilt from the values read now: all CTAs then agree, since
+  // they all read the same values after the wait.  Otherwise the first
+  // window's block ids are checked (flagged) here.
+  issue_stages(false);
+  bool ok = true;
+  if (a.recheck) {
+    const bool lens_changed = context_changed(a, s_ctx, NW * 32, blockIdx.x == 0);
+    bool table_changed = false;
+    if (!lens_changed && win_s + lane < win_e)
+      table_changed = __ldcg(tables + static_cast<int64_t>(wb) * a.max_blocks + wj) != wphys;
+    table_changed = __any_sync(0xffffffffu, table_changed);
+    if (lens_changed || table_changed) {
+      ok = drain();
+      if (lens_changed) {  // CTA-uniform: every thread takes this branch
+        context_prefix_again(a, s_P, s_ctx, s_warp_sum, NW * 32);
+        part = Partition(Hkv * s_P[B], gridDim.x * NW);
+      }
+      start_head();
+    } else if (win_s + lane < win_e) {
+      tile_row(wphys, wkvh, a, true);
+    }
+  }
+
+  // ---- consume side
+  Attn at;
+  float unit_sl2 = a.scale_log2, unit_vs = 1.f;  // logit scale (log2 units) and output factor of the unit
+  int unit_first_j = 0;
+  bool seg_first_flush = true;
+  while (ok) {
+    issue_stages(true);
     __syncwarp();  // the descriptors written by lane 0 are visible to the warp
     if (consumed == issued) break;
 
@@ -1093,7 +1184,8 @@ __global__ void __launch_bounds__(PersistentShape<D, F8>::kWarps * 32, 1)
 // Units wholly inside one segment were written by the decode kernel; an empty
 // context gives a zero row.  Everything that depends only on the inputs (the
 // block prefix of the contexts) is computed before griddepcontrol.wait, while
-// the decode grid is still running; after it, only the partials are read.  The
+// the decode grid is still running; after it, the lengths are checked again
+// and the partials are read.  The
 // unit's blocks [U, U+nb) overlap shares w0..w1 of 5 segments each; lanes test
 // those candidates in parallel, the overlapping ones are compacted into a
 // list, and their rows are accumulated with independent loads, up to kBatch
@@ -1118,8 +1210,17 @@ __global__ void __launch_bounds__(kMergeWarps * 32, COOP ? 6 : WIDE ? 4 : 8)
   __shared__ __align__(16) float s_o[COOP ? kMergeWarps : 1][COOP ? D : 4];
   int* s_P = merge_smem;
   int* s_ctx = s_P + a.num_seqs + 1;
-  context_prefix(a, s_P, s_ctx, s_warp_sum, kMergeWarps * 32, false);
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The lengths read before the wait are a guess (as in the decode kernel);
+  // the decode grid partitioned the values read after its wait, so the merge
+  // rebuilds its prefix from those if they differ (a second pass).
+  const int32_t* lens = a.pre_context_lens ? a.pre_context_lens : a.context_lens;
+  for (int pass = 0;; ++pass) {
+    context_prefix(a, lens, s_P, s_ctx, s_warp_sum, kMergeWarps * 32, false);
+    if (pass == 1) break;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!a.recheck || !context_changed(a, s_ctx, kMergeWarps * 32, false)) break;
+    lens = a.context_lens;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int rows_per_cta = COOP ? 1 : kMergeWarps;
