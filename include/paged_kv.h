@@ -135,8 +135,10 @@ int paged_kv_append(const void* k_new, const void* v_new, const int32_t* slot_ma
  * The workspace (device) must hold paged_decode_workspace_bytes(dims,
  * num_splits) bytes, be 256-byte aligned, and be zero-filled before its first
  * use (and again after a call that reported an error); the kernels leave the
- * counters in it at zero.  It may be NULL when that size is 0.  Calls that share
- * a workspace must not run concurrently.
+ * counters in it at zero (on the automatic path it also carries, from the
+ * decode kernel to the merge of the same call, the lengths the decode kernel
+ * used, under a per-call tag).  It may be NULL when that size is 0.  Calls
+ * that share a workspace must not run concurrently.
  *
  * Requirements: head_dim 64 or 128, block_size 16, 1 <= Hq/Hkv <= 8,
  * caches and q/out 16-byte aligned, num_blocks * num_kv_heads * 16 < 2^31.

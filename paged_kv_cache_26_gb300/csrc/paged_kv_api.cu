@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -41,6 +42,14 @@ int device_sms() {
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Per-call tags of the decode grid's publication to its merge (never 0).
+uint32_t next_epoch() {
+  static std::atomic<uint32_t> counter{0};
+  uint32_t e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  if (e == 0) e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  return e;
+}
 
 int cuda_fail(cudaError_t e, const char* what) {
   return pkv_fail(PKV_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
@@ -179,10 +188,11 @@ int plan_splits(const pkv_dims* d, int32_t requested, SplitPlan* plan) {
   return PKV_OK;
 }
 
-// Workspace regions: [partial outputs][partial log-sum-exps][scheduler counters].
+// Workspace regions: [partial outputs][partial log-sum-exps][publication of
+// the decode grid's lengths to its merge][scheduler counters].
 struct WorkspaceLayout {
-  size_t o_bytes = 0, lse_bytes = 0, sched_bytes = 0;
-  size_t total() const { return o_bytes + lse_bytes + sched_bytes; }
+  size_t o_bytes = 0, lse_bytes = 0, sched_bytes = 0, pub_bytes = 0;
+  size_t total() const { return o_bytes + lse_bytes + sched_bytes + pub_bytes; }
 };
 
 // Segments of the persistent partition for the largest grid (one CTA per SM).
@@ -197,6 +207,9 @@ WorkspaceLayout workspace_layout(const pkv_dims* d, const SplitPlan& p) {
     w.o_bytes = align256(seg * 2 * pkv::kMaxGroup * d->head_dim * sizeof(float));
     w.lse_bytes = align256(seg * 2 * pkv::kMaxGroup * sizeof(float));
     w.sched_bytes = 256;
+    // The decode grid's validated lengths and block prefix, for the merge:
+    // [epoch][context B][prefix B + 1] int32.
+    w.pub_bytes = align256((2 * static_cast<size_t>(d->num_seqs) + 2) * sizeof(int32_t));
   } else if (p.num_splits > 1) {
     const size_t rows = static_cast<size_t>(d->num_seqs) * d->num_q_heads * p.num_splits;
     w.o_bytes = align256(rows * d->head_dim * sizeof(float));
@@ -378,7 +391,22 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, void* k_cac
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   args.part_o = need ? reinterpret_cast<float*>(ws) : nullptr;
   args.part_lse = need ? reinterpret_cast<float*>(ws + wl.o_bytes) : nullptr;
-  args.sched = wl.sched_bytes ? reinterpret_cast<int32_t*>(ws + wl.o_bytes + wl.lse_bytes) : nullptr;
+  // [partials][log-sum-exps][publication][scheduler counters]
+  args.pub = wl.pub_bytes ? reinterpret_cast<int32_t*>(ws + wl.o_bytes + wl.lse_bytes) : nullptr;
+  args.sched = wl.sched_bytes ? reinterpret_cast<int32_t*>(ws + wl.o_bytes + wl.lse_bytes + wl.pub_bytes) : nullptr;
+  args.epoch = 0;
+  if (recheck && plan.persistent && args.pub) {
+    // A new tag per call, so that a merge never takes an earlier call's
+    // publication for its own; 0 (no publication: the merge re-reads the
+    // lengths itself) while the stream is being captured, since a graph
+    // replays the tag it captured.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+      cudaGetLastError();
+      cap = cudaStreamCaptureStatusActive;
+    }
+    if (cap == cudaStreamCaptureStatusNone) args.epoch = next_epoch();
+  }
   args.block_tables = block_tables;
   args.context_lens = context_lens;
   args.pre_context_lens = pre_lens;

@@ -567,6 +567,9 @@ struct DecodeArgs {
   float* part_o;              // split: f32[B][Hq][splits][D]; persistent: f32[segments][2][8][D]
   float* part_lse;            // split: f32[B][Hq][splits];    persistent: f32[segments][2][8]
   int32_t* sched;             // persistent: int32[2] chunk counter and finished-warp counter, zero between calls
+  int32_t* pub;               // persistent: [epoch][context B][prefix B + 1]: the decode grid's validated
+                              // lengths, published (release) for the merge of the same call
+  uint32_t epoch;             // persistent: this call's publication tag; 0 = none (the merge re-reads)
   const int32_t* pre_context_lens;  // persistent: where the decode and merge prologues (before their grid
   const int32_t* pre_block_tables;  // wait) read the lengths and tables; null: context_lens / block_tables.
                                     // The host-buffer step points them at the mapped host inputs that a copy
@@ -1032,24 +1035,62 @@ __global__ void __maxnreg__(F8 ? 168 : 192)
   // window are rebuilt from the values read now: all CTAs then agree, since
   // they all read the same values after the wait.  Otherwise the first
   // window's block ids are checked (flagged) here.
+  //
+  // With at most kWarpChecked sequences every warp re-reads all the lengths
+  // itself (lane-strided) and compares them once its first stage has landed,
+  // so their latency hides under that load and no CTA barrier is needed: all
+  // warps read the same values, so they all reach the same verdict.  Larger
+  // batches compare at once with a CTA vote.
   issue_stages(false);
   bool ok = true;
   if (a.recheck) {
-    const bool lens_changed = context_changed(a, s_ctx, NW * 32, blockIdx.x == 0);
-    bool table_changed = false;
-    if (!lens_changed && win_s + lane < win_e)
-      table_changed = __ldcg(tables + static_cast<int64_t>(wb) * a.max_blocks + wj) != wphys;
-    table_changed = __any_sync(0xffffffffu, table_changed);
+    constexpr int kHeld = 4;
+    constexpr int kWarpChecked = 32 * kHeld;
+    const bool warp_check = B <= kWarpChecked;
+    int held[kHeld];
+#pragma unroll
+    for (int k = 0; k < kHeld; ++k)
+      held[k] = warp_check && lane + 32 * k < B ? __ldcg(a.context_lens + lane + 32 * k) : 0;
+    const bool in_window = win_s + lane < win_e;
+    const int tv = in_window ? __ldcg(tables + static_cast<int64_t>(wb) * a.max_blocks + wj) : wphys;
+    if (warp_check && issued > consumed) ok = mbar_wait(smem_u32(&full_bar[warp][st_c]), ph_c);
+    bool lens_changed;
+    if (warp_check) {
+      bool d = false;
+      const bool flag = blockIdx.x == 0 && warp == 0;
+#pragma unroll
+      for (int k = 0; k < kHeld; ++k)
+        if (lane + 32 * k < B) d |= clamp_context(held[k], a.max_blocks, flag) != s_ctx[lane + 32 * k];
+      lens_changed = __any_sync(0xffffffffu, d);
+    } else {
+      lens_changed = context_changed(a, s_ctx, NW * 32, blockIdx.x == 0);
+    }
+    const bool table_changed = __any_sync(0xffffffffu, !lens_changed && in_window && tv != wphys);
     if (lens_changed || table_changed) {
-      ok = drain();
-      if (lens_changed) {  // CTA-uniform: every thread takes this branch
+      if (ok) ok = drain();
+      if (lens_changed) {
+        // CTA-uniform: every warp takes this branch.  The barrier keeps the
+        // rebuild from changing s_ctx while another warp still compares.
+        __syncthreads();
         context_prefix_again(a, s_P, s_ctx, s_warp_sum, NW * 32);
         part = Partition(Hkv * s_P[B], gridDim.x * NW);
       }
       start_head();
-    } else if (win_s + lane < win_e) {
+    } else if (in_window) {
       tile_row(wphys, wkvh, a, true);
     }
+  }
+
+  // The lengths and block prefix this grid partitioned (known final now) go
+  // to the merge of the same call: the grid's last warp, whose share (the
+  // last one, often partial) leaves it time to spare, writes them and
+  // releases the call's tag, which the merge acquires instead of reading the
+  // lengths again after its own wait.
+  if (a.epoch != 0 && blockIdx.x == gridDim.x - 1 && warp == NW - 1) {
+    for (int b = lane; b < B; b += 32) a.pub[1 + b] = s_ctx[b];
+    for (int b = lane; b <= B; b += 32) a.pub[1 + B + b] = s_P[b];
+    __syncwarp();  // the lanes' stores come before lane 0's (cumulative) release
+    if (lane == 0) st_release_gpu(a.pub, static_cast<int32_t>(a.epoch));
   }
 
   // ---- consume side
@@ -1210,26 +1251,57 @@ __global__ void __launch_bounds__(kMergeWarps * 32, COOP ? 6 : WIDE ? 4 : 8)
   __shared__ __align__(16) float s_o[COOP ? kMergeWarps : 1][COOP ? D : 4];
   int* s_P = merge_smem;
   int* s_ctx = s_P + a.num_seqs + 1;
-  // The lengths read before the wait are a guess (as in the decode kernel);
-  // the decode grid partitioned the values read after its wait, so the merge
-  // rebuilds its prefix from those if they differ (a second pass).
-  const int32_t* lens = a.pre_context_lens ? a.pre_context_lens : a.context_lens;
-  for (int pass = 0;; ++pass) {
-    context_prefix(a, lens, s_P, s_ctx, s_warp_sum, kMergeWarps * 32, false);
-    if (pass == 1) break;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kThreads = kMergeWarps * 32;
+  // Before its wait the merge needs the lengths and the block prefix the
+  // decode grid partitioned.  When the decode grid publishes them (device
+  // inputs, tag != 0) every thread acquires the call's tag, then takes the
+  // published values: final by construction, so nothing is read again after
+  // the wait.  Otherwise the lengths are read before the wait (host-written
+  // inputs are final; device inputs are then checked again after the wait and
+  // the prefix rebuilt if they changed).
+  bool published = false;
+  if (a.recheck && a.epoch != 0) {
+    // One thread polls, backing off so that the merge CTAs waiting beside the
+    // decode grid do not load the memory system; its acquire and the CTA
+    // barrier after it order every thread's reads of the published values.
+    const int32_t tag = static_cast<int32_t>(a.epoch);
+    __shared__ int s_got;
+    if (threadIdx.x == 0) {
+      const unsigned long long t0 = global_ns();
+      bool got = ld_acquire_gpu(a.pub) == tag;
+      while (!got && global_ns() - t0 < kWaitLimitNs) {
+        __nanosleep(256);
+        got = ld_acquire_gpu(a.pub) == tag;
+      }
+      s_got = got;
+    }
+    __syncthreads();
+    published = s_got != 0;
+  }
+  if (published) {
+    for (int b = threadIdx.x; b < a.num_seqs; b += kThreads) s_ctx[b] = __ldcg(a.pub + 1 + b);
+    for (int b = threadIdx.x; b <= a.num_seqs; b += kThreads) s_P[b] = __ldcg(a.pub + 1 + a.num_seqs + b);
+    __syncthreads();
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (!a.recheck || !context_changed(a, s_ctx, kMergeWarps * 32, false)) break;
-    lens = a.context_lens;
+  } else {
+    const int32_t* lens = a.pre_context_lens ? a.pre_context_lens : a.context_lens;
+    for (int pass = 0;; ++pass) {
+      context_prefix(a, lens, s_P, s_ctx, s_warp_sum, kThreads, false);
+      if (pass == 1) break;
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      if (!a.recheck || !context_changed(a, s_ctx, kThreads, false)) break;
+      lens = a.context_lens;
+    }
   }
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int rows_per_cta = COOP ? 1 : kMergeWarps;
   constexpr int wpr = kMergeWarps / rows_per_cta;  // warps per row
   const int sub = warp % wpr;                      // this warp's part of its row
   const int Hkv = a.num_kv_heads;
+  const int rows = a.num_seqs * a.num_q_heads;
   const Partition part(Hkv * s_P[a.num_seqs], nwarps);
   const int kSegPerShare = part.seg_per_share();
-  const int rows = a.num_seqs * a.num_q_heads;
   // Every warp of the CTA runs the same number of iterations (barriers inside).
   for (int base_row = blockIdx.x * rows_per_cta; base_row < rows; base_row += gridDim.x * rows_per_cta) {
     const int row = base_row + warp / wpr;
@@ -1243,13 +1315,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32, COOP ? 6 : WIDE ? 4 : 8)
       nb = (s_ctx[b] + kBlockSize - 1) / kBlockSize;
     }
     T* dst = static_cast<T*>(a.out) + static_cast<int64_t>(row) * D + lane * kPer;
-    if (work && nb == 0) {
-      if (sub == 0) {
-#pragma unroll
-        for (int k = 0; k < kPer; k += 2) *reinterpret_cast<uint32_t*>(dst + k) = 0u;
-      }
-      work = false;
-    }
+    const bool zero_row = work && nb == 0;
+    if (zero_row) work = false;
     if (work) {
       U = Hkv * s_P[b] + kvh * nb;
       Uend = U + nb;
@@ -1326,6 +1393,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32, COOP ? 6 : WIDE ? 4 : 8)
         }
         __syncwarp();
       }
+    }
+    if (zero_row && sub == 0) {
+#pragma unroll
+      for (int k = 0; k < kPer; k += 2) *reinterpret_cast<uint32_t*>(dst + k) = 0u;
     }
     if constexpr (COOP) {
       // Combine the row's warps: (m, L, o) of each through shared memory.
