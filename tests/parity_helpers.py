@@ -77,3 +77,25 @@ def sample_rows(w, n, seed=0):
     while len(picks) < min(n, B * H):
         picks.add((int(rng.integers(B)), int(rng.integers(H))))
     return sorted(picks)
+
+
+def oracle_all_rows(w, kc_bits, vc_bits, layer=0):
+    """Every (sequence, query head) output of the oracle, float64 [B][Hq][D].
+    The same definition as oracle.decode_attention_rows (gather through the
+    table, then softmax(scale q K^T) V in fp64), but each (sequence, KV head)
+    is gathered once and shared by its group's query heads, which keeps
+    full-size configurations to seconds."""
+    s = w.spec
+    B, H, D, g = s.batch, s.num_q_heads, s.head_dim, s.group
+    q = oracle.widen(bits(w.q[layer]), s.dtype)
+    out = np.zeros((B, H, D))
+    for b in range(B):
+        L = int(w.context_lens[b])
+        if L == 0:
+            continue
+        for kvh in range(s.num_kv_heads):
+            K = oracle.widen(oracle.gather_kv(kc_bits, w.block_tables[b], L, kvh, s.block_size), s.dtype)
+            V = oracle.widen(oracle.gather_kv(vc_bits, w.block_tables[b], L, kvh, s.block_size), s.dtype)
+            for h in range(kvh * g, (kvh + 1) * g):
+                out[b, h] = oracle.attend_one(q[b, h], K, V, w.scale)[0]
+    return out

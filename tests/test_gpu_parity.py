@@ -17,8 +17,8 @@ import oracle
 import paged_kv_cache_26_gb300 as pkv
 import workloads as wl
 from paged_kv_cache_26_gb300 import build as pkv_build
-from parity_helpers import (ATOL, RTOL, assert_close, bits, oracle_caches, oracle_rows, run_gpu_step,
-                            sample_rows, widen_out)
+from parity_helpers import (ATOL, RTOL, assert_close, bits, oracle_all_rows, oracle_caches, oracle_rows,
+                            run_gpu_step, sample_rows, widen_out)
 
 pytestmark = pytest.mark.gpu
 
@@ -81,26 +81,46 @@ def test_llama3_8b_full_single_pass_sampled():
     full_check(w, 1, rows=sample_rows(w, 64))
 
 
-def test_llama70b_tail_full_sampled():
+def full_check_every_output(w, num_splits, layer=0):
+    """full_check over every output row, with the oracle gathering each
+    (sequence, KV head) once."""
+    out, kc, vc = run_gpu_step(w, layer, num_splits)
+    rk, rv = oracle_caches(w, layer)
+    assert np.array_equal(bits(kc), rk), "K append differs from the oracle"
+    assert np.array_equal(bits(vc), rv), "V append differs from the oracle"
+    assert_close(widen_out(out, w.spec.dtype), oracle_all_rows(w, rk, rv, layer),
+                 f"{w.spec.name} splits={num_splits} layer={layer}")
+    return out
+
+
+def test_llama70b_tail_full_every_output():
+    # 256 sequences x 64 query heads, lognormal lengths, 64 sequences sharing a
+    # 512-token prefix: every output row against the oracle.
     w = wl.generate(wl.LLAMA70B_TAIL, seed=0, device="cuda")
     assert w.shared_seqs.size == 64
-    full_check(w, 0, rows=sample_rows(w, 96))
+    full_check_every_output(w, 0)
 
 
-@pytest.mark.parametrize("spec", [wl.MHA_7B_B16, wl.MHA_7B_B64], ids=lambda s: s.name)
-def test_mha7b_full_sampled(spec):
+def test_mha7b_b16_full_sampled():
     # Every layer is an identical, independent call; two layers are checked.
-    w = wl.generate(spec, seed=0, device="cuda", layers=2)
+    w = wl.generate(wl.MHA_7B_B16, seed=0, device="cuda", layers=2)
     for layer in range(2):
         full_check(w, 0, layer, rows=sample_rows(w, 48, seed=layer))
 
 
+def test_mha7b_b64_eight_of_32_layers_sampled():
+    # Batch 64 x 4096 tokens, 32 query / 32 KV heads: 8 of the configuration's
+    # 32 layer calls (each its own cache, the same tables), 96 seeded rows each.
+    w = wl.generate(wl.MHA_7B_B64, seed=0, device="cuda", layers=8)
+    for layer in range(8):
+        full_check(w, 0, layer, rows=sample_rows(w, 96, seed=layer))
+
+
 @pytest.mark.parametrize("splits", [64, 0])
-def test_long_context_split_k_full_sampled(splits):
+def test_long_context_split_k_full_every_output(splits):
+    # 8 sequences x 32768 tokens with one +8-logit spike key each: all 256 rows.
     w = wl.generate(wl.LONG_CTX, seed=0, device="cuda")
-    g = w.spec.group
-    rows = sample_rows(w, 48) + [(b, 0) for b in range(w.spec.batch)]  # head 0 sees the +8 spike
-    full_check(w, splits, rows=sorted(set(rows)))
+    full_check_every_output(w, splits)
 
 
 # ---------------------------------------------------------------- edge cases
