@@ -10,17 +10,18 @@
 //
 //  append_multi_kernel      -- each sequence's q_len new K/V rows into the slots
 //                              of positions L - q_len .. L - 1 of its table.
-//  decode_multi_query_kernel-- one CTA per (split, KV head, sequence).  A TMA
-//                              producer warp streams the split's blocks through
-//                              a ring; the consumer warps each own 16 (or, for
-//                              at most 8 rows in all, 8) of the unit's
-//                              g * q_len query rows and all of them read every
-//                              staged block, so K/V leave HBM once for all the
-//                              new tokens of the group.  Rows are ordered
-//                              token-major (row r = token r / g, head r % g),
-//                              the order of q in memory.  With more than 8 rows
-//                              the query rows are the mma M dimension (16 per
-//                              warp), unlike the one-token kernels.
+//  decode_multi_rows_kernel -- more than 8 query rows per KV head: one CTA per
+//                              (split, KV head, sequence); a TMA producer warp
+//                              streams the split's blocks through a ring and
+//                              each consumer warp owns 16 of the unit's
+//                              g * q_len query rows in the mma M dimension, so
+//                              K/V leave HBM once for all the new tokens of
+//                              the group.  Rows are ordered token-major (row
+//                              r = token r / g, head r % g), the order of q in
+//                              memory.
+//  decode_multi_query_kernel-- at most 8 rows: one consumer warp with the rows
+//                              in the mma N dimension, as in the one-token
+//                              kernels.
 // The split partials are combined by merge_split_kernel with q_len * Hq rows
 // per sequence.
 #pragma once
@@ -32,7 +33,8 @@ namespace pkv {
 constexpr int kMaxQueryLen = 8;
 constexpr int kQueryRowsPerWarp = 16;
 constexpr int kMaxQueryWarps = kMaxGroup * kMaxQueryLen / kQueryRowsPerWarp;  // 4 consumer warps
-constexpr int kMultiStages = 4;
+constexpr int kMultiStages = 4;   // ring stages of one block
+constexpr int kRowStages2 = 3;    // ring stages of two blocks (the 64-row kernel)
 
 // Token (b, i) of k_new / v_new ([B][q_len][Hkv][D]) goes to position
 // context_lens[b] - q_len + i through the block table (nothing for a negative
@@ -181,24 +183,68 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t (&r)[4
                : "r"(addr));
 }
 
+
+// 2^x by the hardware approximation (PTX ex2.approx.ftz.f32: relative error
+// about 2^-22; 2^-inf = 0; results below 2^-126 flush to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// mma.sync m16n8k16 (fp32 accumulate) as a plain register operation, free to
+// be interleaved with the shared-memory loads around it.
+template <typename T>
+__device__ __forceinline__ void mma_rr(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                       uint32_t b0, uint32_t b1) {
+  if constexpr (MmaKind<T>::kBf16) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
 // One warp's attention state for 16 query rows (rows gid and gid + 8 of the
-// mma layout, gid = lane / 4, c = lane % 4) over the blocks of one unit.
-//  * S = Q K^T per block: M = the 16 rows, N = 2 tiles of 8 tokens, K = head_dim
-//    in steps of 16; K fragments come from the swizzled tile with ldmatrix.
+// mma layout, gid = lane / 4, c = lane % 4) over the blocks of one unit, NSUB
+// consecutive 16-token blocks per softmax step.
+//  * S = Q K^T per step: M = the 16 rows, N = 8-token tiles, K = head_dim in
+//    steps of 16 (2 NSUB independent accumulator chains).  Q fragments are
+//    staged once in shared memory (one 16-byte load per k-step, so they cost
+//    no registers); K fragments come from the swizzled tile with ldmatrix.
 //  * The score accumulators are already the A fragments of P V (rows gid,
-//    gid + 8; tokens 2c, 2c+1 and 2c+8, 2c+9), so P never leaves registers.
-//  * O = P V: M = the 16 rows, N = head_dim in tiles of 8, K = the 16 tokens;
-//    V fragments come with ldmatrix.trans.  The lane holds O for rows gid and
-//    gid + 8, columns 8 nd + 2c and + 1.
-//  * Each row has its own causal limit: the first vc0 (vc1) tokens of a block
-//    are visible to row gid (gid + 8).  A row with nothing visible so far keeps
-//    m = -inf and l = 0; O is rescaled only when a row's maximum grows.
-//  * bf16 weights enter P V as two bf16 terms, p = hi + lo (fp16: one term).
-template <typename T, int D>
+//    gid + 8; tokens 2c, 2c+1 and 2c+8, 2c+9 of each block), so P never
+//    leaves registers.  O = P V: M = the rows, N = head_dim in tiles of 8,
+//    K = the tokens; V fragments come with ldmatrix.trans.  The lane holds O
+//    for rows gid and gid + 8, columns 8 nd + 2c and + 1.
+//  * Each row has its own causal limit: the first vc0 (vc1) tokens of a step
+//    are visible to row gid (gid + 8); masks are applied only on steps that
+//    some row of the warp does not see whole.  A row with nothing visible so
+//    far keeps m = -inf and l = 0.
+//  * Lazy reference maximum: a row's reference m (log2 units) moves only when
+//    a step's maximum exceeds it by more than kLazy, so weights stay below
+//    2^kLazy and O is rescaled in a few steps per unit; out = O / l and
+//    lse = m + log2 l hold for any reference.
+//  * Weights: hi = the weight rounded to T always enters P V.  For bf16 the
+//    remainder lo = bf16(p - hi) enters as well in each step whose weights
+//    carry more than kLoShare of a row's running sum after the step (any row
+//    of the warp): every token holding more than that share of its row's
+//    final weight is exact to about 2^-17, the others carry a rounding error
+//    below 2^-9 of their own weight.  l sums the unrounded weights (bf16) or
+//    the rounded ones (fp16, one term, 2^-11).  l is kept as the full row sum
+//    (reduced over the lane quad every step).
+template <typename T, int D, int NSUB>
 struct WarpAttnRows {
   static constexpr int kKSteps = D / 16;
   static constexpr int kNTiles = D / 8;
-  uint32_t qa[kKSteps][4];
+  static constexpr int kTok = 16 * NSUB;
+  static constexpr float kLazy = 8.f;
+  static constexpr float kLoShare = 0.125f;
   float o[kNTiles][4];
   float m0, m1, l0, l1;
 
@@ -209,54 +255,109 @@ struct WarpAttnRows {
     for (int i = 0; i < kNTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   }
 
-  // rows gid (row0) and gid + 8 (row1) of q; null: a padding row of zeros.
-  __device__ __forceinline__ void load_q(const T* row0, const T* row1, int lane) {
+  // Store this lane's A fragments of rows gid (row0) and gid + 8 (row1) at
+  // qs[kk * 32] (qs already offset by the lane); a null row is zeros.  With
+  // `negate` the rows are stored negated (an exact sign flip), which lets a
+  // negative softmax scale use the same maximum as a positive one.
+  __device__ __forceinline__ static void stage_q(uint4* qs, const T* row0, const T* row1, bool negate, int lane) {
     const int c = lane & 3;
+    const uint32_t flip = negate ? 0x80008000u : 0u;
 #pragma unroll
     for (int kk = 0; kk < kKSteps; ++kk) {
       const int d = 16 * kk + 2 * c;
-      qa[kk][0] = row0 ? __ldg(reinterpret_cast<const uint32_t*>(row0 + d)) : 0u;
-      qa[kk][1] = row1 ? __ldg(reinterpret_cast<const uint32_t*>(row1 + d)) : 0u;
-      qa[kk][2] = row0 ? __ldg(reinterpret_cast<const uint32_t*>(row0 + d + 8)) : 0u;
-      qa[kk][3] = row1 ? __ldg(reinterpret_cast<const uint32_t*>(row1 + d + 8)) : 0u;
+      uint4 f;
+      f.x = (row0 ? __ldg(reinterpret_cast<const uint32_t*>(row0 + d)) : 0u) ^ flip;
+      f.y = (row1 ? __ldg(reinterpret_cast<const uint32_t*>(row1 + d)) : 0u) ^ flip;
+      f.z = (row0 ? __ldg(reinterpret_cast<const uint32_t*>(row0 + d + 8)) : 0u) ^ flip;
+      f.w = (row1 ? __ldg(reinterpret_cast<const uint32_t*>(row1 + d + 8)) : 0u) ^ flip;
+      qs[kk * 32] = f;
     }
   }
 
-  __device__ __forceinline__ void block(uint32_t ks, uint32_t vs, int valid_v, int vc0, int vc1, float scale_log2,
-                                        int lane) {
+  // O += P V over the step's blocks (block j's V tile at vs + j * sub_stride);
+  // with LO the remainder weights too.  MASK: V rows at or past valid_v read
+  // as zeros (never 0 * NaN).
+  template <bool MASK, bool LO>
+  __device__ __forceinline__ void pv(uint32_t vs, uint32_t sub_stride, const uint32_t (&ph)[NSUB][4],
+                                     const uint32_t (&pl)[NSUB][4], int valid_v, int lane) {
+    const int c = lane & 3, mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+    for (int pr = 0; pr < kNTiles / 2; ++pr) {
+      // matrices: (tokens 0-7, d tile 2pr), (tokens 8-15, 2pr), (0-7, 2pr+1), (8-15, 2pr+1)
+      const int nd = 2 * pr + (mi >> 1);
+      const int token = 8 * (mi & 1) + rr;
+#pragma unroll
+      for (int j = 0; j < NSUB; ++j) {
+        uint32_t vb[4];
+        ldmatrix_x4_trans(vs + j * sub_stride + (nd >> 3) * 2048 + token * 128 + (((nd & 7) ^ rr) << 4), vb);
+        if constexpr (MASK) {
+          const int vv = valid_v - 16 * j;
+          const uint32_t keep0 = (2 * c < vv ? 0x0000FFFFu : 0u) | (2 * c + 1 < vv ? 0xFFFF0000u : 0u);
+          const uint32_t keep1 = (2 * c + 8 < vv ? 0x0000FFFFu : 0u) | (2 * c + 9 < vv ? 0xFFFF0000u : 0u);
+          vb[0] &= keep0;
+          vb[1] &= keep1;
+          vb[2] &= keep0;
+          vb[3] &= keep1;
+        }
+        mma_rr<T>(o[2 * pr], ph[j][0], ph[j][1], ph[j][2], ph[j][3], vb[0], vb[1]);
+        mma_rr<T>(o[2 * pr + 1], ph[j][0], ph[j][1], ph[j][2], ph[j][3], vb[2], vb[3]);
+        if constexpr (LO) {
+          mma_rr<T>(o[2 * pr], pl[j][0], pl[j][1], pl[j][2], pl[j][3], vb[0], vb[1]);
+          mma_rr<T>(o[2 * pr + 1], pl[j][0], pl[j][1], pl[j][2], pl[j][3], vb[2], vb[3]);
+        }
+      }
+    }
+  }
+
+  // One step: block j's K tile at ks + j * sub_stride.  c2 = |scale| / ln 2.
+  template <bool MASK>
+  __device__ __forceinline__ void step(uint32_t ks, uint32_t vs, uint32_t sub_stride, const uint4* qs, int valid_v,
+                                       int vc0, int vc1, float c2, int lane) {
     const int c = lane & 3;
-    const int mi = lane >> 3, rr = lane & 7;  // the matrix and row this lane addresses
-    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    const int mi = lane >> 3, rr = lane & 7;
+    float s[2 * NSUB][4];
+#pragma unroll
+    for (int a = 0; a < 2 * NSUB; ++a) s[a][0] = s[a][1] = s[a][2] = s[a][3] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < kKSteps; ++kk) {
+      const uint4 qf = qs[kk * 32];
       // matrices: (tokens 0-7, d lo), (tokens 0-7, d hi), (tokens 8-15, d lo), (tokens 8-15, d hi)
       const int token = 8 * (mi >> 1) + rr;
       const int chunk = 2 * (kk & 3) + (mi & 1);
-      uint32_t kb[4];
-      ldmatrix_x4(ks + (kk >> 2) * 2048 + token * 128 + ((chunk ^ rr) << 4), kb);
-      mma16816<T>(s[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], kb[0], kb[1]);
-      mma16816<T>(s[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], kb[2], kb[3]);
-    }
-    float x[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = 8 * nt + 2 * c + e;
-        x[nt][e] = t < vc0 ? s[nt][e] * scale_log2 : -INFINITY;
-        x[nt][2 + e] = t < vc1 ? s[nt][2 + e] * scale_log2 : -INFINITY;
+      for (int j = 0; j < NSUB; ++j) {
+        uint32_t kb[4];
+        ldmatrix_x4(ks + j * sub_stride + (kk >> 2) * 2048 + token * 128 + ((chunk ^ rr) << 4), kb);
+        mma_rr<T>(s[2 * j], qf.x, qf.y, qf.z, qf.w, kb[0], kb[1]);
+        mma_rr<T>(s[2 * j + 1], qf.x, qf.y, qf.z, qf.w, kb[2], kb[3]);
       }
     }
-    float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-    float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+    if constexpr (MASK) {
+#pragma unroll
+      for (int nt = 0; nt < 2 * NSUB; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int t = 8 * nt + 2 * c + e;
+          if (t >= vc0) s[nt][e] = -INFINITY;
+          if (t >= vc1) s[nt][2 + e] = -INFINITY;
+        }
+    }
+    float mx0 = fmaxf(s[0][0], s[0][1]), mx1 = fmaxf(s[0][2], s[0][3]);
+#pragma unroll
+    for (int nt = 1; nt < 2 * NSUB; ++nt) {
+      mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+      mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+    }
 #pragma unroll
     for (int off = 1; off <= 2; off <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    if (__any_sync(0xffffffffu, mn0 > m0 || mn1 > m1)) {
-      const float al0 = mn0 > m0 ? exp2f(m0 - mn0) : 1.f, al1 = mn1 > m1 ? exp2f(m1 - mn1) : 1.f;
+    mx0 *= c2;  // c2 >= 0: the maximum of the scaled scores
+    mx1 *= c2;
+    const bool up0 = mx0 > m0 + kLazy, up1 = mx1 > m1 + kLazy;
+    if (__any_sync(0xffffffffu, up0 || up1)) {
+      const float al0 = up0 ? ex2(m0 - mx0) : 1.f, al1 = up1 ? ex2(m1 - mx1) : 1.f;
       l0 *= al0;
       l1 *= al1;
 #pragma unroll
@@ -266,79 +367,235 @@ struct WarpAttnRows {
         o[nd][2] *= al1;
         o[nd][3] *= al1;
       }
-      m0 = mn0;
-      m1 = mn1;
+      if (up0) m0 = mx0;
+      if (up1) m1 = mx1;
     }
-    const float r0 = m0 == -INFINITY ? 0.f : m0, r1 = m1 == -INFINITY ? 0.f : m1;  // nothing visible yet
-    float p[2][4];
+    const float nr0 = m0 == -INFINITY ? 0.f : -m0, nr1 = m1 == -INFINITY ? 0.f : -m1;  // nothing visible yet
+    float p[NSUB][2][4];
+    uint32_t ph[NSUB][4], pl[NSUB][4];
+    float ps0 = 0.f, ps1 = 0.f;  // this lane's part of the step's row sums
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      p[nt][0] = exp2f(x[nt][0] - r0);
-      p[nt][1] = exp2f(x[nt][1] - r0);
-      p[nt][2] = exp2f(x[nt][2] - r1);
-      p[nt][3] = exp2f(x[nt][3] - r1);
-    }
-    uint32_t ph[4], pl[4] = {0u, 0u, 0u, 0u};
-    ph[0] = pack2<T>(p[0][0], p[0][1]);  // row gid, tokens 2c, 2c+1
-    ph[1] = pack2<T>(p[0][2], p[0][3]);  // row gid + 8
-    ph[2] = pack2<T>(p[1][0], p[1][1]);  // row gid, tokens 2c+8, 2c+9
-    ph[3] = pack2<T>(p[1][2], p[1][3]);
-    if constexpr (MmaKind<T>::kBf16) {
+    for (int j = 0; j < NSUB; ++j) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 h = unpack2<T>(ph[i]);
-        const int nt = i >> 1, e = (i & 1) * 2;
-        pl[i] = pack2<T>(p[nt][e] - h.x, p[nt][e + 1] - h.y);
+      for (int h = 0; h < 2; ++h) {
+        p[j][h][0] = ex2(fmaf(s[2 * j + h][0], c2, nr0));
+        p[j][h][1] = ex2(fmaf(s[2 * j + h][1], c2, nr0));
+        p[j][h][2] = ex2(fmaf(s[2 * j + h][2], c2, nr1));
+        p[j][h][3] = ex2(fmaf(s[2 * j + h][3], c2, nr1));
       }
-      l0 += (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
-      l1 += (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
-    } else {
-      const float2 a = unpack2<T>(ph[0]), b = unpack2<T>(ph[1]), cc = unpack2<T>(ph[2]), dd = unpack2<T>(ph[3]);
-      l0 += (a.x + a.y) + (cc.x + cc.y);  // the rounded weights the product uses
-      l1 += (b.x + b.y) + (dd.x + dd.y);
-    }
-    // V rows at or past valid_v read as zeros (never 0 * NaN).
-    const uint32_t keep0 = (2 * c < valid_v ? 0x0000FFFFu : 0u) | (2 * c + 1 < valid_v ? 0xFFFF0000u : 0u);
-    const uint32_t keep1 = (2 * c + 8 < valid_v ? 0x0000FFFFu : 0u) | (2 * c + 9 < valid_v ? 0xFFFF0000u : 0u);
-#pragma unroll
-    for (int pr = 0; pr < kNTiles / 2; ++pr) {
-      // matrices: (tokens 0-7, d tile 2pr), (tokens 8-15, 2pr), (0-7, 2pr+1), (8-15, 2pr+1)
-      const int nd = 2 * pr + (mi >> 1);
-      const int token = 8 * (mi & 1) + rr;
-      uint32_t vb[4];
-      ldmatrix_x4_trans(vs + (nd >> 3) * 2048 + token * 128 + (((nd & 7) ^ rr) << 4), vb);
-      if (valid_v < kBlockSize) {
-        vb[0] &= keep0;
-        vb[1] &= keep1;
-        vb[2] &= keep0;
-        vb[3] &= keep1;
-      }
-      mma16816<T>(o[2 * pr], ph[0], ph[1], ph[2], ph[3], vb[0], vb[1]);
-      mma16816<T>(o[2 * pr + 1], ph[0], ph[1], ph[2], ph[3], vb[2], vb[3]);
+      ph[j][0] = pack2<T>(p[j][0][0], p[j][0][1]);  // row gid, tokens 2c, 2c+1
+      ph[j][1] = pack2<T>(p[j][0][2], p[j][0][3]);  // row gid + 8
+      ph[j][2] = pack2<T>(p[j][1][0], p[j][1][1]);  // row gid, tokens 2c+8, 2c+9
+      ph[j][3] = pack2<T>(p[j][1][2], p[j][1][3]);
+      pl[j][0] = pl[j][1] = pl[j][2] = pl[j][3] = 0u;
       if constexpr (MmaKind<T>::kBf16) {
-        mma16816<T>(o[2 * pr], pl[0], pl[1], pl[2], pl[3], vb[0], vb[1]);
-        mma16816<T>(o[2 * pr + 1], pl[0], pl[1], pl[2], pl[3], vb[2], vb[3]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 hh = unpack2<T>(ph[j][i]);
+          const int h = i >> 1, e = (i & 1) * 2;
+          pl[j][i] = pack2<T>(p[j][h][e] - hh.x, p[j][h][e + 1] - hh.y);
+        }
+        ps0 += (p[j][0][0] + p[j][0][1]) + (p[j][1][0] + p[j][1][1]);
+        ps1 += (p[j][0][2] + p[j][0][3]) + (p[j][1][2] + p[j][1][3]);
+      } else {
+        const float2 a = unpack2<T>(ph[j][0]), b = unpack2<T>(ph[j][1]), cc = unpack2<T>(ph[j][2]),
+                     dd = unpack2<T>(ph[j][3]);
+        ps0 += (a.x + a.y) + (cc.x + cc.y);  // the rounded weights the product uses
+        ps1 += (b.x + b.y) + (dd.x + dd.y);
       }
     }
-  }
-
-  // Complete the row sums (each lane summed its own columns).
-  __device__ __forceinline__ void finish_sums() {
 #pragma unroll
     for (int off = 1; off <= 2; off <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+      ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
+      ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
+    }
+    bool lo = false;
+    if constexpr (MmaKind<T>::kBf16)
+      lo = __any_sync(0xffffffffu, ps0 > kLoShare * (l0 + ps0) || ps1 > kLoShare * (l1 + ps1));
+    l0 += ps0;
+    l1 += ps1;
+    if (lo) {
+      pv<MASK, true>(vs, sub_stride, ph, pl, valid_v, lane);
+    } else {
+      pv<MASK, false>(vs, sub_stride, ph, pl, valid_v, lane);
     }
   }
 };
 
+// More than 8 query rows per KV head: one CTA per (split, KV head, sequence),
+// NQ = ceil(rows / 16) consumer warps of 16 rows each (WarpAttnRows) and one
+// TMA warp that streams the split's blocks, NSUB per ring stage, so that K/V
+// leave HBM once for all the new tokens of the group.  Rows are ordered
+// token-major (row r = token r / g, head r % g), the order of q in memory.
+// Stages hold NSUB blocks of the same split; a step at the end of a split
+// with fewer blocks masks the rest.
+template <typename T, int D, int S, int NSUB>
+__global__ void __launch_bounds__(kMaxQueryWarps * 32 + 32, 3)
+    decode_multi_rows_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                             const DecodeArgs args, int32_t q_len) {
+  using Shape = TileShape<D>;
+  using Attn = WarpAttnRows<T, D, NSUB>;
+  constexpr int kStep = NSUB * Shape::kStageBytes;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[S];
+  __shared__ __align__(8) uint64_t empty_bar[S];
+  __shared__ int s_abort;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint4* qsm = reinterpret_cast<uint4*>(smem + S * kStep);  // Q fragments: [warp][k-step][lane]
+
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int NQ = static_cast<int>(blockDim.x >> 5) - 1;  // consumer warps; warp NQ produces
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = args.group, Hq = args.num_q_heads, n = q_len;
+  const int nrows = g * n;  // query rows of this (sequence, KV head)
+
+  const int ctx = clamped_context(args.context_lens, b, args.max_blocks, threadIdx.x == 0 && split == 0);
+  const int nblk = (ctx + kBlockSize - 1) / kBlockSize;
+  const int blk0 = split * args.split_blocks;
+  const int nb = min(nblk, blk0 + args.split_blocks) - blk0;
+  const int nsteps = (nb + NSUB - 1) / NSUB;
+  auto row_index = [&](int r) -> int64_t {  // output row of query row r
+    return (static_cast<int64_t>(b) * n + r / g) * Hq + kvh * g + r % g;
+  };
+
+  if (nb <= 0) {
+    // Empty split.  In one pass this is an empty context: zero rows.
+    if (args.num_splits == 1) {
+      for (int idx = threadIdx.x; idx < nrows * D; idx += blockDim.x) {
+        const int r = idx / D, d = idx - r * D;
+        static_cast<T*>(args.out)[row_index(r) * D + d] = T(0.0f);
+      }
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), NQ);
+    }
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == NQ) {
+    // ------------------------------------------------------------ producer
+    const int32_t* trow = args.block_tables + static_cast<int64_t>(b) * args.max_blocks + blk0;
+    const uint64_t policy = l2_evict_first_policy();
+    if (lane == 0) {
+      prefetch_tensormap(&tmap_k);
+      prefetch_tensormap(&tmap_v);
+    }
+    int issued = 0;
+    bool ok = true;
+    // Table entries in windows of 32 blocks (a multiple of NSUB: no step straddles two).
+    for (int base = 0; base < nb && ok; base += 32) {
+      const int jb = base + lane;
+      const int row = jb < nb ? tile_row(trow[jb], kvh, args) : 0;
+      const int cnt = min(32, nb - base);
+      for (int k = 0; k < cnt; k += NSUB) {
+        int r[NSUB];
+#pragma unroll
+        for (int j = 0; j < NSUB; ++j) r[j] = __shfl_sync(0xffffffffu, row, k + j);
+        if (lane == 0 && ok) {
+          const int i = (base + k) / NSUB;
+          const int st = i % S;
+          const int here = min(NSUB, nb - base - k);
+          if (i >= S && !mbar_wait(smem_u32(&empty_bar[st]), ((i / S) & 1) ^ 1)) {
+            ok = false;
+            s_abort = 1;
+          } else if (*reinterpret_cast<volatile int*>(&s_abort)) {
+            ok = false;
+          } else {
+            const uint32_t sa = smem_u32(smem + st * kStep), fb = smem_u32(&full_bar[st]);
+            mbar_arrive_expect_tx(fb, here * Shape::kStageBytes);
+#pragma unroll
+            for (int j = 0; j < NSUB; ++j)
+              if (j < here) issue_tiles<D, false>(sa + j * Shape::kStageBytes, fb, &tmap_k, &tmap_v, r[j], policy);
+            ++issued;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
+    }
+    // No copy may still be landing in shared memory when the CTA exits.
+    if (lane == 0) {
+      for (int i = max(0, issued - S); i < issued; ++i) mbar_wait(smem_u32(&full_bar[i % S]), (i / S) & 1);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int ra = kQueryRowsPerWarp * warp + (lane >> 2), rb = ra + 8;  // this lane's two rows
+  uint4* qs = qsm + warp * Attn::kKSteps * 32 + lane;
+  {
+    const T* q = static_cast<const T*>(args.q);
+    Attn::stage_q(qs, ra < nrows ? q + row_index(ra) * D : nullptr, rb < nrows ? q + row_index(rb) * D : nullptr,
+                  args.scale_log2 < 0.f, lane);
+    __syncwarp();
+  }
+  Attn at;
+  at.reset();
+  // Last position each row attends to (padding rows: the last of the context).
+  const int lim_a = ra < nrows ? ctx - n + ra / g : ctx - 1;
+  const int lim_b = rb < nrows ? ctx - n + rb / g : ctx - 1;
+  // Every row of this warp sees a whole step of this split starting at t0 when
+  // t0 + kTok <= full_end (its first row has the smallest limit).
+  const int full_end = ctx - n + (kQueryRowsPerWarp * warp) / g + 1;
+  const float c2 = fabsf(args.scale_log2);
+  for (int i = 0; i < nsteps; ++i) {
+    if (*reinterpret_cast<volatile int*>(&s_abort)) return;
+    const int st = i % S;
+    if (!mbar_wait(smem_u32(&full_bar[st]), (i / S) & 1)) {
+      s_abort = 1;
+      return;
+    }
+    const int t0 = (blk0 + NSUB * i) * kBlockSize;
+    const int here_tok = min(NSUB, nb - NSUB * i) * kBlockSize;  // tokens of this split in the step
+    const uint32_t ks = smem_u32(smem + st * kStep);
+    if (here_tok == Attn::kTok && t0 + Attn::kTok <= full_end) {
+      at.template step<false>(ks, ks + Shape::kTileBytes, Shape::kStageBytes, qs, Attn::kTok, Attn::kTok, Attn::kTok,
+                              c2, lane);
+    } else {
+      const int valid = min(here_tok, ctx - t0);
+      const int vc0 = max(0, min(valid, lim_a + 1 - t0));
+      const int vc1 = max(0, min(valid, lim_b + 1 - t0));
+      at.template step<true>(ks, ks + Shape::kTileBytes, Shape::kStageBytes, qs, valid, vc0, vc1, c2, lane);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));  // this warp is done with the stage
+  }
+  const int c = lane & 3;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int r = half ? rb : ra;
+    if (r >= nrows) continue;
+    const float l = half ? at.l1 : at.l0;
+    const float inv = l > 0.f ? 1.0f / l : 0.f;  // no visible token: a zero row
+    const int64_t orow = row_index(r);
+    if (args.num_splits == 1) {
+      T* dst = static_cast<T*>(args.out) + orow * D + 2 * c;
+#pragma unroll
+      for (int nd = 0; nd < Attn::kNTiles; ++nd)
+        *reinterpret_cast<uint32_t*>(dst + 8 * nd) = pack2<T>(at.o[nd][2 * half] * inv, at.o[nd][2 * half + 1] * inv);
+    } else {
+      const int64_t prow = orow * args.num_splits + split;
+      float* dst = args.part_o + prow * D + 2 * c;
+#pragma unroll
+      for (int nd = 0; nd < Attn::kNTiles; ++nd)
+        *reinterpret_cast<float2*>(dst + 8 * nd) = make_float2(at.o[nd][2 * half] * inv, at.o[nd][2 * half + 1] * inv);
+      if (c == 0) args.part_lse[prow] = l > 0.f ? (half ? at.m1 : at.m0) + log2f(l) : -INFINITY;
+    }
+  }
+}
+
 // args.num_q_heads = Hq; q / out are T[B][q_len][Hq][D]; split partials are
 // indexed by row = (b * q_len + i) * Hq + h (args.num_splits, args.split_blocks).
-// ROWS: query rows in the mma M dimension, 16 per warp (WarpAttnRows), for
-// more than 8 rows per KV head; else 8 rows per warp in the N dimension
-// (WarpAttnCausal), which pads less when the rows are few.
-template <typename T, int D, int S, bool ROWS>
-__global__ void __launch_bounds__((ROWS ? kMaxQueryWarps : 1) * 32 + 32)
+// At most 8 query rows per KV head: one consumer warp with the rows in the
+// mma N dimension (WarpAttnCausal), which pads less than 16-row M tiles.
+template <typename T, int D, int S>
+__global__ void __launch_bounds__(64)
     decode_multi_query_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                               const DecodeArgs args, int32_t q_len) {
   using Shape = TileShape<D>;
@@ -425,57 +682,7 @@ __global__ void __launch_bounds__((ROWS ? kMaxQueryWarps : 1) * 32 + 32)
 
   // -------------------------------------------------------------- consumers
   const int gid = lane >> 2, c = lane & 3;
-  if constexpr (ROWS) {
-    const int ra = kQueryRowsPerWarp * warp + gid, rb = ra + 8;  // this lane's two rows
-    WarpAttnRows<T, D> at;
-    {
-      const T* q = static_cast<const T*>(args.q);
-      at.load_q(ra < nrows ? q + row_index(ra) * D : nullptr, rb < nrows ? q + row_index(rb) * D : nullptr, lane);
-    }
-    at.reset();
-    // Last position each row attends to (-1: a padding row).
-    const int lim_a = ra < nrows ? ctx - n + ra / g : -1;
-    const int lim_b = rb < nrows ? ctx - n + rb / g : -1;
-    for (int i = 0; i < nb; ++i) {
-      if (*reinterpret_cast<volatile int*>(&s_abort)) return;
-      const int st = i % S;
-      if (!mbar_wait(smem_u32(&full_bar[st]), (i / S) & 1)) {
-        s_abort = 1;
-        return;
-      }
-      const int t0 = (blk0 + i) * kBlockSize;
-      const int vc0 = max(0, min(kBlockSize, lim_a + 1 - t0));
-      const int vc1 = max(0, min(kBlockSize, lim_b + 1 - t0));
-      const uint32_t ks = smem_u32(smem + st * Shape::kStageBytes);
-      at.block(ks, ks + Shape::kTileBytes, min(kBlockSize, ctx - t0), vc0, vc1, args.scale_log2, lane);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));  // this warp is done with the stage
-    }
-    at.finish_sums();
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int r = half ? rb : ra;
-      if (r >= nrows) continue;
-      const float l = half ? at.l1 : at.l0;
-      const float inv = l > 0.f ? 1.0f / l : 0.f;  // no visible token: a zero row
-      const int64_t orow = row_index(r);
-      if (args.num_splits == 1) {
-        T* dst = static_cast<T*>(args.out) + orow * D + 2 * c;
-#pragma unroll
-        for (int nd = 0; nd < WarpAttnRows<T, D>::kNTiles; ++nd)
-          *reinterpret_cast<uint32_t*>(dst + 8 * nd) =
-              pack2<T>(at.o[nd][2 * half] * inv, at.o[nd][2 * half + 1] * inv);
-      } else {
-        const int64_t prow = orow * args.num_splits + split;
-        float* dst = args.part_o + prow * D + 2 * c;
-#pragma unroll
-        for (int nd = 0; nd < WarpAttnRows<T, D>::kNTiles; ++nd)
-          *reinterpret_cast<float2*>(dst + 8 * nd) =
-              make_float2(at.o[nd][2 * half] * inv, at.o[nd][2 * half + 1] * inv);
-        if (c == 0) args.part_lse[prow] = l > 0.f ? (half ? at.m1 : at.m0) + log2f(l) : -INFINITY;
-      }
-    }
-  } else {
+  {
     WarpAttnCausal<T, D> at;
     {
       const int rq = 8 * warp + gid;  // the query row this lane loads

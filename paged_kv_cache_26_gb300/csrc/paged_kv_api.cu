@@ -515,10 +515,15 @@ int append_fp8_impl(const void* k_new, const void* v_new, const int32_t* slot_ma
 
 // ------------------------------------------------------------------ several new tokens per sequence
 
-// Splits of the multi-token kernel: 512-token splits, more when the
-// (sequence, KV head) units alone would not give two CTAs per SM.
-void multi_plan(const pkv_dims* d, int32_t requested, int32_t* splits, int32_t* split_blocks) {
+// Splits of the multi-token kernels: 512-token splits, at least 2 blocks per
+// query row of a (sequence, KV head) unit with more than 8 rows (its split
+// partials, 8 bytes per row and dimension written and read back, then stay
+// under 1/16 of the K/V bytes the split reads), more splits when the units
+// alone would not give two CTAs per SM.
+void multi_plan(const pkv_dims* d, int32_t q_len, int32_t requested, int32_t* splits, int32_t* split_blocks) {
   const int32_t mb = d->max_blocks_per_seq;
+  const int32_t rows = d->num_kv_heads > 0 ? d->num_q_heads / d->num_kv_heads * q_len : 1;
+  const int32_t min_per = rows > 8 ? std::max<int32_t>(kAutoSplitBlocks, 2 * rows) : kAutoSplitBlocks;
   if (mb <= 1) {
     *splits = 1;
     *split_blocks = mb > 0 ? mb : 1;
@@ -527,7 +532,7 @@ void multi_plan(const pkv_dims* d, int32_t requested, int32_t* splits, int32_t* 
   int64_t n = requested;
   if (n == 0) {
     const int64_t units = static_cast<int64_t>(d->num_seqs) * d->num_kv_heads;
-    n = (mb + kAutoSplitBlocks - 1) / kAutoSplitBlocks;
+    n = (mb + min_per - 1) / min_per;
     const int64_t fill = (2 * static_cast<int64_t>(device_sms()) + units - 1) / units;
     if (fill > n) n = fill;
   }
@@ -576,7 +581,7 @@ int decode_multi_impl(const void* q, const void* k_new, const void* v_new, void*
   if (append && (!aligned(k_new, 16) || !aligned(v_new, 16)))
     return pkv_fail(PKV_ERR_INVALID_ARG, "decode_step_multi: k_new / v_new must be 16-byte aligned");
   int32_t splits, split_blocks;
-  multi_plan(d, num_splits, &splits, &split_blocks);
+  multi_plan(d, q_len, num_splits, &splits, &split_blocks);
   const size_t need = multi_workspace(d, q_len, splits);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
     return pkv_fail(PKV_ERR_INVALID_ARG, "decode_attention_multi: workspace missing, too small (" +
@@ -618,46 +623,58 @@ int decode_multi_impl(const void* q, const void* k_new, const void* v_new, void*
   args.num_splits = splits;
   args.split_blocks = split_blocks;
   // More than 8 query rows per KV head: 16 rows per warp in the mma M
-  // dimension; else one warp with the rows in N.
+  // dimension, two blocks per step for 64 rows (one otherwise, which keeps
+  // more CTAs resident for fewer rows); else one warp with the rows in N.
   const bool rows_in_m = args.group * q_len > 8;
   const int nq = rows_in_m ? (args.group * q_len + pkv::kQueryRowsPerWarp - 1) / pkv::kQueryRowsPerWarp : 1;
+  const bool two_blocks = nq == pkv::kMaxQueryWarps;
   const dim3 grid(splits, d->num_kv_heads, d->num_seqs);
-  auto launch = [&](auto kern_rows, auto kern_cols, auto merge, int stage_bytes, auto typed_out) -> int {
-    const int smem = pkv::kMultiStages * stage_bytes + 1024;
-    auto kern = rows_in_m ? kern_rows : kern_cols;
+  auto launch = [&](auto kern, int smem, auto merge, auto typed_out) -> int {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (err != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute(decode_multi_query_kernel)");
+    if (err != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute(multi-token decode kernel)");
     kern<<<grid, (nq + 1) * 32, smem, stream>>>(mk, mv, args, q_len);
     err = cudaGetLastError();
-    if (err != cudaSuccess) return cuda_fail(err, "decode_multi_query_kernel launch");
+    if (err != cudaSuccess) return cuda_fail(err, "multi-token decode kernel launch");
     if (splits > 1) {
       merge<<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(
           args.part_o, args.part_lse, context_lens, static_cast<decltype(typed_out)>(out), d->num_seqs,
-          q_len * d->num_q_heads, splits,
-          split_blocks, d->max_blocks_per_seq);
+          q_len * d->num_q_heads, splits, split_blocks, d->max_blocks_per_seq);
       err = cudaGetLastError();
       if (err != cudaSuccess) return cuda_fail(err, "merge_split_kernel launch");
     }
     return PKV_OK;
   };
+  // Dynamic shared memory: the ring (1024-byte aligned) and, for the row
+  // kernel, each consumer warp's Q fragments (16 rows x head_dim x 2 bytes).
+  auto pick = [&](auto kern_rows1, auto kern_rows2, auto kern_cols, auto merge, int stage_bytes,
+                  auto typed_out) -> int {
+    if (!rows_in_m) return launch(kern_cols, pkv::kMultiStages * stage_bytes + 1024, merge, typed_out);
+    const int qbytes = nq * pkv::kQueryRowsPerWarp * d->head_dim * 2;
+    if (two_blocks) return launch(kern_rows2, pkv::kRowStages2 * 2 * stage_bytes + 1024 + qbytes, merge, typed_out);
+    return launch(kern_rows1, pkv::kMultiStages * stage_bytes + 1024 + qbytes, merge, typed_out);
+  };
   if (d->head_dim == 128) {
     if (bf16)
-      return launch(pkv::decode_multi_query_kernel<__nv_bfloat16, 128, pkv::kMultiStages, true>,
-                    pkv::decode_multi_query_kernel<__nv_bfloat16, 128, pkv::kMultiStages, false>,
-                    pkv::merge_split_kernel<__nv_bfloat16, 128>, pkv::TileShape<128>::kStageBytes,
-                    static_cast<__nv_bfloat16*>(nullptr));
-    return launch(pkv::decode_multi_query_kernel<__half, 128, pkv::kMultiStages, true>,
-                  pkv::decode_multi_query_kernel<__half, 128, pkv::kMultiStages, false>, pkv::merge_split_kernel<__half, 128>,
-                  pkv::TileShape<128>::kStageBytes, static_cast<__half*>(nullptr));
+      return pick(pkv::decode_multi_rows_kernel<__nv_bfloat16, 128, pkv::kMultiStages, 1>,
+                  pkv::decode_multi_rows_kernel<__nv_bfloat16, 128, pkv::kRowStages2, 2>,
+                  pkv::decode_multi_query_kernel<__nv_bfloat16, 128, pkv::kMultiStages>,
+                  pkv::merge_split_kernel<__nv_bfloat16, 128>, pkv::TileShape<128>::kStageBytes,
+                  static_cast<__nv_bfloat16*>(nullptr));
+    return pick(pkv::decode_multi_rows_kernel<__half, 128, pkv::kMultiStages, 1>,
+                pkv::decode_multi_rows_kernel<__half, 128, pkv::kRowStages2, 2>,
+                pkv::decode_multi_query_kernel<__half, 128, pkv::kMultiStages>, pkv::merge_split_kernel<__half, 128>,
+                pkv::TileShape<128>::kStageBytes, static_cast<__half*>(nullptr));
   }
   if (bf16)
-    return launch(pkv::decode_multi_query_kernel<__nv_bfloat16, 64, pkv::kMultiStages, true>,
-                  pkv::decode_multi_query_kernel<__nv_bfloat16, 64, pkv::kMultiStages, false>,
-                  pkv::merge_split_kernel<__nv_bfloat16, 64>, pkv::TileShape<64>::kStageBytes,
-                  static_cast<__nv_bfloat16*>(nullptr));
-  return launch(pkv::decode_multi_query_kernel<__half, 64, pkv::kMultiStages, true>,
-                pkv::decode_multi_query_kernel<__half, 64, pkv::kMultiStages, false>, pkv::merge_split_kernel<__half, 64>,
-                pkv::TileShape<64>::kStageBytes, static_cast<__half*>(nullptr));
+    return pick(pkv::decode_multi_rows_kernel<__nv_bfloat16, 64, pkv::kMultiStages, 1>,
+                pkv::decode_multi_rows_kernel<__nv_bfloat16, 64, pkv::kRowStages2, 2>,
+                pkv::decode_multi_query_kernel<__nv_bfloat16, 64, pkv::kMultiStages>,
+                pkv::merge_split_kernel<__nv_bfloat16, 64>, pkv::TileShape<64>::kStageBytes,
+                static_cast<__nv_bfloat16*>(nullptr));
+  return pick(pkv::decode_multi_rows_kernel<__half, 64, pkv::kMultiStages, 1>,
+              pkv::decode_multi_rows_kernel<__half, 64, pkv::kRowStages2, 2>,
+              pkv::decode_multi_query_kernel<__half, 64, pkv::kMultiStages>, pkv::merge_split_kernel<__half, 64>,
+              pkv::TileShape<64>::kStageBytes, static_cast<__half*>(nullptr));
 }
 
 }  // namespace
@@ -851,7 +868,7 @@ int paged_decode_step_multi(const void* q, const void* k_new, const void* v_new,
 size_t paged_decode_multi_workspace_bytes(const pkv_dims* dims, int32_t q_len, int32_t num_splits) {
   if (check_multi(dims, q_len, num_splits) != PKV_OK) return 0;
   int32_t splits, split_blocks;
-  multi_plan(dims, num_splits, &splits, &split_blocks);
+  multi_plan(dims, q_len, num_splits, &splits, &split_blocks);
   return multi_workspace(dims, q_len, splits);
 }
 
@@ -859,7 +876,7 @@ int32_t paged_decode_multi_resolve_splits(const pkv_dims* dims, int32_t q_len, i
   int rc = check_multi(dims, q_len, num_splits);
   if (rc != PKV_OK) return rc;
   int32_t splits, split_blocks;
-  multi_plan(dims, num_splits, &splits, &split_blocks);
+  multi_plan(dims, q_len, num_splits, &splits, &split_blocks);
   return splits;
 }
 
