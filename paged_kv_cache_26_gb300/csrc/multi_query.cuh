@@ -389,12 +389,6 @@ struct WarpAttnRows {
       ph[j][3] = pack2<T>(p[j][1][2], p[j][1][3]);
       pl[j][0] = pl[j][1] = pl[j][2] = pl[j][3] = 0u;
       if constexpr (MmaKind<T>::kBf16) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 hh = unpack2<T>(ph[j][i]);
-          const int h = i >> 1, e = (i & 1) * 2;
-          pl[j][i] = pack2<T>(p[j][h][e] - hh.x, p[j][h][e + 1] - hh.y);
-        }
         ps0 += (p[j][0][0] + p[j][0][1]) + (p[j][1][0] + p[j][1][1]);
         ps1 += (p[j][0][2] + p[j][0][3]) + (p[j][1][2] + p[j][1][3]);
       } else {
@@ -415,6 +409,14 @@ struct WarpAttnRows {
     l0 += ps0;
     l1 += ps1;
     if (lo) {
+#pragma unroll
+      for (int j = 0; j < NSUB; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 hh = unpack2<T>(ph[j][i]);
+          const int h = i >> 1, e = (i & 1) * 2;
+          pl[j][i] = pack2<T>(p[j][h][e] - hh.x, p[j][h][e + 1] - hh.y);
+        }
       pv<MASK, true>(vs, sub_stride, ph, pl, valid_v, lane);
     } else {
       pv<MASK, false>(vs, sub_stride, ph, pl, valid_v, lane);
