@@ -711,8 +711,8 @@ def run_multi(args, rank, world, local):
         "steps_per_s": round(1e3 / ms_per_step, 2),
         "query_tokens_per_s": round(world * s.batch * n * 1e3 / ms_per_step, 1),
         "roofline": {"bound": "hbm", "kernel": "paged_decode_step_multi: append_multi_kernel + "
-                     ("decode_multi_rows_kernel" if s.num_q_heads // s.num_kv_heads * n > 8
-                      else "decode_multi_query_kernel") + (" + merge_split_kernel" if splits > 1 else ""),
+                     + ("decode_multi_rows_kernel" if s.num_q_heads // s.num_kv_heads * n > 8
+                        else "decode_multi_query_kernel") + (" + merge_split_kernel" if splits > 1 else ""),
                      "achieved": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / peak, 4), "traffic": None,

@@ -104,3 +104,21 @@ def test_ncu_traffic_is_dropped_when_the_kernel_changed(tmp_path, monkeypatch):
     assert bench.ncu_traffic("x") == 123.0
     (csrc / bench.DECODE_KERNEL_SOURCES[0]).write_text("two")
     assert bench.ncu_traffic("x") is None
+
+
+def test_repository_python_compiles_without_warnings():
+    # A warning at compile time (for example a string literal followed by a
+    # parenthesised expression, which Python reads as a call) is a bug that
+    # only shows when that line runs.
+    import glob
+    import warnings
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    files = [os.path.join(root, f) for f in ("bench.py", "__graft_entry__.py")]
+    for d in ("paged_kv_cache_26_gb300", "oracle", "workloads", "tests"):
+        files += glob.glob(os.path.join(root, d, "**", "*.py"), recursive=True)
+    for f in files:
+        with open(f) as fh:
+            src = fh.read()
+        with warnings.catch_warnings():
+            warnings.simplefilter("error")
+            compile(src, f, "exec")
