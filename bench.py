@@ -629,7 +629,8 @@ def run_multi(args, rank, world, local):
                  P(w.k_cache[0].data_ptr()), P(w.v_cache[0].data_ptr()), P(bt.data_ptr()), P(cl.data_ptr()), n,
                  ctypes.c_float(w.scale), P(out.data_ptr()), args.splits, P(ws.data_ptr()), ws_bytes,
                  ctypes.byref(dims), sp)
-    f_step = L.paged_decode_step_multi
+    tensor_cores = getattr(args, "tc", False)
+    f_step = L.paged_decode_step_multi_tc if tensor_cores else L.paged_decode_step_multi
 
     def step():
         if f_step(*step_args):
@@ -706,12 +707,16 @@ def run_multi(args, rank, world, local):
                    "context_tokens": int(w.context_lens.sum()), "num_blocks": w.num_blocks,
                    "partition": f"{splits} splits per sequence",
                    "l2": f"no flush: each call streams {kv_b / 2**20:.0f} MiB, {kv_b / L2_BYTES:.1f}x the 129 MiB L2",
-                   "step": "paged_decode_step_multi: q_len-token KV append + causal multi-token paged attention"
-                           + (" + merge" if splits > 1 else "")},
+                   "step": ("paged_decode_step_multi_tc" if tensor_cores else "paged_decode_step_multi")
+                           + ": q_len-token KV append + causal multi-token paged attention"
+                           + (" + merge" if splits > 1 else ""),
+                   **({"e2e_step": "paged_decode_step_multi_from_host (the default kernel: there is no "
+                                   "host-buffer tcgen05 step)"} if tensor_cores else {})},
         "steps_per_s": round(1e3 / ms_per_step, 2),
         "query_tokens_per_s": round(world * s.batch * n * 1e3 / ms_per_step, 1),
         "roofline": {"bound": "hbm", "kernel": "paged_decode_step_multi: append_multi_kernel + "
-                     + ("decode_multi_rows_kernel" if s.num_q_heads // s.num_kv_heads * n > 8
+                     + ("decode_multi_tc_kernel (tcgen05)" if tensor_cores
+                        else "decode_multi_rows_kernel" if s.num_q_heads // s.num_kv_heads * n > 8
                         else "decode_multi_query_kernel") + (" + merge_split_kernel" if splits > 1 else ""),
                      "achieved": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s",
@@ -999,6 +1004,9 @@ def main():
                     help="pool format: the configuration's fp16/bf16, or E4M3 codes with per-head scales")
     ap.add_argument("--loop", action="store_true", help="continuous-batching loop instead of the fixed batch")
     ap.add_argument("--q-len", type=int, default=1, help="new tokens per sequence (>1: multi-token decode)")
+    ap.add_argument("--tc", action="store_true",
+                    help="multi-token decode on the tcgen05 kernel (64 query rows per KV head; the e2e leg keeps "
+                         "the default host-buffer step)")
     ap.add_argument("--cow", action="store_true", help="copy-on-write block copies instead of the decode step")
     ap.add_argument("--graph", action="store_true", help="capture the step in a CUDA graph and replay it")
     ap.add_argument("--cow-pairs", type=int, default=2048, help="block pairs per copy-on-write call")

@@ -345,6 +345,21 @@ int paged_decode_step_multi(const void* q, const void* k_new, const void* v_new,
                             int32_t q_len, float scale, void* out, int32_t num_splits, void* workspace,
                             size_t workspace_bytes, const pkv_dims* dims, void* stream);
 
+/* paged_decode_step_multi on the fifth-generation tensor cores (tcgen05
+ * MMAs with accumulators in tensor memory), for 64 query rows per KV head:
+ * group x q_len == 64 (for example 64 query heads over 8 KV heads at q_len 8),
+ * head_dim 128, an even number of KV heads.  Defining passage as
+ * paged_decode_step_multi (youngju.dev "LLM サービング最適化完全ガイド",
+ * speculative decoding section).  Same arguments, layouts, ownership,
+ * workspace and results (within the attention tolerance: both kernels
+ * accumulate in fp32 with the same weight rounding); other shapes give
+ * PKV_ERR_UNSUPPORTED before any launch.  One CTA per pair of KV heads of a
+ * sequence; the default paged_decode_step_multi is faster on GB300 for now. */
+int paged_decode_step_multi_tc(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                               void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+                               int32_t q_len, float scale, void* out, int32_t num_splits, void* workspace,
+                               size_t workspace_bytes, const pkv_dims* dims, void* stream);
+
 /* Workspace bytes, and the number of splits, a multi-token call with these
  * arguments uses (0 bytes / a negative error code for invalid arguments). */
 size_t paged_decode_multi_workspace_bytes(const pkv_dims* dims, int32_t q_len, int32_t num_splits);

@@ -74,6 +74,10 @@ _SIGNATURES = {
                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                                ctypes.c_float, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                                ctypes.c_size_t, ctypes.POINTER(PkvDims), ctypes.c_void_p]),
+    "paged_decode_step_multi_tc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                                  ctypes.c_float, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                                  ctypes.c_size_t, ctypes.POINTER(PkvDims), ctypes.c_void_p]),
     "paged_decode_multi_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(PkvDims), ctypes.c_int32,
                                                              ctypes.c_int32]),
     "paged_decode_multi_resolve_splits": (ctypes.c_int32, [ctypes.POINTER(PkvDims), ctypes.c_int32, ctypes.c_int32]),

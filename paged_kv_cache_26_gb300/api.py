@@ -288,10 +288,12 @@ def paged_decode_attention_multi(q: torch.Tensor, k_cache: torch.Tensor, v_cache
 def paged_decode_step_multi(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
                             v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
                             scale: float, out: Optional[torch.Tensor] = None, num_splits: int = 0,
-                            workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                            workspace: Optional[torch.Tensor] = None, stream=None,
+                            tensor_cores: bool = False) -> torch.Tensor:
     """Append the q_len new tokens' K/V (k_new, v_new: [B][q_len][Hkv][D]) at
     positions context_lens[b] - q_len .. context_lens[b] - 1, then
-    paged_decode_attention_multi."""
+    paged_decode_attention_multi.  tensor_cores: run the tcgen05 kernel
+    (paged_decode_step_multi_tc; 64 query rows per KV head only)."""
     if out is None:
         out = torch.empty_like(q)
     _multi_checks(q, k_cache, v_cache, block_tables, context_lens, out)
@@ -301,10 +303,11 @@ def paged_decode_step_multi(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.T
         raise ValueError("k_new / v_new must be [num_seqs][q_len][num_kv_heads][head_dim]")
     dims = _multi_dims(q, k_cache, block_tables)
     workspace, ws_bytes = _multi_workspace(q, k_cache, block_tables, num_splits, workspace)
-    _check(lib().paged_decode_step_multi(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
-                                         _ptr(block_tables), _ptr(context_lens), q.shape[1], float(scale), _ptr(out),
-                                         num_splits, _ptr(workspace), ws_bytes, ctypes.byref(dims), _stream(stream)),
-           "paged_decode_step_multi")
+    name = "paged_decode_step_multi_tc" if tensor_cores else "paged_decode_step_multi"
+    _check(getattr(lib(), name)(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(block_tables), _ptr(context_lens), q.shape[1], float(scale), _ptr(out),
+                                num_splits, _ptr(workspace), ws_bytes, ctypes.byref(dims), _stream(stream)),
+           name)
     return out
 
 

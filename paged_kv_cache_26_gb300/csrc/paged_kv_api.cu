@@ -16,6 +16,7 @@
 #include "block_copy.cuh"
 #include "host_copy.cuh"
 #include "multi_query.cuh"
+#include "multi_query_tc.cuh"
 #include "paged_kv_kernels.cuh"
 #include "pkv_errors.h"
 #include "pkv_internal.h"
@@ -565,9 +566,14 @@ int check_multi(const pkv_dims* d, int32_t q_len, int32_t num_splits) {
 int decode_multi_impl(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                       const int32_t* block_tables, const int32_t* context_lens, int32_t q_len, float scale,
                       void* out, int32_t num_splits, void* workspace, size_t workspace_bytes, const pkv_dims* d,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool tensor_cores = false) {
   int rc = check_multi(d, q_len, num_splits);
   if (rc != PKV_OK) return rc;
+  if (tensor_cores && (d->num_kv_heads < 1 || d->num_q_heads / d->num_kv_heads * q_len != pkv::Tc2::kRows ||
+                       d->head_dim != 128 || d->num_kv_heads % 2 != 0))
+    return pkv_fail(PKV_ERR_UNSUPPORTED,
+                    "decode_step_multi_tc: needs 64 query rows per KV head (group x q_len), head_dim 128 and an even "
+                    "number of KV heads");
   if (d->num_seqs == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || (!block_tables && d->max_blocks_per_seq > 0) || !context_lens || !out)
     return pkv_fail(PKV_ERR_INVALID_ARG, "decode_attention_multi: NULL pointer");
@@ -649,6 +655,29 @@ int decode_multi_impl(const void* q, const void* k_new, const void* v_new, void*
   auto pick = [&](auto kern_rows1, auto kern_rows2, auto kern_cols, auto merge, int stage_bytes,
                   auto typed_out) -> int {
     if (!rows_in_m) return launch(kern_cols, pkv::kMultiStages * stage_bytes + 1024, merge, typed_out);
+    if (tensor_cores) {
+      // One CTA per (split, pair of KV heads, sequence) on the tensor-core kernel.
+      const void* kern = bf16 ? reinterpret_cast<const void*>(pkv::decode_multi_tc_kernel<__nv_bfloat16>)
+                              : reinterpret_cast<const void*>(pkv::decode_multi_tc_kernel<__half>);
+      cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pkv::Tc2::kSmem);
+      if (err != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute(decode_multi_tc_kernel)");
+      const dim3 tgrid(splits, d->num_kv_heads / 2, d->num_seqs);
+      if (bf16)
+        pkv::decode_multi_tc_kernel<__nv_bfloat16>
+            <<<tgrid, pkv::Tc2::kThreads, pkv::Tc2::kSmem, stream>>>(mk, mv, args, q_len);
+      else
+        pkv::decode_multi_tc_kernel<__half><<<tgrid, pkv::Tc2::kThreads, pkv::Tc2::kSmem, stream>>>(mk, mv, args, q_len);
+      err = cudaGetLastError();
+      if (err != cudaSuccess) return cuda_fail(err, "decode_multi_tc_kernel launch");
+      if (splits > 1) {
+        merge<<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(
+            args.part_o, args.part_lse, context_lens, static_cast<decltype(typed_out)>(out), d->num_seqs,
+            q_len * d->num_q_heads, splits, split_blocks, d->max_blocks_per_seq);
+        err = cudaGetLastError();
+        if (err != cudaSuccess) return cuda_fail(err, "merge_split_kernel launch");
+      }
+      return PKV_OK;
+    }
     const int qbytes = nq * pkv::kQueryRowsPerWarp * d->head_dim * 2;
     if (two_blocks) return launch(kern_rows2, pkv::kRowStages2 * 2 * stage_bytes + 1024 + qbytes, merge, typed_out);
     return launch(kern_rows1, pkv::kMultiStages * stage_bytes + 1024 + qbytes, merge, typed_out);
@@ -863,6 +892,15 @@ int paged_decode_step_multi(const void* q, const void* k_new, const void* v_new,
   if (!k_new || !v_new) return pkv_fail(PKV_ERR_INVALID_ARG, "decode_step_multi: NULL k_new / v_new");
   return decode_multi_impl(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, q_len, scale, out,
                            num_splits, workspace, workspace_bytes, dims, static_cast<cudaStream_t>(stream));
+}
+
+int paged_decode_step_multi_tc(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                               const int32_t* block_tables, const int32_t* context_lens, int32_t q_len, float scale,
+                               void* out, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                               const pkv_dims* dims, void* stream) {
+  if (!k_new || !v_new) return pkv_fail(PKV_ERR_INVALID_ARG, "decode_step_multi_tc: NULL k_new / v_new");
+  return decode_multi_impl(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, q_len, scale, out,
+                           num_splits, workspace, workspace_bytes, dims, static_cast<cudaStream_t>(stream), true);
 }
 
 size_t paged_decode_multi_workspace_bytes(const pkv_dims* dims, int32_t q_len, int32_t num_splits) {

@@ -122,3 +122,17 @@ def test_repository_python_compiles_without_warnings():
         with warnings.catch_warnings():
             warnings.simplefilter("error")
             compile(src, f, "exec")
+
+
+@pytest.mark.parametrize("q_len", [1, 4, 8])
+def test_shared_prefix_sequences_never_append_into_the_shared_blocks(q_len):
+    # Sequences that share the prefix blocks must write their new tokens into
+    # blocks of their own (an engine copies a shared block before writing it).
+    import workloads as wl
+    w, _ = wl.generate_multi(wl.LLAMA70B_TAIL.replace(batch=256), q_len, seed=0, layers=1)
+    prefix_blocks = wl.LLAMA70B_TAIL.shared_prefix[1] // wl.LLAMA70B_TAIL.block_size
+    shared = set(int(x) for x in w.block_tables[w.shared_seqs[0], :prefix_blocks])
+    for b in range(w.spec.batch):
+        L = int(w.context_lens[b])
+        for pos in range(max(0, L - q_len), L):
+            assert int(w.block_tables[b, pos // w.spec.block_size]) not in shared or b not in w.shared_seqs

@@ -26,14 +26,15 @@ def built():
     pkv_build.build()
 
 
-def run_multi(w, m, layer=0, num_splits=0, fused=True):
+def run_multi(w, m, layer=0, num_splits=0, fused=True, tensor_cores=False):
     kc = w.k_cache[layer].to(DEV, copy=True)
     vc = w.v_cache[layer].to(DEV, copy=True)
     q, kn, vn = (t[layer].to(DEV) for t in (m.q, m.k_new, m.v_new))
     bt = torch.from_numpy(w.block_tables).to(DEV)
     cl = torch.from_numpy(w.context_lens).to(DEV)
     if fused:
-        out = pkv.paged_decode_step_multi(q, kn, vn, kc, vc, bt, cl, w.scale, num_splits=num_splits)
+        out = pkv.paged_decode_step_multi(q, kn, vn, kc, vc, bt, cl, w.scale, num_splits=num_splits,
+                                          tensor_cores=tensor_cores)
     else:
         slots = pkv.paged_kv_slot_mapping_multi(w.block_tables, w.context_lens, m.q_len).reshape(-1)
         B, n = kn.shape[:2]
@@ -52,8 +53,8 @@ def oracle_multi_caches(w, m, layer=0):
                             vn.reshape(B * n, *vn.shape[2:]), slots, w.spec.block_size)
 
 
-def check_multi(w, m, layer=0, num_splits=0, rows=None, fused=True):
-    out, kc, vc = run_multi(w, m, layer, num_splits, fused)
+def check_multi(w, m, layer=0, num_splits=0, rows=None, fused=True, tensor_cores=False):
+    out, kc, vc = run_multi(w, m, layer, num_splits, fused, tensor_cores)
     rk, rv = oracle_multi_caches(w, m, layer)
     assert np.array_equal(bits(kc), rk), "K append differs from the oracle"
     assert np.array_equal(bits(vc), rv), "V append differs from the oracle"
@@ -176,3 +177,43 @@ def test_multi_invalid_arguments_are_rejected():
     with pytest.raises(ValueError):
         pkv.paged_decode_attention_multi(torch.zeros(2, 8, 128, dtype=torch.bfloat16, device=dev), kc, kc, bt, cl,
                                          0.1)
+
+
+# ---- the tensor-core (tcgen05) kernel: 64 query rows per KV head, head_dim 128
+
+TC_70B_SMALL = wl.LLAMA70B_TAIL.replace(name="70b_small", batch=6, lengths=("lognormal", 200.0, 1.0, 1, 900),
+                                        shared_prefix=(2, 64))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("splits", [1, 3, 0])
+def test_multi_tensor_cores_every_output(dtype, splits):
+    w, m = wl.generate_multi(TC_70B_SMALL.replace(dtype=dtype), 8, seed=7)
+    check_multi(w, m, num_splits=splits, tensor_cores=True)
+
+
+def test_multi_tensor_cores_edge_lengths():
+    # empty, shorter than q_len, exactly q_len, new tokens across block boundaries,
+    # a split boundary (512 / 513 with two splits)
+    lens = (1, 2, 8, 18, 16, 17, 0, 33, 512, 513)
+    spec = wl.LLAMA3_8B.replace(name="custom", batch=len(lens), lengths=("fixed", lens), pool=("factor", 1.5),
+                                num_q_heads=16, num_kv_heads=2)
+    w, m = wl.generate_multi(spec, 8, seed=3)
+    for splits in (1, 2, 0):
+        out = check_multi(w, m, num_splits=splits, tensor_cores=True)
+        assert torch.all(out[6] == 0)              # empty context: zero rows
+        assert torch.all(out[0, :7] == 0)          # tokens before position 0: zero rows
+
+
+def test_multi_tensor_cores_llama70b_full_sampled():
+    w, m = wl.generate_multi(wl.LLAMA70B_TAIL, 8, seed=0, device=DEV)
+    rng = np.random.default_rng(1)
+    rows = sorted({(int(rng.integers(256)), int(rng.integers(8)), int(rng.integers(64))) for _ in range(96)}
+                  | {(int(np.argmax(w.context_lens)), 7, 0), (int(np.argmin(w.context_lens)), 0, 63)})
+    check_multi(w, m, rows=rows, tensor_cores=True)
+
+
+def test_multi_tensor_cores_reject_other_shapes():
+    w, m = wl.generate_multi(TC_70B_SMALL, 4, seed=7)     # 32 rows per KV head
+    with pytest.raises(pkv.PagedKVError):
+        run_multi(w, m, tensor_cores=True)

@@ -135,9 +135,13 @@ def _cdiv(a, b):
     return -(-a // b)
 
 
-def generate(spec: WorkloadSpec, seed: int = 0, device="cpu", layers: Optional[int] = None) -> Workload:
+def generate(spec: WorkloadSpec, seed: int = 0, device="cpu", layers: Optional[int] = None,
+             new_tokens: int = 1) -> Workload:
     """Draw one decode batch.  ``layers`` caps the number of layer caches built
-    (the structure, i.e. lengths and tables, is the same for every layer)."""
+    (the structure, i.e. lengths and tables, is the same for every layer).
+    ``new_tokens``: tokens each sequence appends this step; a sequence sharing
+    the prefix holds at least prefix + new_tokens tokens, so that its new
+    tokens never land in a shared block."""
     rng = np.random.default_rng(seed)
     bs = spec.block_size
     lens = draw_lengths(spec, rng)
@@ -148,12 +152,12 @@ def generate(spec: WorkloadSpec, seed: int = 0, device="cpu", layers: Optional[i
         n_share, prefix_tokens = spec.shared_prefix
         assert prefix_tokens % bs == 0, "shared prefix must cover whole blocks"
         prefix_blocks = prefix_tokens // bs
-        eligible = np.flatnonzero(lens > prefix_tokens)
+        eligible = np.flatnonzero(lens >= prefix_tokens + new_tokens)
         if eligible.size >= n_share:
             shared_seqs = np.sort(rng.choice(eligible, size=n_share, replace=False))
         else:
             shared_seqs = np.sort(rng.choice(spec.batch, size=n_share, replace=False))
-            lens[shared_seqs] = np.maximum(lens[shared_seqs], prefix_tokens + 1)
+            lens[shared_seqs] = np.maximum(lens[shared_seqs], prefix_tokens + new_tokens)
 
     nblk = _cdiv(lens, bs)
     is_shared = np.zeros(spec.batch, bool)
@@ -294,7 +298,7 @@ def generate_multi(spec: WorkloadSpec, q_len: int, seed: int = 0, device="cpu",
     cache holds the first L - q_len tokens of each sequence and NaN in every
     other slot (the q_len slots the append fills included); the new tokens'
     queries and K/V are N(0,1) like the rest."""
-    w = generate(spec, seed=seed, device=device, layers=layers)
+    w = generate(spec, seed=seed, device=device, layers=layers, new_tokens=q_len)
     bs = spec.block_size
     blk, off = [], []
     for b in range(spec.batch):
