@@ -430,11 +430,14 @@ struct WarpAttnRows {
 // leave HBM once for all the new tokens of the group.  Rows are ordered
 // token-major (row r = token r / g, head r % g), the order of q in memory.
 // Stages hold NSUB blocks of the same split; a step at the end of a split
-// with fewer blocks masks the rest.
+// with fewer blocks masks the rest.  split_major: the grid is (sequence, KV
+// head, split), so that every unit's first split is dispatched before any
+// later one (the later splits of short sequences are empty and exit at the
+// tail); otherwise (split, KV head, sequence).
 template <typename T, int D, int S, int NSUB>
 __global__ void __launch_bounds__(kMaxQueryWarps * 32 + 32, 3)
     decode_multi_rows_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                             const DecodeArgs args, int32_t q_len) {
+                             const DecodeArgs args, int32_t q_len, int32_t split_major) {
   using Shape = TileShape<D>;
   using Attn = WarpAttnRows<T, D, NSUB>;
   constexpr int kStep = NSUB * Shape::kStageBytes;
@@ -445,7 +448,8 @@ __global__ void __launch_bounds__(kMaxQueryWarps * 32 + 32, 3)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint4* qsm = reinterpret_cast<uint4*>(smem + S * kStep);  // Q fragments: [warp][k-step][lane]
 
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int split = split_major ? blockIdx.z : blockIdx.x, kvh = blockIdx.y;
+  const int b = split_major ? blockIdx.x : blockIdx.z;
   const int NQ = static_cast<int>(blockDim.x >> 5) - 1;  // consumer warps; warp NQ produces
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = args.group, Hq = args.num_q_heads, n = q_len;

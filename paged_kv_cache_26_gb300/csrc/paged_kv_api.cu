@@ -635,6 +635,28 @@ int decode_multi_impl(const void* q, const void* k_new, const void* v_new, void*
   const int nq = rows_in_m ? (args.group * q_len + pkv::kQueryRowsPerWarp - 1) / pkv::kQueryRowsPerWarp : 1;
   const bool two_blocks = nq == pkv::kMaxQueryWarps;
   const dim3 grid(splits, d->num_kv_heads, d->num_seqs);
+  // The row kernel dispatches every unit's first split before any later one
+  // when the units alone give at least 8 CTAs per SM (measured, Llama-70B tail
+  // q_len 8: 0.540 -> 0.560 of the copy peak; with 512 units, Llama-8B B=64,
+  // interleaved splits balance the tail better: 0.745 against 0.735).
+  const int64_t units = static_cast<int64_t>(d->num_seqs) * d->num_kv_heads;
+  const int32_t split_major = splits > 1 && units >= 8 * static_cast<int64_t>(device_sms()) ? 1 : 0;
+  const dim3 rgrid = split_major ? dim3(d->num_seqs, d->num_kv_heads, splits) : grid;
+  auto launch_rows = [&](auto kern, int smem, auto merge, auto typed_out) -> int {
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute(decode_multi_rows_kernel)");
+    kern<<<rgrid, (nq + 1) * 32, smem, stream>>>(mk, mv, args, q_len, split_major);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return cuda_fail(err, "decode_multi_rows_kernel launch");
+    if (splits > 1) {
+      merge<<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(
+          args.part_o, args.part_lse, context_lens, static_cast<decltype(typed_out)>(out), d->num_seqs,
+          q_len * d->num_q_heads, splits, split_blocks, d->max_blocks_per_seq);
+      err = cudaGetLastError();
+      if (err != cudaSuccess) return cuda_fail(err, "merge_split_kernel launch");
+    }
+    return PKV_OK;
+  };
   auto launch = [&](auto kern, int smem, auto merge, auto typed_out) -> int {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute(multi-token decode kernel)");
@@ -679,8 +701,9 @@ int decode_multi_impl(const void* q, const void* k_new, const void* v_new, void*
       return PKV_OK;
     }
     const int qbytes = nq * pkv::kQueryRowsPerWarp * d->head_dim * 2;
-    if (two_blocks) return launch(kern_rows2, pkv::kRowStages2 * 2 * stage_bytes + 1024 + qbytes, merge, typed_out);
-    return launch(kern_rows1, pkv::kMultiStages * stage_bytes + 1024 + qbytes, merge, typed_out);
+    if (two_blocks)
+      return launch_rows(kern_rows2, pkv::kRowStages2 * 2 * stage_bytes + 1024 + qbytes, merge, typed_out);
+    return launch_rows(kern_rows1, pkv::kMultiStages * stage_bytes + 1024 + qbytes, merge, typed_out);
   };
   if (d->head_dim == 128) {
     if (bf16)
