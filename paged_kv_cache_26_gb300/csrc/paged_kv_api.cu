@@ -266,12 +266,14 @@ int launch_persistent(const CUtensorMap& mk, const CUtensorMap& mv, const pkv::D
   e = cudaLaunchKernelEx(&cfg, kern, mk, mv, args);
   if (e != cudaSuccess) return cuda_fail(e, "decode_persistent_kernel launch");
   cfg.numAttrs = 1;
-  // Long units cut into many pieces (on average 6 or more warp shares per
+  // Long units cut into many pieces (on average 8 or more warp shares per
   // unit): a CTA per row, its warps splitting the row's pieces; otherwise a
-  // warp per row.
+  // warp per row (measured: at 7.1 shares, the E4M3 pool at B=32, a warp per
+  // row 0.741 against 0.703; at 9.5, bf16 at B=16, a CTA per row 0.784
+  // against 0.770).
   const int32_t nwarps = static_cast<int32_t>(grid) * PS::kWarps;
   const int64_t units = static_cast<int64_t>(d->num_seqs) * d->num_kv_heads;
-  const bool coop = nwarps >= 6 * units;
+  const bool coop = nwarps >= 8 * units;
   // Two or more warp shares per unit on average: rows have many pieces, so
   // fold up to 16 per round trip (fewer registers leave room for more merge
   // CTAs beside the decode grid, which pays when rows are many and short).
