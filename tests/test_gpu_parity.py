@@ -445,6 +445,21 @@ def test_large_batch_falls_back_to_splits():
     full_check(w, 0, rows=sample_rows(w, 64))
 
 
+@pytest.mark.parametrize("head_dim", [128, 64])
+def test_persistent_path_at_its_largest_batch(head_dim):
+    """2048 sequences, the most the persistent kernel's shared-memory plan
+    holds: still the persistent path, every output and the append exact, for
+    the fused step and for append + attention."""
+    spec = wl.LLAMA3_8B.replace(name="b2048", batch=2048, lengths=("uniform", 1, 40), num_q_heads=8,
+                                num_kv_heads=2, head_dim=head_dim, pool=("factor", 1.2))
+    w = wl.generate(spec, seed=6)
+    dev = torch.device("cuda")
+    assert pkv.paged_decode_resolve_splits(w.q[0].to(dev), w.k_cache[0].to(dev),
+                                           torch.from_numpy(w.block_tables).to(dev), 0) == 0
+    full_check_every_output(w, 0)
+    full_check(w, 0, fused=True, rows=sample_rows(w, 256))
+
+
 @pytest.mark.parametrize("lens", [(1,), (5, 0, 7), (16,) * 3, (4096, 1, 1, 1), (0, 0)])
 def test_persistent_short_and_uneven_batches(lens):
     w = _custom(lens, spec=wl.LLAMA3_8B.replace(num_q_heads=8, num_kv_heads=2))
