@@ -1224,16 +1224,18 @@ __global__ void __maxnreg__(F8 ? 168 : 192)
 // chain).
 // Units wholly inside one segment were written by the decode kernel; an empty
 // context gives a zero row.  Everything that depends only on the inputs (the
-// block prefix of the contexts) is computed before griddepcontrol.wait, while
-// the decode grid is still running; after it, the lengths are checked again
-// and the partials are read.  The
-// unit's blocks [U, U+nb) overlap shares w0..w1 of 5 segments each; lanes test
-// those candidates in parallel, the overlapping ones are compacted into a
-// list, and their rows are accumulated with independent loads, up to kBatch
-// pieces per round trip.  Small CTAs (4 warps at <= 64 registers, 80 for
-// COOP) fit two beside a decode CTA.  WIDE (a warp per row, 16 pieces per
-// round trip, <= 128 registers, one beside a decode CTA) is for units cut
-// into many pieces, whose rows would otherwise take two round trips.
+// block prefix of the contexts, and the plan of the CTA's first row with its
+// first batch of candidate pieces) is computed before griddepcontrol.wait,
+// while the decode grid is still running; after it, unpublished lengths are
+// checked again and the partials are read.  The unit's blocks [U, U+nb)
+// overlap shares w0..w1 of 5 segments each; lanes test those candidates in
+// parallel, the overlapping ones are compacted into a list, and their rows
+// are accumulated with independent loads, up to kBatch pieces per round trip
+// (6 in the small warp-per-row CTAs, which then need no spills).  Small CTAs
+// (4 warps at <= 64 registers, 80 for COOP) fit two beside a decode CTA.
+// WIDE (a warp per row, 16 pieces per round trip, <= 128 registers, one
+// beside a decode CTA) is for units cut into many pieces, whose rows would
+// otherwise take two round trips.
 constexpr int kMergeWarps = 4;
 
 template <typename T, int D, bool COOP, bool WIDE = false>
@@ -1283,16 +1285,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32, COOP ? 6 : WIDE ? 4 : 8)
     for (int b = threadIdx.x; b < a.num_seqs; b += kThreads) s_ctx[b] = __ldcg(a.pub + 1 + b);
     for (int b = threadIdx.x; b <= a.num_seqs; b += kThreads) s_P[b] = __ldcg(a.pub + 1 + a.num_seqs + b);
     __syncthreads();
-    asm volatile("griddepcontrol.wait;" ::: "memory");
   } else {
-    const int32_t* lens = a.pre_context_lens ? a.pre_context_lens : a.context_lens;
-    for (int pass = 0;; ++pass) {
-      context_prefix(a, lens, s_P, s_ctx, s_warp_sum, kThreads, false);
-      if (pass == 1) break;
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      if (!a.recheck || !context_changed(a, s_ctx, kThreads, false)) break;
-      lens = a.context_lens;
-    }
+    context_prefix(a, a.pre_context_lens ? a.pre_context_lens : a.context_lens, s_P, s_ctx, s_warp_sum, kThreads,
+                   false);
   }
 
   constexpr int rows_per_cta = COOP ? 1 : kMergeWarps;
@@ -1300,59 +1295,119 @@ __global__ void __launch_bounds__(kMergeWarps * 32, COOP ? 6 : WIDE ? 4 : 8)
   const int sub = warp % wpr;                      // this warp's part of its row
   const int Hkv = a.num_kv_heads;
   const int rows = a.num_seqs * a.num_q_heads;
-  const Partition part(Hkv * s_P[a.num_seqs], nwarps);
-  const int kSegPerShare = part.seg_per_share();
-  // Every warp of the CTA runs the same number of iterations (barriers inside).
-  for (int base_row = blockIdx.x * rows_per_cta; base_row < rows; base_row += gridDim.x * rows_per_cta) {
-    const int row = base_row + warp / wpr;
-    bool work = row < rows;
-    int b = 0, kvh = 0, h = 0, nb = 0, U = 0, Uend = 0;
-    if (work) {
-      b = row / a.num_q_heads;
-      const int hq = row - b * a.num_q_heads;
-      kvh = hq / a.group;
-      h = hq - kvh * a.group;
-      nb = (s_ctx[b] + kBlockSize - 1) / kBlockSize;
+  // What the lengths fix for one row: its unit's blocks [U, Uend), whether
+  // the decode kernel left it in pieces (work: the unit spans two or more
+  // segments) or it is empty (zero_row), and its candidate segments, shares
+  // w0.. of seg_per_share() segments each.
+  struct RowPlan {
+    int b, kvh, h, U, Uend, w0, ncand;
+    bool work, zero_row;
+  };
+  auto plan_row = [&](const Partition& part, int row) -> RowPlan {
+    RowPlan r{0, 0, 0, 0, 0, 0, 0, row < rows, false};
+    int nb = 0;
+    if (r.work) {
+      r.b = row / a.num_q_heads;
+      const int hq = row - r.b * a.num_q_heads;
+      r.kvh = hq / a.group;
+      r.h = hq - r.kvh * a.group;
+      nb = (s_ctx[r.b] + kBlockSize - 1) / kBlockSize;
     }
-    T* dst = static_cast<T*>(a.out) + static_cast<int64_t>(row) * D + lane * kPer;
-    const bool zero_row = work && nb == 0;
-    if (zero_row) work = false;
-    if (work) {
-      U = Hkv * s_P[b] + kvh * nb;
-      Uend = U + nb;
+    r.zero_row = r.work && nb == 0;
+    if (r.zero_row) r.work = false;
+    if (r.work) {
+      r.U = Hkv * s_P[r.b] + r.kvh * nb;
+      r.Uend = r.U + nb;
       int s, e;
-      part.segment_of(U, s, e);
-      if (e >= Uend) work = false;  // one segment: the decode kernel wrote it
+      part.segment_of(r.U, s, e);
+      if (e >= r.Uend) r.work = false;  // one segment: the decode kernel wrote it
     }
+    if (r.work) {
+      r.w0 = r.U / part.R;
+      r.ncand = ((r.Uend - 1) / part.R - r.w0 + 1) * part.seg_per_share();
+    }
+    return r;
+  };
+  // Candidate c of a row: the row of its piece in the partials, or -1 when
+  // that segment does not overlap the unit.
+  auto piece = [&](const Partition& part, const RowPlan& r, int c) -> int64_t {
+    const int kSegPerShare = part.seg_per_share();
+    const int w = r.w0 + c / kSegPerShare, k = c % kSegPerShare;
+    int s, e, sid;
+    if (k == 0) {
+      part.head(w, s, e);
+      sid = w;
+    } else {
+      part.chunk(k - 1, w, s, e);
+      sid = part.nwarps + (k - 1) * part.nwarps + w;
+    }
+    if (e <= s || e <= r.U || s >= r.Uend) return -1;
+    return (static_cast<int64_t>(sid) * 2 + (r.U > s ? 1 : 0)) * kMaxGroup + r.h;
+  };
+  // Batch k of this warp's candidates, one per lane: candidate
+  // sub + wpr * (32 k + lane), so that the row's warps (COOP) share even a
+  // short candidate list.  The overlapping ones are compacted into
+  // s_row[warp] (the result: their lanes).
+  auto gather = [&](const Partition& part, const RowPlan& r, int k) -> unsigned {
+    const int c = sub + wpr * (32 * k + lane);
+    const int64_t pr = c < r.ncand ? piece(part, r, c) : -1;
+    const unsigned valid = __ballot_sync(0xffffffffu, pr >= 0);
+    if (pr >= 0) s_row[warp][__popc(valid & ((1u << lane) - 1))] = pr;
+    return valid;
+  };
+
+  // The CTA's first row and its first batch of candidates depend on the
+  // lengths only: planned before the wait (the partition arithmetic then runs
+  // while the decode grid drains), so that after it the loads go out at once.
+  // Device inputs without publication are checked after the wait and the plan
+  // rebuilt if they changed.  Only the first batch's lane mask stays in a
+  // register across the wait; each lane finds its own piece in s_row again.
+  const int first_base = blockIdx.x * rows_per_cta;
+  RowPlan r{};
+  unsigned valid0 = 0;
+  auto plan_first = [&]() {
+    const Partition part(Hkv * s_P[a.num_seqs], nwarps);
+    r = plan_row(part, first_base + warp / wpr);
+    valid0 = r.work && sub < r.ncand ? gather(part, r, 0) : 0u;
+  };
+  plan_first();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (!published && a.recheck && context_changed(a, s_ctx, kThreads, false)) {
+    context_prefix(a, a.context_lens, s_P, s_ctx, s_warp_sum, kThreads, false);
+    __syncwarp();
+    plan_first();
+  }
+
+  // Every warp of the CTA runs the same number of iterations (barriers inside).
+  for (int base_row = first_base; base_row < rows; base_row += gridDim.x * rows_per_cta) {
+    const int row = base_row + warp / wpr;
+    const bool first = base_row == first_base;
+    const Partition part(Hkv * s_P[a.num_seqs], nwarps);
+    if (!first) r = plan_row(part, row);
+    const bool work = r.work, zero_row = r.zero_row;
+    T* dst = static_cast<T*>(a.out) + static_cast<int64_t>(row) * D + lane * kPer;
     float m = -INFINITY, L = 0.f, o[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) o[k] = 0.f;
     if (work) {
-      const int w0 = U / part.R, ncand = ((Uend - 1) / part.R - w0 + 1) * kSegPerShare;
-      auto piece = [&](int c) -> int64_t {
-        const int w = w0 + c / kSegPerShare, k = c % kSegPerShare;
-        int s, e, sid;
-        if (k == 0) {
-          part.head(w, s, e);
-          sid = w;
-        } else {
-          part.chunk(k - 1, w, s, e);
-          sid = part.nwarps + (k - 1) * part.nwarps + w;
-        }
-        if (e <= s || e <= U || s >= Uend) return -1;
-        return (static_cast<int64_t>(sid) * 2 + (U > s ? 1 : 0)) * kMaxGroup + h;
-      };
-
       // Pieces are folded in with a running log-sum-exp, in batches of up to
       // 32 candidates (this warp's share of them); within a batch the
       // log-sum-exps and the partial rows are loaded together (one round
       // trip), at most kBatch rows in flight.
-      constexpr int kBatch = WIDE ? 16 : 8;
-      for (int base = 32 * sub; base < ncand; base += 32 * wpr) {
-        const int64_t pr = base + lane < ncand ? piece(base + lane) : -1;
-        const unsigned valid = __ballot_sync(0xffffffffu, pr >= 0);
-        const int rank = __popc(valid & ((1u << lane) - 1));
-        if (pr >= 0) s_row[warp][rank] = pr;
+      constexpr int kBatch = WIDE ? 16 : COOP ? 8 : 6;
+      for (int k = 0; sub + wpr * 32 * k < r.ncand; ++k) {
+        unsigned valid;
+        int rank;
+        int64_t pr;
+        if (first && k == 0) {
+          valid = valid0;
+          rank = __popc(valid & ((1u << lane) - 1));
+          pr = (valid >> lane) & 1u ? s_row[warp][rank] : -1;
+        } else {
+          valid = gather(part, r, k);
+          rank = __popc(valid & ((1u << lane) - 1));
+          pr = (valid >> lane) & 1u ? s_row[warp][rank] : -1;
+        }
         const float lse = pr >= 0 ? __ldcg(a.part_lse + pr) : -INFINITY;
         __syncwarp();
         const int cnt = __popc(valid);
