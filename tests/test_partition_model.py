@@ -9,8 +9,9 @@ directly; every other unit leaves one partial per segment that cuts it, in
 slot 0 (the segment's first flush) or 1, and the merge finds them by testing
 the segments of the shares the unit overlaps.  This checks, over random
 shapes, that every block is streamed exactly once and that the merge's
-enumeration finds exactly the partials the decode side writes.  The GPU
-parity tests check the kernels themselves.
+enumeration finds exactly the partials the decode side writes, also when a
+row's candidates are dealt to its warps in interleaved batches of 32 (one
+warp per row, or four).  The GPU parity tests check the kernels themselves.
 """
 import numpy as np
 
@@ -107,6 +108,14 @@ def _check(lens, hkv, nwarps):
             assert u not in complete
             w0 = U // part.R
             ncand = ((Uend - 1) // part.R - w0 + 1) * sps
+            for wpr in (1, 4):  # warp `sub` of the row takes candidates sub + wpr * (32 k + lane)
+                dealt = []
+                for sub in range(wpr):
+                    k = 0
+                    while sub + wpr * 32 * k < ncand:
+                        dealt += [c for c in (sub + wpr * (32 * k + lane) for lane in range(32)) if c < ncand]
+                        k += 1
+                assert sorted(dealt) == list(range(ncand))
             mine = set()
             for c in range(ncand):
                 w, k = w0 + c // sps, c % sps
