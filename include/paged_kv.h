@@ -407,13 +407,17 @@ int paged_kv_selftest_wait(void* stream);
  * Such a read stands in for inputs whose latest writes are not yet visible.
  * After their wait the kernels read block_tables / context_lens again and
  * rebuild what they derived from the stale values, so out and the caches must
- * be exactly what paged_decode_step gives on the real inputs.  Arguments and
- * errors otherwise as paged_decode_step with num_splits = 0. */
+ * be exactly what paged_decode_step gives on the real inputs.  publish != 0:
+ * the decode grid hands its validated lengths to the merge, as a
+ * paged_decode_step outside stream capture does; 0: it does not, as under
+ * capture, and the merge plans from the stale lengths before its own wait and
+ * plans again after it.  Arguments and errors otherwise as paged_decode_step
+ * with num_splits = 0. */
 int paged_kv_selftest_stale_prologue(const void* q, const void* k_new, const void* v_new, void* k_cache,
                                      void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
                                      const int32_t* stale_block_tables, const int32_t* stale_context_lens,
                                      float scale, void* out, void* workspace, size_t workspace_bytes,
-                                     const pkv_dims* dims, void* stream);
+                                     int32_t publish, const pkv_dims* dims, void* stream);
 
 /* Synchronises `stream`, then reads and clears this device's error word.
  * Returns PKV_OK, PKV_ERR_OUT_OF_RANGE, PKV_ERR_TIMEOUT or PKV_ERR_CUDA. */

@@ -88,7 +88,8 @@ _SIGNATURES = {
                                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                         ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
-                                                        ctypes.c_size_t, ctypes.POINTER(PkvDims), ctypes.c_void_p]),
+                                                        ctypes.c_size_t, ctypes.c_int32, ctypes.POINTER(PkvDims),
+                                                        ctypes.c_void_p]),
     "paged_kv_check_status": (ctypes.c_int, [ctypes.c_void_p]),
     "paged_kv_last_error": (ctypes.c_char_p, []),
     "paged_kv_slot_mapping": (ctypes.c_int, [c_int32_p, c_int32_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,

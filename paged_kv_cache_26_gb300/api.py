@@ -490,10 +490,13 @@ def paged_kv_selftest_stale_prologue(q: torch.Tensor, k_new: torch.Tensor, v_new
                                      context_lens: torch.Tensor, stale_block_tables: torch.Tensor,
                                      stale_context_lens: torch.Tensor, scale: float,
                                      out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                                     stream=None) -> torch.Tensor:
+                                     stream=None, publish: bool = True) -> torch.Tensor:
     """paged_decode_step (automatic path) whose kernels read the stale
     tables / lengths before their grid wait, as if the real ones were still
-    being written: the result must be that of the real inputs.  Returns out."""
+    being written: the result must be that of the real inputs.  With publish
+    False the decode grid does not hand its validated lengths to the merge
+    (as under stream capture), so the merge rebuilds its own plan after its
+    wait.  Returns out."""
     for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache), ("v_cache", v_cache)):
         _need_cuda(n, t, k_cache.dtype)
     for n, t in (("block_tables", block_tables), ("context_lens", context_lens),
@@ -515,7 +518,7 @@ def paged_kv_selftest_stale_prologue(q: torch.Tensor, k_new: torch.Tensor, v_new
     _check(lib().paged_kv_selftest_stale_prologue(
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         _ptr(stale_block_tables), _ptr(stale_context_lens), float(scale), _ptr(out), _ptr(workspace), ws_bytes,
-        ctypes.byref(dims), _stream(stream)), "paged_kv_selftest_stale_prologue")
+        1 if publish else 0, ctypes.byref(dims), _stream(stream)), "paged_kv_selftest_stale_prologue")
     return out
 
 

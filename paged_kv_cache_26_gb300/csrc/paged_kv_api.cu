@@ -341,7 +341,7 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, void* k_cac
                 int32_t num_splits, void* workspace, size_t workspace_bytes, const pkv_dims* d,
                 cudaStream_t stream, bool f8 = false, const float* k_scale = nullptr,
                 const float* v_scale = nullptr, bool pdl = true, const int32_t* pre_lens = nullptr,
-                const int32_t* pre_tables = nullptr, bool recheck = true) {
+                const int32_t* pre_tables = nullptr, bool recheck = true, bool publish = true) {
   int rc = check_dims(d, true);
   if (rc != PKV_OK) return rc;
   if (f8) {
@@ -398,7 +398,7 @@ int decode_impl(const void* q, const void* k_new, const void* v_new, void* k_cac
   args.pub = wl.pub_bytes ? reinterpret_cast<int32_t*>(ws + wl.o_bytes + wl.lse_bytes) : nullptr;
   args.sched = wl.sched_bytes ? reinterpret_cast<int32_t*>(ws + wl.o_bytes + wl.lse_bytes + wl.pub_bytes) : nullptr;
   args.epoch = 0;
-  if (recheck && plan.persistent && args.pub) {
+  if (recheck && publish && plan.persistent && args.pub) {
     // A new tag per call, so that a merge never takes an earlier call's
     // publication for its own; 0 (no publication: the merge re-reads the
     // lengths itself) while the stream is being captured, since a graph
@@ -980,13 +980,13 @@ int paged_kv_selftest_stale_prologue(const void* q, const void* k_new, const voi
                                      void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
                                      const int32_t* stale_block_tables, const int32_t* stale_context_lens,
                                      float scale, void* out, void* workspace, size_t workspace_bytes,
-                                     const pkv_dims* dims, void* stream) {
+                                     int32_t publish, const pkv_dims* dims, void* stream) {
   if (!stale_block_tables || !stale_context_lens || !aligned(stale_block_tables, 4) ||
       !aligned(stale_context_lens, 4))
     return pkv_fail(PKV_ERR_INVALID_ARG, "selftest_stale_prologue: stale inputs missing or misaligned");
   return decode_impl(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, out, 0, workspace,
                      workspace_bytes, dims, static_cast<cudaStream_t>(stream), false, nullptr, nullptr, true,
-                     stale_context_lens, stale_block_tables);
+                     stale_context_lens, stale_block_tables, true, publish != 0);
 }
 
 int paged_kv_append_fp8(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t num_tokens,

@@ -143,8 +143,9 @@ def _stale_case(seed):
     return w
 
 
+@pytest.mark.parametrize("publish", [True, False], ids=["published", "merge_rechecks"])
 @pytest.mark.parametrize("kind", ["lengths_and_tables", "tables_only", "garbage"])
-def test_stale_prologue_inputs_are_rebuilt_after_the_wait(kind):
+def test_stale_prologue_inputs_are_rebuilt_after_the_wait(kind, publish):
     w = _stale_case(11)
     dev = torch.device("cuda")
     rk, rv = oracle_caches(w)
@@ -164,7 +165,7 @@ def test_stale_prologue_inputs_are_rebuilt_after_the_wait(kind):
     kc, vc = w.k_cache[0].clone(), w.v_cache[0].clone()
     out = pkv.paged_kv_selftest_stale_prologue(
         w.q[0], w.k_new[0], w.v_new[0], kc, vc, bt, cl, torch.from_numpy(stale_bt).to(dev),
-        torch.from_numpy(stale_cl).to(dev), w.scale)
+        torch.from_numpy(stale_cl).to(dev), w.scale, publish=publish)
     pkv.paged_kv_check_status()  # raises if a stale value was flagged
     assert np.array_equal(bits(kc), rk) and np.array_equal(bits(vc), rv)
     rows = [(b, h) for b in range(w.spec.batch) for h in range(w.spec.num_q_heads)]
