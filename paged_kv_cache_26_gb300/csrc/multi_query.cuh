@@ -244,7 +244,7 @@ struct WarpAttnRows {
   static constexpr int kNTiles = D / 8;
   static constexpr int kTok = 16 * NSUB;
   static constexpr float kLazy = 8.f;
-  static constexpr float kLoShare = 0.125f;
+  static constexpr float kLoShare = 0.25f;
   float o[kNTiles][4];
   float m0, m1, l0, l1;
 
