@@ -567,7 +567,8 @@ def run_ours(args, rank, world, local):
                                 + (" + merge_split_kernel" if splits > 1 else "")),
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": ncu_traffic(s.name + ("_fp8" if fp8 else "")),
-                     "bytes_per_launch": step_bytes // nl, "avg_launch_us": round(step_s * 1e6, 2),
+                     "bytes_per_launch": step_bytes // nl, "attention_bytes_per_launch": attn_b // nl,
+                     "append_bytes_per_launch": app_b // nl, "avg_launch_us": round(step_s * 1e6, 2),
                      "isolated_call_us": round(call_avg_s * 1e6, 2),
                      "isolated_call_us_p10_p50_p90": [round(float(x) * 1e3, 2)
                                                       for x in np.percentile(call_ms, [10, 50, 90])]},
